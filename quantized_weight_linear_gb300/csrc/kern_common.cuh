@@ -1,0 +1,187 @@
+// Device helpers shared by the libqlin kernels (sm_103a).
+//
+// * mbarrier waits are bounded: after kSpinLimit polls a waiter records kStatusTimeout in
+//   the workspace status word and gives up, so a broken pipeline ends with an error the
+//   host can read instead of a hung GPU.
+// * Bulk copies use the non-tensor cp.async.bulk (TMA engine, 16-byte granularity) with
+//   mbarrier transaction counts.
+// * Launches use programmatic dependent launch: a kernel may start streaming weights while
+//   the previous kernel on the stream drains, and waits (griddepcontrol.wait) before it
+//   touches activations, outputs or workspace.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qlin_internal.h"
+
+namespace qlin {
+
+constexpr uint32_t kSpinLimit = 1u << 21;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on the phase with the given parity.  Returns false after `limit` polls and
+// records the timeout in *status (if non-null).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
+                                          uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= 64) __nanosleep(64);
+  }
+  if (status) atomicExch(status, kStatusTimeout);
+  return false;
+}
+
+// global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16_4(float& d0, float& d1, float& d2, float& d3, const uint32_t (&a)[4],
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A(16x16 f16) * B(16x8 f16), fp32 accumulate
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  return (a & mask) | orv;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 r = __hsub2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 z = *reinterpret_cast<__nv_bfloat162*>(&c);
+  __nv_bfloat162 r = __hfma2(x, y, z);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a);
+  __half2 y = *reinterpret_cast<__half2*>(&b);
+  __half2 r = __hsub2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint16_t f2bf(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ float bf2f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+__device__ __forceinline__ float h2f_dev(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+
+// Static split of `units` work units over `grid` CTAs: CTA c owns [start(c), start(c+1)).
+__device__ __forceinline__ int64_t split_start(int64_t c, int64_t units, int64_t grid) {
+  return c * units / grid;
+}
+// The CTA whose range contains unit u.
+__device__ __forceinline__ int64_t split_owner(int64_t u, int64_t units, int64_t grid) {
+  return ((u + 1) * grid - 1) / units;
+}
+
+// Cross-CTA completion of a row group split over several CTAs.  Every contributor stores
+// its partial sums (64 rows x 16 tokens, fp32 or int32 bits) into its slot
+// partials[(cta * 2 + side) * 1024 ...], then counts itself on counters[rg]; the last one
+// sums all slots in CTA order (deterministic) and writes the row group.  The counter is
+// reset to 0 by the last contributor so the next forward starts clean.
+struct SplitInfo {
+  int64_t first_cta, last_cta;
+};
+
+__device__ __forceinline__ SplitInfo split_info(int64_t rg, int64_t per_rg, int64_t units, int64_t grid) {
+  SplitInfo s;
+  s.first_cta = split_owner(rg * per_rg, units, grid);
+  s.last_cta = split_owner(rg * per_rg + per_rg - 1, units, grid);
+  return s;
+}
+
+__device__ __forceinline__ int split_side(int64_t cta, int64_t rg, int64_t per_rg, int64_t units, int64_t grid) {
+  const int64_t first_rg = split_start(cta, units, grid) / per_rg;
+  return rg == first_rg ? 0 : 1;
+}
+
+}  // namespace qlin

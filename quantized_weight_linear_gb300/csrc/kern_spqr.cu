@@ -1,0 +1,433 @@
+// SpQR decode GEMV (1 <= M <= 16): Y = X (D + S)^T, dense 3-bit bi-level part D and fp16
+// outliers S applied in the same pass.
+//
+// SpQR page ("Makale Bülteni — SpQR", "İddia ve Gerçeklik: SpQR"): the kernel unpacks the
+// dense 3-bit codes while it runs the sparse fp16 product, and the page warns that
+// register pressure and warp divergence are the cost of the hybrid.  Design here:
+//
+// * same persistent weight stream as the W4 kernel: one CTA per SM, equal contiguous
+//   ranges of (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group
+//   statistics and fp16 supergroup statistics), a producer warp with cp.async.bulk into a
+//   6-deep ring, the unit's outlier bucket and X slice staged alongside;
+// * code words hold five 3-bit fields per 16-bit half; one AND/OR turns a field pair into
+//   bf16 (base + q) with base 128 or 16 depending on the field, no shifts for 2 of 5;
+// * M == 1: the eight MMA columns carry eight different 16-groups (block-diagonal B), so
+//   each accumulator is one (row, group) partial sum of exact integer products; the
+//   bi-level statistics are applied once per (row, group) in fp32:
+//     y += s^_g * (sum (base + q) x - sum base x - z^_g * sum x)
+//   and every (row, group) pair belongs to exactly one thread (no redundant decoding);
+// * M >= 2: the same A pairs are dequantized to bf16 s^ (q - z^) in registers and the
+//   MMA columns carry the tokens;
+// * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
+//   fp16 value) and adds value * x[k] into per-row shared accumulators.
+#include "kern_decode_common.cuh"
+
+namespace qlin {
+namespace {
+
+constexpr int kStagesSp = 6;
+constexpr int kXStrideSp = 264;    // 256 bf16 + 8 pad
+constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
+constexpr int kOffsCap = 4096 + 16;  // offsets staged per CTA
+
+template <int XR>  // staged X rows (1 for the M == 1 kernel, 8 or 16 otherwise)
+struct SpSmem {
+  __align__(16) uint8_t unit[kStagesSp][kSpqrUnitBytes];
+  __align__(16) uint16_t x[kStagesSp][XR][kXStrideSp];
+  __align__(16) uint32_t out[kStagesSp][kOutCap + 8];
+  __align__(16) uint32_t offs[kOffsCap];
+  __align__(16) uint32_t zeros[8];
+  float rowacc[4][16][XR];
+  uint64_t full[kStagesSp];
+  uint64_t empty[kStagesSp];
+  uint64_t offs_bar;
+  uint64_t cons_bar;
+  int flag;
+};
+
+// bucket bounds of unit u, row tile rt, from the staged offsets
+struct OffsView {
+  const uint32_t* s;
+  int64_t base;  // global index of s[0]
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const { return s[i - base]; }
+};
+
+// A register pair for MMA j, register r, from the lane's six code words (bf16 base + q).
+template <int J, int R>
+__device__ __forceinline__ uint32_t spqr_pair(const uint32_t (&w)[6]) {
+  if constexpr (J <= 4) {
+    constexpr int i = 4 * J + R;
+    if constexpr (i < 18) {
+      constexpr int wi = i / 3, f = (i % 3) * 2;
+      return lop_and_or(w[wi] >> (3 * f), 0x00070007u, 0x43004300u);
+    } else {
+      constexpr int b = 3 * (i - 18);
+      return ((w[b] >> 15) & 0x00010001u) | ((w[b + 1] >> 14) & 0x00020002u) |
+             ((w[b + 2] >> 13) & 0x00040004u) | 0x43004300u;
+    }
+  } else {
+    constexpr int i = 4 * (J - 5) + R;
+    constexpr int wi = i / 2, f = (i % 2) * 2 + 1;
+    return lop_and_or(w[wi] >> (3 * (f - 1)), 0x00380038u, 0x41804180u);
+  }
+}
+
+template <int J>
+__device__ __forceinline__ void spqr_frag(const uint32_t (&w)[6], uint32_t (&a)[4]) {
+  a[0] = spqr_pair<J, 0>(w);
+  a[1] = spqr_pair<J, 1>(w);
+  a[2] = spqr_pair<J, 2>(w);
+  a[3] = spqr_pair<J, 3>(w);
+}
+
+// 6-bit (qs, qz) entry of (row r_in_tile, group gb in block) from the block's 96-byte field area
+__device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int gb) {
+  const int lane = 4 * (r & 7) + (gb >> 1);
+  const int i = ((r >> 3) << 1) | (gb & 1);
+  const int bit = 24 * lane + 6 * i;
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(area);
+  const uint32_t lo = wp[bit >> 5], hi = wp[(bit >> 5) + 1];
+  return __funnelshift_r(lo, hi, bit & 31) & 63u;
+}
+
+template <int MODE, int MT>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT
+__global__ void __launch_bounds__(160, 1)
+    spqr_decode_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
+  constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SpSmem<XR>& sm = *reinterpret_cast<SpSmem<XR>*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t grid = gridDim.x, cta = blockIdx.x;
+  const int64_t S = v.S, U = (int64_t)v.RG * S;
+  const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
+  const int n_units = (int)(u1 - u0);
+  // staged offsets: global indices [4 u0, 4 u1] (aligned down to 16 bytes)
+  const int64_t off_base = (u0 * 4) & ~int64_t(3);
+  const int64_t off_end = (u1 * 4 + 1 + 3) & ~int64_t(3);
+  const OffsView offs{sm.offs, off_base};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesSp; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 4);
+    }
+    mbar_init(&sm.offs_bar, 1);
+    mbar_init(&sm.cons_bar, 128);
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  {
+    uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0][0]);
+    for (int i = threadIdx.x; i < kStagesSp * XR * kXStrideSp / 2; i += blockDim.x) xz[i] = 0u;
+    if (threadIdx.x < 8) sm.zeros[threadIdx.x] = 0u;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (warp == 4) {
+    if (lane != 0) return;
+    mbar_arrive_expect_tx(&sm.offs_bar, (uint32_t)(off_end - off_base) * 4);
+    bulk_g2s(sm.offs, v.offs + off_base, (uint32_t)(off_end - off_base) * 4, &sm.offs_bar);
+    if (!mbar_wait(&sm.offs_bar, 0, ws.status)) return;
+    const uint32_t xbytes = kSpqrSuper * 2;
+    auto weights = [&](int s, int64_t u) -> uint32_t {  // returns bytes issued
+      bulk_g2s(sm.unit[s], v.units + u * (int64_t)kSpqrUnitBytes, kSpqrUnitBytes, &sm.full[s]);
+      const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
+      uint32_t bytes = kSpqrUnitBytes;
+      if (e1 - e0 <= (uint32_t)kOutCap && e1 > e0) {
+        const uint32_t a0 = e0 & ~3u, a1 = (e1 + 3u) & ~3u;
+        bulk_g2s(sm.out[s], v.ents + a0, (a1 - a0) * 4, &sm.full[s]);
+        bytes += (a1 - a0) * 4;
+      }
+      return bytes;
+    };
+    auto out_bytes = [&](int64_t u) -> uint32_t {
+      const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
+      if (e1 - e0 <= (uint32_t)kOutCap && e1 > e0) return (((e1 + 3u) & ~3u) - (e0 & ~3u)) * 4;
+      return 0u;
+    };
+    const int xm = MODE == 1 ? 1 : M;
+    auto load_x = [&](int s, int64_t u) {
+      const int64_t k0 = (u % S) * kSpqrSuper;
+      for (int m = 0; m < xm; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+    };
+    const int pro = n_units < kStagesSp ? n_units : kStagesSp;
+    for (int i = 0; i < pro; ++i) {
+      mbar_arrive_expect_tx(&sm.full[i], kSpqrUnitBytes + out_bytes(u0 + i) + (uint32_t)xm * xbytes);
+      weights(i, u0 + i);
+    }
+    pdl_wait();
+    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = kStagesSp; i < n_units; ++i) {
+      const int s = i % kStagesSp;
+      const uint32_t ph = (uint32_t)(i / kStagesSp) & 1u;
+      if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
+      mbar_arrive_expect_tx(&sm.full[s], kSpqrUnitBytes + out_bytes(u0 + i) + (uint32_t)xm * xbytes);
+      weights(s, u0 + i);
+      load_x(s, u0 + i);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  pdl_wait();
+  const int g = lane >> 2, t = lane & 3;
+  const int rt = warp;
+  ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
+  if (!mbar_wait(&sm.offs_bar, 0, ws.status)) return;
+  constexpr int NACC = (MODE == 1) ? 4 : 4 * MT;
+  float acc[NACC];
+#pragma unroll
+  for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
+  for (int i = lane; i < 16 * XR; i += 32) (&sm.rowacc[rt][0][0])[i] = 0.f;
+  __syncwarp();
+  int64_t cur_rg = u0 / S;
+
+  auto flush = [&](int64_t rg) -> bool {
+    __syncwarp();
+    if constexpr (MODE == 1) {
+      float r0 = acc[0] + acc[1], r1 = acc[2] + acc[3];
+      r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+      r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+      r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+      r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+      float vals[2] = {r0 + sm.rowacc[rt][g][0], r1 + sm.rowacc[rt][g + 8][0]};
+      int idx[2] = {t == 0 ? (rt * 16 + g) * 16 : -1, t == 0 ? (rt * 16 + g + 8) * 16 : -1};
+      auto done = [&](const float (&out)[2]) {
+        for (int j = 0; j < 2; ++j) {
+          if (idx[j] < 0) continue;
+          const int64_t n = rg * kRowGroup + idx[j] / 16;
+          if (n < v.N) Y[n] = f2bf(out[j]);
+        }
+      };
+      return finish_row_group<float, 2>(rg, S, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+    } else {
+      float vals[NACC];
+      int idx[NACC];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = g + ((i & 2) ? 8 : 0);
+          const int m = 2 * t + (i & 1) + 8 * mt;
+          const bool ok = m < M;
+          vals[mt * 4 + i] = acc[mt * 4 + i] + (ok ? sm.rowacc[rt][r][m] : 0.f);
+          idx[mt * 4 + i] = ok ? (rt * 16 + r) * 16 + m : -1;
+        }
+      auto done = [&](const float (&out)[NACC]) {
+#pragma unroll
+        for (int j = 0; j < NACC; ++j) {
+          if (idx[j] < 0) continue;
+          const int64_t n = rg * kRowGroup + idx[j] / 16;
+          const int m = idx[j] % 16;
+          if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+        }
+      };
+      return finish_row_group<float, NACC>(rg, S, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+    }
+  };
+
+  for (int it = 0; it < n_units; ++it) {
+    const int s = it % kStagesSp;
+    const uint32_t ph = (uint32_t)(it / kStagesSp) & 1u;
+    const int64_t u = u0 + it;
+    const int64_t rg = u / S;
+    if (rg != cur_rg) {
+      if (!flush(cur_rg)) return;
+#pragma unroll
+      for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
+      __syncwarp();
+      for (int i = lane; i < 16 * XR; i += 32) (&sm.rowacc[rt][0][0])[i] = 0.f;
+      __syncwarp();
+      cur_rg = rg;
+    }
+    if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
+    const uint8_t* unit = sm.unit[s];
+    const uint16_t* sgst = reinterpret_cast<const uint16_t*>(unit + kSpqrCodeBytes + kSpqrQsqzBytes);
+    const uint16_t* ra = sgst + (rt * 16 + g) * 4;
+    const uint16_t* rb = sgst + (rt * 16 + g + 8) * 4;
+    const float ssA = h2f_dev(ra[0]), zsA = h2f_dev(ra[1]), szA = h2f_dev(ra[2]), zzA = h2f_dev(ra[3]);
+    const float ssB = h2f_dev(rb[0]), zsB = h2f_dev(rb[1]), szB = h2f_dev(rb[2]), zzB = h2f_dev(rb[3]);
+
+    if constexpr (MODE == 1) {
+      // per-group X sums of the unit: lane l covers group l/2, half l%2
+      const uint16_t* x0 = &sm.x[s][0][0];
+      float sa = 0.f, sb = 0.f;
+      {
+        const int gl = lane >> 1, h = lane & 1;
+        const uint4 xv = *reinterpret_cast<const uint4*>(x0 + gl * 16 + h * 8);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xf = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+          if (h * 8 + e < 10) sa += xf; else sb += xf;
+        }
+        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      }
+      const float bsum = 128.f * sa + 16.f * sb, xsum = sa + sb;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
+        uint32_t w[6];
+        {
+          const uint2 p0 = *reinterpret_cast<const uint2*>(cw);
+          const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
+          const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
+          w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
+        }
+        const uint16_t* xb = x0 + blk * 128 + 16 * g;
+        const uint32_t* pb0 = (g == t) ? reinterpret_cast<const uint32_t*>(xb) : sm.zeros;
+        const uint32_t* pb1 = (g == t + 4) ? reinterpret_cast<const uint32_t*>(xb) : sm.zeros;
+        const uint4 bx0 = *reinterpret_cast<const uint4*>(pb0);
+        const uint4 bx1 = *reinterpret_cast<const uint4*>(pb1);
+        const uint4 by0 = *reinterpret_cast<const uint4*>(pb0 == sm.zeros ? sm.zeros : pb0 + 4);
+        const uint4 by1 = *reinterpret_cast<const uint4*>(pb1 == sm.zeros ? sm.zeros : pb1 + 4);
+        const uint32_t b0v[8] = {bx0.x, bx0.y, bx0.z, bx0.w, by0.x, by0.y, by0.z, by0.w};
+        const uint32_t b1v[8] = {bx1.x, bx1.y, bx1.z, bx1.w, by1.x, by1.y, by1.z, by1.w};
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4];
+        spqr_frag<0>(w, a); mma_bf16(c, a, b0v[0], b1v[0]);
+        spqr_frag<1>(w, a); mma_bf16(c, a, b0v[1], b1v[1]);
+        spqr_frag<2>(w, a); mma_bf16(c, a, b0v[2], b1v[2]);
+        spqr_frag<3>(w, a); mma_bf16(c, a, b0v[3], b1v[3]);
+        spqr_frag<4>(w, a); mma_bf16(c, a, b0v[4], b1v[4]);
+        spqr_frag<5>(w, a); mma_bf16(c, a, b0v[5], b1v[5]);
+        spqr_frag<6>(w, a); mma_bf16(c, a, b0v[6], b1v[6]);
+        spqr_frag<7>(w, a); mma_bf16(c, a, b0v[7], b1v[7]);
+        // group sums of the two accumulator groups 2t, 2t+1 of this block
+        const int l0 = 2 * (blk * 8 + 2 * t);
+        const float B0 = __shfl_sync(0xffffffffu, bsum, l0), S0 = __shfl_sync(0xffffffffu, xsum, l0);
+        const float B1 = __shfl_sync(0xffffffffu, bsum, l0 + 2), S1 = __shfl_sync(0xffffffffu, xsum, l0 + 2);
+        const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(qarea);
+        const int bit = 24 * lane;
+        const uint32_t f24 = __funnelshift_r(qw[bit >> 5], qw[(bit >> 5) + 1], bit & 31);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float qs = (float)((f24 >> (6 * i)) & 7u), qz = (float)((f24 >> (6 * i + 3)) & 7u);
+          const float ss = i < 2 ? ssA : ssB, zs = i < 2 ? zsA : zsB;
+          const float sz = i < 2 ? szA : szB, zz = i < 2 ? zzA : zzB;
+          const float sh = __fmul_rn(__fsub_rn(qs, zs), ss);
+          const float zh = __fmul_rn(__fsub_rn(qz, zz), sz);
+          const float Bg = (i & 1) ? B1 : B0, Sg = (i & 1) ? S1 : S0;
+          acc[i] += sh * (c[i] - Bg - zh * Sg);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
+        uint32_t w[6];
+        {
+          const uint2 p0 = *reinterpret_cast<const uint2*>(cw);
+          const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
+          const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
+          w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
+        }
+        // A-side statistics: (row g, group t), (row g+8, group t), (row g, group t+4), (row g+8, group t+4)
+        const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+        uint32_t sh2[4], ch2[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = g + ((r & 1) ? 8 : 0), gb = t + ((r & 2) ? 4 : 0);
+          const uint32_t e = qsqz_entry(qarea, row, gb);
+          const float ss = (r & 1) ? ssB : ssA, zs = (r & 1) ? zsB : zsA;
+          const float sz = (r & 1) ? szB : szA, zz = (r & 1) ? zzB : zzA;
+          const float sh = __fmul_rn(__fsub_rn((float)(e & 7u), zs), ss);
+          const float zh = __fmul_rn(__fsub_rn((float)(e >> 3), zz), sz);
+          sh2[r] = pack_bf16x2(sh, sh);
+          const float cz = -sh * zh;
+          ch2[r] = pack_bf16x2(cz, cz);
+        }
+        const int kb = blk * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t a[4];
+          switch (j) {
+            case 0: spqr_frag<0>(w, a); break;
+            case 1: spqr_frag<1>(w, a); break;
+            case 2: spqr_frag<2>(w, a); break;
+            case 3: spqr_frag<3>(w, a); break;
+            case 4: spqr_frag<4>(w, a); break;
+            case 5: spqr_frag<5>(w, a); break;
+            case 6: spqr_frag<6>(w, a); break;
+            default: spqr_frag<7>(w, a); break;
+          }
+          const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint16_t* xr = &sm.x[s][g + 8 * mt][0];
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + kb + 16 * t + 2 * j);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + kb + 16 * (t + 4) + 2 * j);
+            mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
+          }
+        }
+      }
+    }
+
+    // outliers of this row tile in this unit
+    {
+      const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
+      const uint32_t b0 = offs(4 * u + rt), b1 = offs(4 * u + rt + 1);
+      const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
+      const uint32_t a0 = e0 & ~3u;
+      for (uint32_t p = b0 + lane; p < b1; p += 32) {
+        const uint32_t e = staged ? sm.out[s][p - a0] : __ldg(v.ents + p);
+        const int r = (int)(e & 15u), k = (int)((e >> 4) & 255u);
+        const float val = h2f_dev((uint16_t)(e >> 16));
+        if constexpr (MODE == 1) {
+          atomicAdd(&sm.rowacc[rt][r][0], val * bf2f(sm.x[s][0][k]));
+        } else {
+          for (int m = 0; m < M; ++m) atomicAdd(&sm.rowacc[rt][r][m], val * bf2f(sm.x[s][m][k]));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+  }
+  if (n_units > 0) flush(cur_rg);
+}
+
+template <int MODE, int MT>
+int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
+                  void* stream) {
+  constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
+  const size_t smem = sizeof(SpSmem<XR>);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(spqr_decode_kernel<MODE, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(160);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT>, v, X, Y, M, ws);
+}
+
+}  // namespace
+
+int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
+                       void* stream) {
+  // every CTA stages its slice of the bucket offsets: keep ranges below kOffsCap entries
+  const int64_t U = (int64_t)v.RG * v.S;
+  const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
+  if (grid < need) grid = (int)need;
+  if (grid > ws.grid) return (int)cudaErrorInvalidValue;
+  if (M == 1) return launch_spqr_t<1, 1>(v, X, Y, M, ws, grid, stream);
+  if (M <= 8) return launch_spqr_t<2, 1>(v, X, Y, M, ws, grid, stream);
+  return launch_spqr_t<2, 2>(v, X, Y, M, ws, grid, stream);
+}
+
+}  // namespace qlin

@@ -1,0 +1,214 @@
+// W4 g128 decode GEMV (1 <= M <= 16): Y[m, n] = sum_k x[m, k] * (q[n, k] - z) * s.
+//
+// GPTQ page ("Makale Bülteni — GPTQ", "İddia ve Gerçeklik: GPTQ"): weight-only 4-bit
+// groups pay off at small batch because the layer is bound by weight bandwidth.  The
+// kernel is therefore a weight stream:
+//
+// * persistent grid of one CTA per SM, each owning an equal, contiguous range of
+//   (64-row group, 128-wide K group) units (4352 bytes of codes + statistics each);
+// * one producer warp streams units with cp.async.bulk into an 8-deep shared-memory
+//   ring (mbarrier full/empty pairs) together with the matching 128-wide slice of X;
+// * four consumer warps (one 16-row tile each) turn code words into bf16 A fragments
+//   with one AND/OR per register pair (bf16 128 + q) and one bf16 subtract of 128 + z,
+//   which leaves the exact integers q - z; mma.sync m16n8k16 accumulates sum (q - z) x in
+//   fp32 per group, and the group's fp16 scale is applied once per group;
+// * a row group split between two CTAs is finished by the last of them (partials in the
+//   workspace, arrival counter), so the split is deterministic.
+#include "kern_decode_common.cuh"
+
+namespace qlin {
+namespace {
+
+constexpr int kStagesW4 = 8;
+constexpr int kXStrideW4 = 136;  // staged X row: 128 bf16 + 8 pad (bank-conflict free B loads)
+
+template <int MT>
+struct W4Smem {
+  __align__(16) uint8_t unit[kStagesW4][kW4UnitBytes];
+  __align__(16) uint16_t x[kStagesW4][8 * MT][kXStrideW4];
+  uint64_t full[kStagesW4];
+  uint64_t empty[kStagesW4];
+  uint64_t cons_bar;
+  int flag;
+};
+
+template <int MT>
+__global__ void __launch_bounds__(160, 1)
+    w4_decode_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t grid = gridDim.x, cta = blockIdx.x;
+  const int64_t G = v.G, U = (int64_t)v.RG * G;
+  const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
+  const int n_units = (int)(u1 - u0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesW4; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 4);
+    }
+    mbar_init(&sm.cons_bar, 128);
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  {
+    uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0][0]);
+    for (int i = threadIdx.x; i < kStagesW4 * 8 * MT * kXStrideW4 / 2; i += blockDim.x) xz[i] = 0u;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (warp == 4) {
+    if (lane != 0) return;
+    const uint32_t xbytes = kW4Group * 2;
+    const uint32_t tx = kW4UnitBytes + (uint32_t)M * xbytes;
+    auto load_x = [&](int s, int64_t u) {
+      const int64_t k0 = (u % G) * kW4Group;
+      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+    };
+    const int pro = n_units < kStagesW4 ? n_units : kStagesW4;
+    for (int i = 0; i < pro; ++i) {
+      mbar_arrive_expect_tx(&sm.full[i], tx);
+      bulk_g2s(sm.unit[i], v.units + (u0 + i) * (int64_t)kW4UnitBytes, kW4UnitBytes, &sm.full[i]);
+    }
+    pdl_wait();  // X is written by the previous kernel on the stream
+    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = kStagesW4; i < n_units; ++i) {
+      const int s = i % kStagesW4;
+      const uint32_t ph = (uint32_t)(i / kStagesW4) & 1u;
+      if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
+      mbar_arrive_expect_tx(&sm.full[s], tx);
+      bulk_g2s(sm.unit[s], v.units + (u0 + i) * (int64_t)kW4UnitBytes, kW4UnitBytes, &sm.full[s]);
+      load_x(s, u0 + i);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  pdl_wait();
+  const int g = lane >> 2, t = lane & 3;
+  ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
+  float acc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+  int64_t cur_rg = u0 / G;
+
+  auto flush = [&](int64_t rg) -> bool {
+    float vals[MT * 4];
+    int idx[MT * 4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
+        const int m = 2 * t + (i & 1) + 8 * mt;
+        vals[mt * 4 + i] = acc[mt][i];
+        idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
+      }
+    auto done = [&](const float (&out)[MT * 4]) {
+#pragma unroll
+      for (int j = 0; j < MT * 4; ++j) {
+        if (idx[j] < 0) continue;
+        const int64_t n = rg * kRowGroup + idx[j] / 16;
+        const int m = idx[j] % 16;
+        if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+      }
+    };
+    return finish_row_group<float, MT * 4>(rg, G, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+  };
+
+  for (int i = 0; i < n_units; ++i) {
+    const int s = i % kStagesW4;
+    const uint32_t ph = (uint32_t)(i / kStagesW4) & 1u;
+    const int64_t rg = (u0 + i) / G;
+    if (rg != cur_rg) {
+      if (!flush(cur_rg)) return;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[mt][q] = 0.f;
+      cur_rg = rg;
+    }
+    if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
+    const uint8_t* unit = sm.unit[s];
+    const uint32_t* st = reinterpret_cast<const uint32_t*>(unit + kW4CodeBytes);
+    const uint32_t sz0 = st[warp * 16 + g], sz1 = st[warp * 16 + g + 8];
+    const float s0 = h2f_dev((uint16_t)(sz0 & 0xFFFFu)), s1 = h2f_dev((uint16_t)(sz1 & 0xFFFFu));
+    const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
+    const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0);
+    const uint32_t zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
+    float c[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[mt][q] = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((warp * 2 + kb) * 32 + lane) * 16);
+      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = words[j];
+        uint32_t a[4];
+        a[0] = bf16x2_sub(lop_and_or(w, 0x000F000Fu, 0x43004300u), zp0);
+        a[1] = bf16x2_sub(lop_and_or(w >> 4, 0x000F000Fu, 0x43004300u), zp1);
+        a[2] = bf16x2_sub(lop_and_or(w >> 8, 0x000F000Fu, 0x43004300u), zp0);
+        a[3] = bf16x2_sub(lop_and_or(w >> 12, 0x000F000Fu, 0x43004300u), zp1);
+        const int kk = kb * 64 + 16 * j + 2 * t;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint16_t* xr = &sm.x[s][g + 8 * mt][0];
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + kk);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + kk + 8);
+          mma_bf16(c[mt], a, b0, b1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      acc[mt][0] += s0 * c[mt][0];
+      acc[mt][1] += s0 * c[mt][1];
+      acc[mt][2] += s1 * c[mt][2];
+      acc[mt][3] += s1 * c[mt][3];
+    }
+  }
+  if (n_units > 0) flush(cur_rg);
+}
+
+template <int MT>
+int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
+                 void* stream) {
+  const size_t smem = sizeof(W4Smem<MT>);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(w4_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(160);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT>, v, X, Y, M, ws);
+}
+
+}  // namespace
+
+int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
+                     void* stream) {
+  if (M <= 8) return launch_w4_mt<1>(v, X, Y, M, ws, grid, stream);
+  return launch_w4_mt<2>(v, X, Y, M, ws, grid, stream);
+}
+
+}  // namespace qlin

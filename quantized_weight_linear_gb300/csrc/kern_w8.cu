@@ -1,0 +1,310 @@
+// SmoothQuant W8A8 decode: per-token activation quantization, then an exact integer GEMV.
+//
+// SmoothQuant page ("Makale Bülteni — SmoothQuant", "İddia ve Gerçeklik: SmoothQuant"):
+// X diag(s)^-1 is quantized per token and diag(s) W per output channel to int8, the
+// product is accumulated in integers and scaled back.
+//
+// Act-quant: x' = x * s_inv (fp32), sx = max|x'| / 127 (1 if 0), q = clamp(rint(x'/sx), +-127),
+// IEEE division and round-half-to-even, one CTA per token.  The forward path stores the
+// codes as fp16 (exact for |q| <= 127) so the GEMV can feed them to the MMA directly.
+//
+// GEMV: Blackwell Ultra's int8 tensor rate is a small fraction of its fp16 rate, so the
+// integer product runs on the fp16 MMA instead: int8 codes are exact in fp16, products
+// (|q| <= 127^2) are exact in fp32, and any sum of at most 1024 of them stays below 2^24,
+// hence exact too.  The kernel drains the fp32 accumulators into int32 every 16 units
+// (1024 K) -- the int32 result equals the integer accumulator bit for bit.  Weight bytes are
+// stored as u = q + 128 in A-fragment order; one byte permute makes fp16 (1024 + u) and one
+// fp16 subtract of 1152 leaves q.  Epilogue y = bf16((fp32(acc) * sx_m) * sw_n).
+#include "kern_decode_common.cuh"
+
+namespace qlin {
+namespace {
+
+constexpr int kStagesW8 = 8;
+constexpr int kXStrideW8 = 72;  // staged qx row: 64 fp16 + 8 pad
+
+template <bool F16OUT>
+__global__ void __launch_bounds__(256)
+    w8_act_quant_kernel(const uint16_t* __restrict__ X, const float* __restrict__ s_inv, int K,
+                        int8_t* __restrict__ q8, uint16_t* __restrict__ q16, float* __restrict__ sx) {
+  __shared__ float red[8];
+  __shared__ float scale_sh;
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int m = blockIdx.x;
+  const uint16_t* xr = X + (int64_t)m * K;
+  float amax = 0.f;
+  for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(xr + k);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+      amax = fmaxf(amax, fabsf(__fmul_rn(x, s_inv[k + e])));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) a = fmaxf(a, red[i]);
+    const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 127.f);
+    scale_sh = sc;
+    sx[m] = sc;
+  }
+  __syncthreads();
+  const float sc = scale_sh;
+  for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(xr + k);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    int qv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+      int q = __float2int_rn(__fdiv_rn(__fmul_rn(x, s_inv[k + e]), sc));
+      qv[e] = q < -127 ? -127 : (q > 127 ? 127 : q);
+    }
+    if constexpr (F16OUT) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 h = __halves2half2(__int2half_rn(qv[2 * e]), __int2half_rn(qv[2 * e + 1]));
+        o[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(q16 + (int64_t)m * K + k) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo |= (uint32_t)(uint8_t)(int8_t)qv[e] << (8 * e);
+        hi |= (uint32_t)(uint8_t)(int8_t)qv[4 + e] << (8 * e);
+      }
+      *reinterpret_cast<uint2*>(q8 + (int64_t)m * K + k) = make_uint2(lo, hi);
+    }
+  }
+}
+
+template <int MT>
+struct W8Smem {
+  __align__(16) uint8_t unit[kStagesW8][kW8UnitBytes];
+  __align__(16) uint16_t x[kStagesW8][8 * MT][kXStrideW8];
+  uint64_t full[kStagesW8];
+  uint64_t empty[kStagesW8];
+  uint64_t cons_bar;
+  int flag;
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(160, 1)
+    w8_decode_kernel(W8View v, const uint16_t* __restrict__ q16, const float* __restrict__ sx,
+                     uint16_t* __restrict__ Y, int32_t* __restrict__ acc_out, int M, Workspace ws) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  W8Smem<MT>& sm = *reinterpret_cast<W8Smem<MT>*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t grid = gridDim.x, cta = blockIdx.x;
+  const int64_t KB = v.KB, U = (int64_t)v.RG * KB;
+  const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
+  const int n_units = (int)(u1 - u0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesW8; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 4);
+    }
+    mbar_init(&sm.cons_bar, 128);
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  {
+    uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0][0]);
+    for (int i = threadIdx.x; i < kStagesW8 * 8 * MT * kXStrideW8 / 2; i += blockDim.x) xz[i] = 0u;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  if (warp == 4) {
+    if (lane != 0) return;
+    const uint32_t xbytes = kW8Block * 2;
+    const uint32_t tx = kW8UnitBytes + (uint32_t)M * xbytes;
+    auto load_x = [&](int s, int64_t u) {
+      const int64_t k0 = (u % KB) * kW8Block;
+      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], q16 + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+    };
+    const int pro = n_units < kStagesW8 ? n_units : kStagesW8;
+    for (int i = 0; i < pro; ++i) {
+      mbar_arrive_expect_tx(&sm.full[i], tx);
+      bulk_g2s(sm.unit[i], v.units + (u0 + i) * (int64_t)kW8UnitBytes, kW8UnitBytes, &sm.full[i]);
+    }
+    pdl_wait();  // the activation codes come from the act-quant kernel
+    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = kStagesW8; i < n_units; ++i) {
+      const int s = i % kStagesW8;
+      const uint32_t ph = (uint32_t)(i / kStagesW8) & 1u;
+      if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
+      mbar_arrive_expect_tx(&sm.full[s], tx);
+      bulk_g2s(sm.unit[s], v.units + (u0 + i) * (int64_t)kW8UnitBytes, kW8UnitBytes, &sm.full[s]);
+      load_x(s, u0 + i);
+    }
+    return;
+  }
+
+  pdl_wait();
+  const int g = lane >> 2, t = lane & 3;
+  ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
+  int32_t iacc[MT][4];
+  float c[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      iacc[mt][i] = 0;
+      c[mt][i] = 0.f;
+    }
+  int since_drain = 0;
+  auto drain = [&]() {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        iacc[mt][i] += __float2int_rn(c[mt][i]);
+        c[mt][i] = 0.f;
+      }
+    since_drain = 0;
+  };
+  int64_t cur_rg = u0 / KB;
+
+  auto flush = [&](int64_t rg) -> bool {
+    drain();
+    int vals[MT * 4];
+    int idx[MT * 4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
+        const int m = 2 * t + (i & 1) + 8 * mt;
+        vals[mt * 4 + i] = iacc[mt][i];
+        idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
+      }
+    auto done = [&](const int (&out)[MT * 4]) {
+#pragma unroll
+      for (int j = 0; j < MT * 4; ++j) {
+        if (idx[j] < 0) continue;
+        const int64_t n = rg * kRowGroup + idx[j] / 16;
+        const int m = idx[j] % 16;
+        if (n >= v.N) continue;
+        if (acc_out) {
+          acc_out[(int64_t)m * v.N + n] = out[j];
+        } else {
+          const float y = __fmul_rn(__fmul_rn(__int2float_rn(out[j]), sx[m]), v.sw[n]);
+          Y[(int64_t)m * v.N + n] = f2bf(y);
+        }
+      }
+    };
+    return finish_row_group<int, MT * 4>(rg, KB, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+  };
+
+  for (int i = 0; i < n_units; ++i) {
+    const int s = i % kStagesW8;
+    const uint32_t ph = (uint32_t)(i / kStagesW8) & 1u;
+    const int64_t rg = (u0 + i) / KB;
+    if (rg != cur_rg) {
+      if (!flush(cur_rg)) return;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) iacc[mt][q] = 0;
+      cur_rg = rg;
+    }
+    if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
+    const uint8_t* unit = sm.unit[s] + (warp * 32 + lane) * 32;
+    const uint4 w01 = *reinterpret_cast<const uint4*>(unit);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(unit + 16);
+    const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+    const uint32_t magic = 0x64646464u, off = 0x64806480u;  // fp16 1152 = 1024 + 128
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t a[4];
+      a[0] = f16x2_sub(prmt(words[2 * j], magic, 0x5140u), off);
+      a[1] = f16x2_sub(prmt(words[2 * j], magic, 0x5342u), off);
+      a[2] = f16x2_sub(prmt(words[2 * j + 1], magic, 0x5140u), off);
+      a[3] = f16x2_sub(prmt(words[2 * j + 1], magic, 0x5342u), off);
+      const int kk = 16 * j + 2 * t;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint16_t* xr = &sm.x[s][g + 8 * mt][0];
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + kk);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + kk + 8);
+        mma_f16(c[mt], a, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    if (++since_drain == 16) drain();
+  }
+  if (n_units > 0) flush(cur_rg);
+}
+
+template <int MT>
+int launch_w8_mt(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc, int M,
+                 const Workspace& ws, int grid, void* stream) {
+  const size_t smem = sizeof(W8Smem<MT>);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(w8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(160);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, w8_decode_kernel<MT>, v, q16, sx, Y, acc, M, ws);
+}
+
+template <bool F16>
+int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, float* sx, int M, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx);
+}
+
+}  // namespace
+
+int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M, void* stream) {
+  return launch_aq<false>(v, X, qx, nullptr, sx, M, stream);
+}
+
+int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int M, void* stream) {
+  return launch_aq<true>(v, X, nullptr, q16, sx, M, stream);
+}
+
+int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc_out, int M,
+                     const Workspace& ws, int grid, void* stream) {
+  if (M <= 8) return launch_w8_mt<1>(v, q16, sx, Y, acc_out, M, ws, grid, stream);
+  return launch_w8_mt<2>(v, q16, sx, Y, acc_out, M, ws, grid, stream);
+}
+
+}  // namespace qlin

@@ -24,3 +24,13 @@ def cuda_available() -> bool:
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def qlin():
+    """The product binding with libqlin.so built in-tree (nvcc cross-compiles without a GPU)."""
+    from quantized_weight_linear_gb300.build import build
+    build()
+    import quantized_weight_linear_gb300 as q
+    q.lib()
+    return q

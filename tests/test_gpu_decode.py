@@ -1,0 +1,175 @@
+"""GPU parity of the decode (M <= 16) path against the oracle, through the C ABI.
+
+Bars (stated target): dequantized weights, int8 codes and int32 accumulators bit-exact;
+bf16 outputs within 1e-2 * sum_k |x_k w_k| + 1 bf16 ulp of the fp64 oracle.
+"""
+import numpy as np
+import pytest
+
+import qlin_synth as synth
+from oracle import forward, gptq_w4, smoothquant, spqr
+from oracle.fp import bits_to_f32, bf16_round
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _y(layer, X, M):
+    Xd = _dev(X).view(torch.bfloat16)
+    Y = layer(Xd)
+    torch.cuda.synchronize()
+    assert layer.poll_status() == 0
+    return bits_to_f32(Y.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def _check(y, x_bits, w_hat):
+    y_ref, bound = forward.reference(bits_to_f32(x_bits), w_hat)
+    ok, worst = forward.within_tolerance(y, y_ref, bound)
+    assert ok, f"worst |err|/tol = {worst}"
+    return worst
+
+
+# ----------------------------------------------------------------------------- W4 g128
+
+@pytest.mark.parametrize("N,K", [(256, 1024), (100, 512), (64, 128)])
+def test_w4_device_dequant_bit_exact(qlin, N, K):
+    W = synth.normal(11, synth.KEY_W, 0.02, (N, K))
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    wd = layer.dequant_device().cpu().numpy()
+    ref = gptq_w4.pack(W)["w_hat"]
+    assert np.array_equal(wd.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(256, 1024), (100, 512), (1000, 2048)])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_w4_forward_tolerance(qlin, N, K, M):
+    W, X = synth.gptq_layer(N, K, M, seed=M)
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    _check(_y(layer, X, M), X, gptq_w4.pack(W)["w_hat"])
+
+
+def test_w4_one_hot_rows_bit_exact(qlin):
+    N, K = 192, 512
+    W = synth.normal(5, synth.KEY_W, 0.02, (N, K))
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    w_hat = gptq_w4.pack(W)["w_hat"]
+    ks = [0, 1, 7, 8, 9, 127, 128, 300, 511]
+    X = np.zeros((len(ks), K), dtype=np.float32)
+    for i, k in enumerate(ks):
+        X[i, k] = 1.0
+    y = _y(layer, synth.f32_to_bf16(X), len(ks))
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], bf16_round(w_hat[:, k]))
+
+
+# ----------------------------------------------------------------------------- SpQR
+
+@pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (64, 256, 0.0)])
+def test_spqr_device_dequant_bit_exact(qlin, N, K, frac):
+    W = synth.student_t3(13, 0.02, (N, K))
+    layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
+    wd = layer.dequant_device().cpu().numpy()
+    ref = spqr.pack(W, frac)["w_hat"]
+    assert np.array_equal(wd.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (1000, 2048, 0.01)])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
+def test_spqr_forward_tolerance(qlin, N, K, frac, M):
+    W, X = synth.spqr_layer(N, K, M, seed=M)
+    layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
+    _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
+
+
+def test_spqr_one_hot_rows_bit_exact(qlin):
+    N, K = 128, 512
+    W = synth.student_t3(17, 0.02, (N, K))
+    layer = qlin.QLinear.from_spqr(W, 0.02).to("cuda")
+    w_hat = spqr.pack(W, 0.02)["w_hat"]
+    for ks in ([0], [3, 100, 255, 256, 511]):
+        X = np.zeros((len(ks), K), dtype=np.float32)
+        for i, k in enumerate(ks):
+            X[i, k] = 1.0
+        y = _y(layer, synth.f32_to_bf16(X), len(ks))
+        for i, k in enumerate(ks):
+            assert np.array_equal(y[i], bf16_round(w_hat[:, k])), (ks, k)
+
+
+# ----------------------------------------------------------------------------- W8A8
+
+@pytest.mark.parametrize("N,K", [(128, 512), (100, 256), (256, 2048)])
+@pytest.mark.parametrize("M", [1, 7, 16])
+def test_w8a8_codes_accumulators_and_output(qlin, N, K, M):
+    W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=M + 1)
+    layer = qlin.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=16)
+    pk = smoothquant.quantize_weights(W, absmax, 0.85)
+    assert np.array_equal(layer.dequant_device().cpu().numpy(), pk["qw"])
+    x = bits_to_f32(X)
+    qx_ref, sx_ref = smoothquant.quantize_activations(x, pk["s_inv"])
+    Xd = _dev(X).view(torch.bfloat16)
+    qx, sx = layer.act_quant(Xd)
+    assert np.array_equal(qx.cpu().numpy(), qx_ref)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+    acc = layer.forward_acc(Xd).cpu().numpy()
+    acc_ref = smoothquant.accumulate(qx_ref, pk["qw"])
+    assert np.array_equal(acc.astype(np.int64), acc_ref)
+    y = _y(layer, X, M)
+    y_ref = smoothquant.epilogue(acc_ref, sx_ref, pk["sw"])
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_m_zero_is_noop_and_bad_args(qlin):
+    W = synth.normal(0, synth.KEY_W, 0.02, (64, 256))
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    X = torch.zeros((1, 256), dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda")
+    qlin.qlin_forward(layer.handle, X, Y, 0)
+    with pytest.raises(qlin.QlinError) as e:
+        qlin.qlin_forward(layer.handle, X.data_ptr() + 2, Y, 1)   # misaligned X
+    assert e.value.status == qlin.QLIN_ERR_INVALID_ARG
+    unbound = qlin.QLinear.from_w4g128(W)
+    with pytest.raises(qlin.QlinError) as e:
+        qlin.qlin_forward(unbound.handle, X, Y, 1)
+    assert e.value.status == qlin.QLIN_ERR_NOT_BOUND
+
+
+def test_zero_weights_and_zero_activations(qlin):
+    N, K = 64, 512
+    layer = qlin.QLinear.from_spqr(np.zeros((N, K), np.float32), 0.01).to("cuda")
+    X = synth.activations_bf16(0, 2, K)
+    assert np.all(_y(layer, X, 2) == 0)
+    W = synth.normal(0, synth.KEY_W, 0.02, (N, K))
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    assert np.all(_y(layer, np.zeros((3, K), np.uint16), 3) == 0)
+
+
+def test_device_wait_limit_reports_timeout(qlin):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qlin.qlin_debug_wait_timeout(status, 2000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == qlin.QLIN_ERR_TIMEOUT
+    # the context is still usable afterwards
+    W = synth.normal(0, synth.KEY_W, 0.02, (64, 256))
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    assert np.all(np.isfinite(_y(layer, synth.activations_bf16(0, 1, 256), 1)))
+
+
+def test_repeated_forwards_are_deterministic(qlin):
+    # many row groups split across CTAs: counters must return to zero between calls
+    W, X = synth.spqr_layer(2000, 1024, 1, seed=3)
+    layer = qlin.QLinear.from_spqr(W, 0.01).to("cuda")
+    Xd = _dev(X).view(torch.bfloat16)
+    ys = [layer(Xd).clone() for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    assert layer.poll_status() == 0
