@@ -1,0 +1,424 @@
+"""Benchmark of the quantized linear forward on GB300 (one JSON line on rank 0).
+
+Workload (default): the SpQR-style decode layer -- W [11008 x 4096] ~ 0.02 * Student-t(3),
+1% largest |w| kept as fp16 CSR outliers, the rest 3-bit in 16-wide groups with bi-level
+3-bit statistics under fp16 second-level statistics per 16 groups; X bf16 [1 x 4096]
+~ N(0, 1); seed 0.  One step = one forward Y = X (D + S)^T of that layer (the whole hot
+path of the format: dense unpack, bi-level dequant, outlier add, GEMV).
+Metric: weight GB/s = canonical packed weight bytes / time per forward, against the
+measured HBM copy bandwidth.
+
+Timing: W untimed warm-up steps, then exactly K timed steps between a barrier and a
+synchronize on both sides, CUDA events on the stream the kernels run on.  Every step
+reads a different resident copy of the packed layer (copies together > 4x L2), so no
+step hits weights left in L2.  Steps are issued as CUDA-graph replays of R forwards
+(one per copy), linked by programmatic dependent launch.
+
+Also reported: e2e (the same metric through the C-ABI host-buffer call
+qlin_forward_host: pinned X -> device, forward, Y -> pinned host, per step), the roofline
+of the kernel, the oracle timed on the host cores (cpu_baseline), SM clocks sampled
+during the timed region, and a few more configurations ("extra").
+
+--impl reference times the oracle (numpy, host cores) on the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload (the layer
+is row-parallel; replicas need no collective), value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "weight GB/s (% HBM peak) at M=1; TFLOP/TOPS (% tensor peak) at M=4096"
+WORKLOAD = ("SpQR 3-bit g16 bi-level + 1% fp16 CSR outliers, decode M=1, W 11008x4096 ~ 0.02*Student-t(3), "
+            "X ~ N(0,1) bf16, seed 0")
+N_, K_, M_, FRAC = 11008, 4096, 1, 0.01
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _traffic(kernel_key: str):
+    """dram bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f).get(kernel_key)
+        if not d:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, "quantized_weight_linear_gb300", "csrc", d["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
+                return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------------ oracle arm
+
+def _oracle_spqr_forward_time(reps_min: int = 2, budget_s: float = 12.0):
+    """Times the oracle's forward (canonical arrays -> fp64 y) on the host; one thread."""
+    import qlin_synth as synth
+    from oracle import forward, spqr
+    from oracle.fp import bits_to_f32
+
+    W, X = synth.spqr_layer(N_, K_, M_, seed=0)
+    p = spqr.pack(W, FRAC)
+    x = bits_to_f32(X)
+    nbytes = spqr.packed_bytes(N_, K_, int(p["rowptr"][-1]))
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < reps_min or (time.perf_counter() - t_all < budget_s and len(times) < 8):
+        t0 = time.perf_counter()
+        w_hat = spqr.dequantize_canonical(N_, K_, p["codes"], p["qs_bits"], p["qz_bits"], p["stats"], p["rowptr"],
+                                          p["col"], p["val"])
+        forward.reference(x, w_hat)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"full layer 11008x4096 M=1, {len(times)} forwards (canonical arrays -> dequant -> fp64 GEMV), "
+                      f"median {t:.2f} s each, one host thread"}
+
+
+def cpu_baseline_subprocess():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_only"], capture_output=True, text=True,
+                       env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "_work", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+
+class Rotated:
+    """One packed layer, R resident copies, graphs of R forwards."""
+
+    def __init__(self, q, layer, X, R, stream):
+        import torch
+        self.q, self.layer, self.R = q, layer, R
+        self.nb = q.qlin_device_bytes(layer.handle)
+        self.copies = [layer.weights[(-layer.weights.data_ptr()) % 256:][:self.nb]]
+        for _ in range(R - 1):
+            buf = torch.empty(self.nb + 256, dtype=torch.uint8, device="cuda")
+            view = buf[(-buf.data_ptr()) % 256:][:self.nb]
+            view.copy_(self.copies[0])
+            self.copies.append(view)
+            setattr(self, f"_buf{len(self.copies)}", buf)
+        self.X = X
+        self.Y = torch.empty((X.shape[0], layer.N), dtype=torch.bfloat16, device="cuda")
+        self.stream = stream
+
+    def forward(self, i):
+        self.q.qlin_attach(self.layer.handle, self.copies[i % self.R].data_ptr(), self.nb)
+        self.q.qlin_forward(self.layer.handle, self.X, self.Y, self.X.shape[0], self.stream)
+
+    def capture(self):
+        import torch
+        for i in range(self.R):  # warm: sets kernel attributes outside capture
+            self.forward(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(self.R):
+                self.forward(i)
+        torch.cuda.synchronize()
+        self.graph = g
+        return g
+
+
+def _time_steps(rot, steps, warmup, dist_ctx):
+    import torch
+    R = rot.R
+    for _ in range(max(1, math.ceil(warmup / R))):
+        rot.graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // R)
+    steps = reps * R
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    ev0.record(rot.stream)
+    for _ in range(reps):
+        rot.graph.replay()
+    ev1.record(rot.stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    ms = ev0.elapsed_time(ev1)
+    return steps, ms
+
+
+def _e2e(q, layer, rot, M, steps_e2e):
+    import torch
+    Xh = torch.empty((M, layer.K), dtype=torch.bfloat16).pin_memory()
+    Xh.copy_(rot.X.cpu())
+    Yh = torch.empty((M, layer.N), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(rot.X)
+    Yd = torch.empty((M, layer.N), dtype=torch.bfloat16, device="cuda")
+    for i in range(10):
+        q.qlin_attach(layer.handle, rot.copies[i % rot.R].data_ptr(), rot.nb)
+        q.qlin_forward_host(layer.handle, Xh, Yh, Xd, Yd, M, rot.stream)
+    t0 = time.perf_counter()
+    for i in range(steps_e2e):
+        q.qlin_attach(layer.handle, rot.copies[i % rot.R].data_ptr(), rot.nb)
+        q.qlin_forward_host(layer.handle, Xh, Yh, Xd, Yd, M, rot.stream)
+    dt = time.perf_counter() - t0
+    return dt / steps_e2e, M * layer.K * 2, M * layer.N * 2
+
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _extra_configs(q, torch, stream, l2):
+    """cfg0 (W4 g128 4096^2 M=1) and cfg2 (W8A8 4096^2 M=16) on the same timing scheme."""
+    import qlin_synth as synth
+    out = {}
+    try:
+        W, X = synth.gptq_layer(4096, 4096, 1, seed=0)
+        layer = q.QLinear.from_w4g128(W).to("cuda")
+        nbytes = layer.handle.info.packed_bytes
+        R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
+        rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
+        rot.capture()
+        steps, ms = _time_steps(rot, 20000, 200, DistCtx.__new__(_NoDist))
+        out["w4g128_4096x4096_M1"] = {"GB/s": round(nbytes / (ms / steps / 1e3) / 1e9, 1),
+                                      "us_per_forward": round(ms / steps * 1e3, 3), "weight_bytes": nbytes}
+        del rot, layer
+        W, X, absmax, _ = synth.smoothquant_layer(4096, 4096, 16, seed=0)
+        layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=16)
+        nbytes = layer.handle.info.packed_bytes
+        R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
+        rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
+        rot.capture()
+        steps, ms = _time_steps(rot, 20000, 200, DistCtx.__new__(_NoDist))
+        t = ms / steps / 1e3
+        out["w8a8_4096x4096_M16"] = {"GB/s": round(nbytes / t / 1e9, 1), "us_per_forward": round(t * 1e6, 3),
+                                     "TOPS": round(2 * 16 * 4096 * 4096 / t / 1e12, 2), "weight_bytes": nbytes}
+    except Exception as e:  # extra lines must never break the headline
+        out["error"] = repr(e)[:300]
+    return out
+
+
+class _NoDist(DistCtx):
+    def __init__(self):  # pragma: no cover
+        pass
+
+    def barrier(self):
+        pass
+
+
+def run_gpu(args):
+    import torch
+
+    import qlin_synth as synth
+    import quantized_weight_linear_gb300 as q
+    from quantized_weight_linear_gb300.build import build
+
+    dist_ctx = DistCtx()
+    torch.cuda.set_device(dist_ctx.local)
+    if dist_ctx.rank == 0:
+        build()
+    dist_ctx.barrier()
+    q.lib()
+    stream = torch.cuda.Stream()
+    peaks = _peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+
+    W, X = synth.spqr_layer(N_, K_, M_, seed=0)
+    with torch.cuda.stream(stream):
+        layer = q.QLinear.from_spqr(W, FRAC).to("cuda", stream=stream)
+        nbytes = layer.handle.info.packed_bytes
+        R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
+        Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
+        rot = Rotated(q, layer, Xd, R, stream)
+        rot.capture()
+        with ClockSampler(dist_ctx.local) as clk:
+            steps, ms = _time_steps(rot, args.steps, args.warmup, dist_ctx)
+        clocks = clk.summary()
+        st = q.qlin_poll_status(layer.handle, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the timed region")
+        ms_max = dist_ctx.max(ms)
+        t_step = ms_max / steps / 1e3
+        value = dist_ctx.world * nbytes / t_step / 1e9
+        e2e_t, h2d, d2h = _e2e(q, layer, rot, M_, args.e2e_steps)
+        e2e_t = dist_ctx.max(e2e_t)
+        extra = _extra_configs(q, torch, stream, l2) if (dist_ctx.rank == 0 and not args.no_extra) else {}
+
+    achieved = nbytes / (ms / steps / 1e3) / 1e9  # this rank's kernel
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist_ctx.world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32 (3-bit codes, fp16 stats/outliers)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "outlier_frac": FRAC, "weight_bytes": nbytes,
+                   "bits_per_param": round(layer.handle.info.bits_per_param, 4),
+                   "l2": f"inputs larger than L2: {R} resident weight copies rotated "
+                         f"({R * q.qlin_device_bytes(layer.handle) / 1e6:.0f} MB > 4x {l2 / 1e6:.0f} MB L2)",
+                   "issue": f"CUDA graph replays of {R} forwards, programmatic dependent launch between forwards",
+                   "parallelism": f"replicas x{dist_ctx.world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("spqr_decode_m1"),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs: torch copy)",
+                     "kernel": "spqr_decode_kernel<1,1>", "bytes_per_launch": nbytes},
+        "e2e": {"value": round(dist_ctx.world * nbytes / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "call": "qlin_forward_host (pinned host X/Y, stream sync per step)"},
+        "gpu_launches": steps,
+        "clocks": clocks,
+    }
+    if extra:
+        line["extra"] = extra
+    if dist_ctx.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess()
+    if dist_ctx.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist_ctx.close()
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    r = cpu_baseline_subprocess()
+    line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "outlier_frac": FRAC},
+            "cpu_baseline": r,
+            "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=480000)
+    ap.add_argument("--warmup", type=int, default=2400)
+    ap.add_argument("--impl", default="qlin", choices=["qlin", "reference"])
+    ap.add_argument("--e2e-steps", dest="e2e_steps", type=int, default=2000)
+    ap.add_argument("--no-extra", dest="no_extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    ap.add_argument("--_oracle_only", dest="oracle_only", action="store_true")
+    args = ap.parse_args()
+    if args.oracle_only:
+        print(json.dumps(_oracle_spqr_forward_time()))
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -129,6 +129,11 @@ qlin_status qlin_workspace_bytes(qlin_handle h, int max_M, size_t* bytes);
  * alive, so the caller need not wait before returning. */
 qlin_status qlin_bind(qlin_handle h, void* dev_weights, size_t bytes, qlin_stream stream);
 
+/* Points the handle at device memory that already holds its image (for example a
+ * device-to-device copy of a bound image), without copying anything.  Lets one packed
+ * layer run from several resident copies.  Same size/alignment rules as qlin_bind. */
+qlin_status qlin_attach(qlin_handle h, void* dev_weights, size_t bytes);
+
 /* Hands the handle a caller-owned device workspace (256-byte aligned) and clears its
  * counters and status word on `stream`.  max_M is the largest M later forwards will use. */
 qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int max_M,
@@ -176,9 +181,10 @@ const char* qlin_status_string(qlin_status s);
 int qlin_sm_count(void);
 
 /* Test hook for device-side wait limits: launches one block that waits on an mbarrier
- * nothing ever arrives on, with a limit of `spins` polls; the block then records
- * QLIN_ERR_TIMEOUT in status (device int32) and exits cleanly. */
-qlin_status qlin_debug_wait_timeout(int32_t* status, int spins, qlin_stream stream);
+ * nothing ever arrives on, with a wall-time limit of limit_us microseconds (1 .. 10^7); the
+ * block then records QLIN_ERR_TIMEOUT in status (device int32) and exits cleanly.  Every
+ * wait inside the library's kernels has the same kind of limit (2 s). */
+qlin_status qlin_debug_wait_timeout(int32_t* status, int limit_us, qlin_stream stream);
 
 #ifdef __cplusplus
 }

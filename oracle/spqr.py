@@ -63,6 +63,25 @@ def select_outliers(W, frac: float) -> np.ndarray:
     return mask.reshape(N, K)
 
 
+def select_outliers_by_threshold(W, frac: float) -> np.ndarray:
+    """Same set as ``select_outliers`` for large matrices: the nnz-th largest |w| found by
+    partition, every |w| above it taken, and the entries equal to it taken in index order
+    until nnz are chosen."""
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    nnz = outlier_count(N, K, frac)
+    a = np.abs(W).ravel()
+    mask = np.zeros(a.size, dtype=bool)
+    if nnz > 0:
+        T = np.partition(a, a.size - nnz)[a.size - nnz]
+        above = a > T
+        mask |= above
+        need = nnz - int(above.sum())
+        ties = np.flatnonzero(a == T)[:need]
+        mask[ties] = True
+    return mask.reshape(N, K)
+
+
 def pack_bits3(codes) -> np.ndarray:
     """[N, L] 3-bit codes -> uint8 [N, 3L/8] LSB-first bitstream per row."""
     c = np.asarray(codes, dtype=np.uint8)
@@ -81,6 +100,22 @@ def unpack_bits3(stream, L: int) -> np.ndarray:
 def quantize(W, frac: float):
     """Runs readings 1-7.  Returns a dict of intermediate and canonical arrays."""
     W = np.asarray(W, dtype=np.float32)
+    _check_shape(W)
+    return quantize_with_mask(W, select_outliers(W, frac))
+
+
+def quantize_rows(W, frac: float, rows):
+    """Readings 1-7 for a subset of rows of a large matrix: the outlier set is chosen over the
+    whole matrix (reading 1), everything after it is row-local.  Rows come back in the order
+    given, as a smaller layer."""
+    W = np.asarray(W, dtype=np.float32)
+    _check_shape(W)
+    mask = select_outliers_by_threshold(W, frac)
+    rows = np.asarray(rows)
+    return quantize_with_mask(W[rows], mask[rows])
+
+
+def _check_shape(W):
     N, K = W.shape
     if K % SUPER:
         raise ValueError("K must be a multiple of 256")
@@ -88,10 +123,14 @@ def quantize(W, frac: float):
         raise ValueError("K must be <= 32768 (int16 CSR columns)")
     if not np.all(np.isfinite(W)):
         raise ValueError("W must be finite")
+
+
+def quantize_with_mask(W, out_mask):
+    """Readings 2-7 given the outlier mask."""
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
     G = K // GROUP
     S = K // SUPER
-
-    out_mask = select_outliers(W, frac)
 
     # first level over the non-outlier entries of each 16-group
     _, s_g, z_g = rtn.quantize_groups(W.reshape(N * G, GROUP), 3, valid=~out_mask.reshape(N * G, GROUP))

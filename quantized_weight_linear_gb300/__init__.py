@@ -36,7 +36,7 @@ FMT_W8A8 = 3
 #: every entry point include/qlin.h declares
 EXPORTED_SYMBOLS = (
     "qlin_pack_w4g128", "qlin_pack_spqr", "qlin_pack_w8", "qlin_device_bytes", "qlin_workspace_bytes",
-    "qlin_bind", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
+    "qlin_bind", "qlin_attach", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
     "qlin_forward_acc", "qlin_dequant_device", "qlin_poll_status", "qlin_export", "qlin_info",
     "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout",
 )
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "qlin_device_bytes": ([H, ctypes.POINTER(sz)], i32),
             "qlin_workspace_bytes": ([H, i32, ctypes.POINTER(sz)], i32),
             "qlin_bind": ([H, vp, sz, vp], i32),
+            "qlin_attach": ([H, vp, sz], i32),
             "qlin_set_workspace": ([H, vp, sz, i32, vp], i32),
             "qlin_forward": ([H, vp, vp, i32, vp], i32),
             "qlin_forward_host": ([H, vp, vp, vp, vp, i32, vp], i32),
@@ -207,6 +208,10 @@ def qlin_bind(h: Handle, dev_weights, nbytes: int, stream=None):
     _check(lib().qlin_bind(h.ptr, _vp(dev_weights), nbytes, _stream(stream)), "qlin_bind")
 
 
+def qlin_attach(h: Handle, dev_weights, nbytes: int):
+    _check(lib().qlin_attach(h.ptr, _vp(dev_weights), nbytes), "qlin_attach")
+
+
 def qlin_set_workspace(h: Handle, dev_ws, nbytes: int, max_M: int, stream=None):
     _check(lib().qlin_set_workspace(h.ptr, _vp(dev_ws), nbytes, max_M, _stream(stream)), "qlin_set_workspace")
 
@@ -240,8 +245,8 @@ def qlin_sm_count() -> int:
     return lib().qlin_sm_count()
 
 
-def qlin_debug_wait_timeout(status_dev, spins: int, stream=None):
-    _check(lib().qlin_debug_wait_timeout(_vp(status_dev), spins, _stream(stream)), "qlin_debug_wait_timeout")
+def qlin_debug_wait_timeout(status_dev, limit_us: int, stream=None):
+    _check(lib().qlin_debug_wait_timeout(_vp(status_dev), limit_us, _stream(stream)), "qlin_debug_wait_timeout")
 
 
 def qlin_export(h: Handle) -> dict:

@@ -1,8 +1,8 @@
 // Device helpers shared by the libqlin kernels (sm_103a).
 //
-// * mbarrier waits are bounded: after kSpinLimit polls a waiter records kStatusTimeout in
-//   the workspace status word and gives up, so a broken pipeline ends with an error the
-//   host can read instead of a hung GPU.
+// * mbarrier waits are bounded in wall time (%globaltimer, 2 s by default): a waiter that
+//   runs out records kStatusTimeout in the workspace status word and gives up, so a broken
+//   pipeline ends with an error the host can read instead of a hung GPU.
 // * Bulk copies use the non-tensor cp.async.bulk (TMA engine, 16-byte granularity) with
 //   mbarrier transaction counts.
 // * Launches use programmatic dependent launch: a kernel may start streaming weights while
@@ -19,7 +19,6 @@
 
 namespace qlin {
 
-constexpr uint32_t kSpinLimit = 1u << 21;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,13 +60,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on the phase with the given parity.  Returns false after `limit` polls and
-// records the timeout in *status (if non-null).
+// try_wait with an explicit suspend-time hint (ns), so one poll never sleeps longer than that
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on the phase with the given parity: gives up after `limit_ns` of wall time
+// (default 2 s), records the timeout in *status (if non-null) and returns false.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
-                                          uint32_t limit = kSpinLimit) {
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i >= 64) __nanosleep(64);
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 10000u)) return true;
+    if (global_ns() - t0 > limit_ns) break;
   }
   if (status) atomicExch(status, kStatusTimeout);
   return false;

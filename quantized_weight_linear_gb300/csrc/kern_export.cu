@@ -118,7 +118,7 @@ __global__ void w8_export_kernel(W8View v, int8_t* __restrict__ out) {
   }
 }
 
-__global__ void wait_timeout_kernel(int32_t* status, int spins) {
+__global__ void wait_timeout_kernel(int32_t* status, int limit_us) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -127,7 +127,7 @@ __global__ void wait_timeout_kernel(int32_t* status, int spins) {
   __syncthreads();
   if (threadIdx.x == 0) {
     // nothing ever arrives on this barrier: the bounded wait must give up and report it
-    mbar_wait(&bar, 0, status, (uint32_t)spins);
+    mbar_wait(&bar, 0, status, (uint64_t)limit_us * 1000ull);
   }
 }
 
@@ -156,8 +156,8 @@ int launch_w8_export(const W8View& v, int8_t* out, void* stream) {
   return (int)cudaGetLastError();
 }
 
-int launch_debug_wait_timeout(int32_t* status, int spins, void* stream) {
-  wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status, spins);
+int launch_debug_wait_timeout(int32_t* status, int limit_us, void* stream) {
+  wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status, limit_us);
   return (int)cudaGetLastError();
 }
 

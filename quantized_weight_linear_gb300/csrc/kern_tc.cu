@@ -1,0 +1,611 @@
+// Prefill (M > 16) forward on the 5th-generation tensor cores: Y = X . W_hat^T with the
+// weights dequantized on the fly into tcgen05 shared-memory operands.
+//
+// GPTQ page ("İddia ve Gerçeklik: GPTQ") and SmoothQuant page ("Ticari Etki"): when the
+// batch grows the layer becomes compute-bound and the dequantization overhead is what
+// erodes weight-only speedups; W8A8 keeps both operands on the tensor cores.  Design:
+//
+// * CTA tile 128 (tokens, MMA M) x 128 (output rows, MMA N), K in blocks of 64;
+// * warp 0: TMA producer -- X tiles through a 2-D tensor map (128B swizzle) and the packed
+//   weight units of the tile (the same device image the decode kernels stream) through
+//   cp.async.bulk into a packed ring;
+// * warp 1: allocates TMEM and issues tcgen05.mma (kind::f16, bf16 or fp16 operands, fp32
+//   accumulator in TMEM) from one elected thread, committing each k-block back to its
+//   shared-memory stage;
+// * warps 2-5: converters -- turn packed codes into the bf16 / fp16 K-major 128B-swizzled
+//   B operand, then run the epilogue (tcgen05.ld -> bf16 -> Y);
+// * W8A8 only, warps 6-9: exactness drain -- int8 x int8 products are exact in fp16 MMA and
+//   every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (two TMEM
+//   regions, double-buffered) are exact integers; these warps add them into int32 registers
+//   while the MMA runs the next chunk, and write y = bf16((acc * sx) * sw) (or acc).
+// Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kern_common.cuh"
+
+namespace qlin {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kNST = 4;     // A/B operand stages
+constexpr int kNPK = 2;     // packed-weight stages
+constexpr int kTileBytes = kBM * kBK * 2;  // 16 KB, one operand tile
+constexpr int kChunkBlocks = 16;           // W8A8: 16 k-blocks = 1024 K per exact chunk
+
+enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
+
+template <int F>
+struct TcCfg;
+template <>
+struct TcCfg<kW4> {
+  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2;
+  static constexpr uint32_t kAType = 1;  // bf16
+};
+template <>
+struct TcCfg<kSpqr> {
+  static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4;
+  static constexpr uint32_t kAType = 1;
+};
+template <>
+struct TcCfg<kW8> {
+  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1;
+  static constexpr uint32_t kAType = 0;  // fp16
+};
+
+template <int F>
+struct TcSmem {
+  __align__(1024) uint8_t a[kNST][kTileBytes];
+  __align__(1024) uint8_t b[kNST][kTileBytes];
+  __align__(16) uint8_t pk[kNPK][2 * TcCfg<F>::kUnitBytes];
+  uint64_t ab_full[kNST], ab_empty[kNST];
+  uint64_t pk_full[kNPK], pk_empty[kNPK];
+  uint64_t acc_full;
+  uint64_t ch_full[2], ch_empty[2];
+  uint32_t tmem;
+  int abort;
+};
+
+struct TcArgs {
+  const uint8_t* units;   // device image units
+  const uint32_t* offs;   // SpQR bucket offsets
+  const uint32_t* ents;   // SpQR outlier entries
+  const float* sw;        // W8: per-row scales
+  const float* sx;        // W8: per-token scales
+  uint16_t* Y;
+  int32_t* acc_out;
+  int32_t* status;
+  int M, N, K, RG, KU;
+};
+
+// ---- tcgen05 helpers -------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t umma_desc_sw128(const void* smem_tile) {
+  const uint64_t addr = smem_u32(smem_tile);
+  uint64_t d = 0;
+  d |= (addr & 0x3FFFFull) >> 4;         // start address
+  d |= 1ull << 16;                       // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;      // stride byte offset: 8 rows x 128 B
+  d |= 1ull << 46;                       // descriptor version (sm_100 family)
+  d |= 2ull << 61;                       // 128-byte swizzle
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, int n, int m) {
+  return (1u << 4) | (ab_type << 7) | (ab_type << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// byte offset of element (row, k) in a 128 x 64 K-major tile with 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int row, int k) {
+  return (uint32_t)(row * 128 + ((((k >> 3) ^ row) & 7) << 4) + ((k & 7) << 1));
+}
+
+__device__ __forceinline__ void sts32(uint8_t* base, uint32_t off, uint32_t v) {
+  *reinterpret_cast<uint32_t*>(base + off) = v;
+}
+
+// SpQR A-pair extraction (same field map as the decode kernel)
+template <int J, int R>
+__device__ __forceinline__ uint32_t sp_pair(const uint32_t (&w)[6]) {
+  if constexpr (J <= 4) {
+    constexpr int i = 4 * J + R;
+    if constexpr (i < 18) {
+      constexpr int wi = i / 3, f = (i % 3) * 2;
+      return ((w[wi] >> (3 * f)) & 0x00070007u) | 0x43004300u;
+    } else {
+      constexpr int b = 3 * (i - 18);
+      return ((w[b] >> 15) & 0x00010001u) | ((w[b + 1] >> 14) & 0x00020002u) | ((w[b + 2] >> 13) & 0x00040004u) |
+             0x43004300u;
+    }
+  } else {
+    constexpr int i = 4 * (J - 5) + R;
+    constexpr int wi = i / 2, f = (i % 2) * 2 + 1;
+    return ((w[wi] >> (3 * (f - 1))) & 0x00380038u) | 0x41804180u;
+  }
+}
+
+__device__ __forceinline__ uint32_t sp_qsqz(const uint8_t* area, int r, int gb) {
+  const int lane = 4 * (r & 7) + (gb >> 1);
+  const int i = ((r >> 3) << 1) | (gb & 1);
+  const int bit = 24 * lane + 6 * i;
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(area);
+  return __funnelshift_r(wp[bit >> 5], wp[(bit >> 5) + 1], bit & 31) & 63u;
+}
+
+template <int J, int R0>
+__device__ __forceinline__ void sp_write_j(uint8_t* bt, const uint32_t (&w)[6], int rowA, int rowB, int t,
+                                           uint32_t shA, uint32_t chA, uint32_t shB, uint32_t chB) {
+  constexpr uint32_t base = J <= 4 ? 0x43004300u : 0x41804180u;
+  const int k = 16 * t + 2 * J;
+  const uint32_t vA = bf16x2_fma(bf16x2_sub(sp_pair<J, R0>(w), base), shA, chA);
+  const uint32_t vB = bf16x2_fma(bf16x2_sub(sp_pair<J, R0 + 1>(w), base), shB, chB);
+  sts32(bt, sw128(rowA, k), vA);
+  sts32(bt, sw128(rowB, k), vB);
+}
+
+// ---- converters: one 32-row slice of the 128-row B tile for k-block kb of the packed stage
+
+template <int F>
+__device__ __forceinline__ void convert_block(uint8_t* bt, const uint8_t* pk, int kb, int cw, int lane, bool rg_valid) {
+  const int g = lane >> 2, t = lane & 3;
+  const int rg_local = cw >> 1;
+  const uint8_t* unit = pk + rg_local * TcCfg<F>::kUnitBytes;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rt = 2 * (cw & 1) + h;                // row tile inside the unit's row group
+    const int row0 = 32 * cw + 16 * h;              // first tile row in the B tile
+    if (!rg_valid) {
+      // rows past N: zero operand
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) sts32(bt, sw128(row0 + g + 8 * r, 8 * kk + 2 * t), 0u);
+      continue;
+    }
+    if constexpr (F == kW4) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + kb) * 32 + lane) * 16);
+      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+      const uint32_t* st = reinterpret_cast<const uint32_t*>(unit + kW4CodeBytes);
+      const uint32_t sz0 = st[rt * 16 + g], sz1 = st[rt * 16 + g + 8];
+      const float s0 = h2f_dev((uint16_t)(sz0 & 0xFFFFu)), s1 = h2f_dev((uint16_t)(sz1 & 0xFFFFu));
+      const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
+      const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0), zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
+      const uint32_t sp0 = pack_bf16x2(s0, s0), sp1 = pack_bf16x2(s1, s1);
+      const uint32_t zero = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = words[j];
+        const int k = 16 * j + 2 * t;
+        sts32(bt, sw128(row0 + g, k), bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+        sts32(bt, sw128(row0 + g + 8, k),
+              bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
+        sts32(bt, sw128(row0 + g, k + 8),
+              bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+        sts32(bt, sw128(row0 + g + 8, k + 8),
+              bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
+      }
+    } else if constexpr (F == kW8) {
+      const uint8_t* src = unit + (rt * 32 + lane) * 32;
+      const uint4 w01 = *reinterpret_cast<const uint4*>(src);
+      const uint4 w23 = *reinterpret_cast<const uint4*>(src + 16);
+      const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+      const uint32_t magic = 0x64646464u, off = 0x64806480u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = 16 * j + 2 * t;
+        uint32_t d;
+        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+        sts32(bt, sw128(row0 + g, k), f16x2_sub(d, off));
+        asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+        sts32(bt, sw128(row0 + g + 8, k), f16x2_sub(d, off));
+        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+        sts32(bt, sw128(row0 + g, k + 8), f16x2_sub(d, off));
+        asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+        sts32(bt, sw128(row0 + g + 8, k + 8), f16x2_sub(d, off));
+      }
+    } else {  // SpQR: k-block kb of the 256-wide unit = block kb/2, groups 4*(kb%2) .. +3
+      const int blk = kb >> 1, half = kb & 1;
+      const uint32_t* cw6 = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
+      uint32_t w[6];
+#pragma unroll
+      for (int x = 0; x < 6; ++x) w[x] = cw6[x];
+      const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+      const uint16_t* sgst = reinterpret_cast<const uint16_t*>(unit + kSpqrCodeBytes + kSpqrQsqzBytes);
+      uint32_t sh[2], ch[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = g + 8 * r, gb = t + 4 * half;
+        const uint16_t* st = sgst + (rt * 16 + row) * 4;
+        const uint32_t e = sp_qsqz(qarea, row, gb);
+        const float s_hat = __fmul_rn(__fsub_rn((float)(e & 7u), h2f_dev(st[1])), h2f_dev(st[0]));
+        const float z_hat = __fmul_rn(__fsub_rn((float)(e >> 3), h2f_dev(st[3])), h2f_dev(st[2]));
+        sh[r] = pack_bf16x2(s_hat, s_hat);
+        const float c = -s_hat * z_hat;
+        ch[r] = pack_bf16x2(c, c);
+      }
+      const int rowA = row0 + g, rowB = row0 + g + 8;
+      if (half == 0) {
+        sp_write_j<0, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<1, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<2, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<3, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<4, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<5, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<6, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<7, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      } else {
+        sp_write_j<0, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<1, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<2, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<3, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<4, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<5, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<6, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+        sp_write_j<7, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      }
+    }
+  }
+}
+
+// SpQR outliers of a (row group, supergroup) unit that fall into k-block kb, for the two
+// row tiles rt0, rt0 + 1 a converter warp owns: added onto the dequantized bf16 operand
+// (D + s, rounded once more to bf16).  Only the warp that wrote those rows touches them.
+__device__ __forceinline__ void spqr_outliers_block(uint8_t* bt, const TcArgs& a, int64_t rg, int64_t sg, int kb,
+                                                    int rt0, int rows_base, int lane) {
+  const int64_t u = rg * a.KU + sg;
+  const uint32_t e0 = __ldg(a.offs + 4 * u + rt0), emid = __ldg(a.offs + 4 * u + rt0 + 1);
+  const uint32_t e1 = __ldg(a.offs + 4 * u + rt0 + 2);
+  for (uint32_t p = e0 + lane; p < e1; p += 32) {
+    const uint32_t e = __ldg(a.ents + p);
+    const int kin = (int)((e >> 4) & 255u);
+    if ((kin >> 6) != kb) continue;
+    const int row = rows_base + (p >= emid ? 16 : 0) + (int)(e & 15u);
+    const uint32_t off = sw128(row, kin & 63);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(bt + off);
+    // each outlier position is unique, so plain read-modify-write is race free
+    const float v = __fadd_rn(bf2f(*dst), h2f_dev((uint16_t)(e >> 16)));
+    *dst = f2bf(v);
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcSmem<F>& sm = *reinterpret_cast<TcSmem<F>*>(base);
+  using C = TcCfg<F>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+  const int64_t rg0 = (int64_t)n_tile * 2;  // two 64-row groups per 128-row tile
+  const int nkb = a.K / kBK;
+  const int bpu = C::kBlocksPerUnit;
+  const int nunits = nkb / bpu;
+  const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
+  constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, kBM);
+  constexpr int nconv = 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNST; ++s) {
+      mbar_init(&sm.ab_full[s], 1 + nconv);
+      mbar_init(&sm.ab_empty[s], 1);
+    }
+    for (int s = 0; s < kNPK; ++s) {
+      mbar_init(&sm.pk_full[s], 1);
+      mbar_init(&sm.pk_empty[s], nconv);
+    }
+    mbar_init(&sm.acc_full, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&sm.ch_full[r], 1);
+      mbar_init(&sm.ch_empty[r], 4);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  if (warp == 1) {
+    const uint32_t cols = F == kW8 ? 256u : 128u;
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      auto load_units = [&](int ui) -> bool {
+        const int p = ui % kNPK;
+        const uint32_t ph = (uint32_t)(ui / kNPK) & 1u;
+        if (!mbar_wait(&sm.pk_empty[p], ph ^ 1u, a.status)) return false;
+        uint32_t bytes = 0;
+        for (int r = 0; r < 2; ++r)
+          if (rg0 + r < a.RG) bytes += C::kUnitBytes;
+        mbar_arrive_expect_tx(&sm.pk_full[p], bytes);
+        for (int r = 0; r < 2; ++r)
+          if (rg0 + r < a.RG)
+            bulk_g2s(sm.pk[p] + r * C::kUnitBytes, a.units + ((rg0 + r) * a.KU + ui) * (int64_t)C::kUnitBytes,
+                     C::kUnitBytes, &sm.pk_full[p]);
+        return true;
+      };
+      // weights do not depend on the previous kernel: prefetch before the dependency wait
+      int next_unit = 0;
+      for (; next_unit < kNPK && next_unit < nunits && ok; ++next_unit) ok = load_units(next_unit);
+      pdl_wait();
+      for (int i = 0; i < nkb && ok; ++i) {
+        if (i % bpu == 0 && i / bpu + kNPK - 1 >= next_unit && next_unit < nunits) {
+          ok = load_units(next_unit);
+          ++next_unit;
+          if (!ok) break;
+        }
+        const int s = i % kNST;
+        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.ab_full[s], kTileBytes);
+        tma_load_2d(sm.a[s], &xmap, i * kBK, m_tile * kBM, &sm.ab_full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    pdl_wait();
+    if (lane == 0) {
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int s = i % kNST;
+        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        uint32_t dcol = 0;
+        bool first = (i == 0);
+        if constexpr (F == kW8) {
+          const int c = i / kChunkBlocks;
+          dcol = (uint32_t)(c & 1) * 128u;
+          first = (i % kChunkBlocks) == 0;
+          if (first && c >= 2) {
+            if (!mbar_wait(&sm.ch_empty[c & 1], (uint32_t)((c / 2) - 1) & 1u, a.status)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!mbar_wait(&sm.ab_full[s], ph, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = umma_desc_sw128(sm.a[s]);
+        const uint64_t db = umma_desc_sw128(sm.b[s]);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_f16(tmem + dcol, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        umma_commit(&sm.ab_empty[s]);
+        if constexpr (F == kW8) {
+          if ((i % kChunkBlocks) == kChunkBlocks - 1 || i == nkb - 1) umma_commit(&sm.ch_full[(i / kChunkBlocks) & 1]);
+        }
+      }
+      umma_commit(&sm.acc_full);
+    }
+    __syncwarp();
+  } else if (warp < 2 + nconv) {
+    // ------------------------------------------------------------------ converters + epilogue
+    pdl_wait();
+    const int cw = warp - 2;
+    const bool rg_valid = rg0 + (cw >> 1) < a.RG;
+    for (int ui = 0; ui < nunits && ok; ++ui) {
+      const int p = ui % kNPK;
+      if (!mbar_wait(&sm.pk_full[p], (uint32_t)(ui / kNPK) & 1u, a.status)) {
+        ok = false;
+        break;
+      }
+      for (int b = 0; b < bpu; ++b) {
+        const int i = ui * bpu + b;
+        const int s = i % kNST;
+        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
+          ok = false;
+          break;
+        }
+        convert_block<F>(sm.b[s], sm.pk[p], b, cw, lane, rg_valid);
+        if constexpr (F == kSpqr) {
+          if (rg_valid) {
+            __syncwarp();
+            spqr_outliers_block(sm.b[s], a, rg0 + (cw >> 1), ui, b, 2 * (cw & 1), 32 * cw, lane);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ab_full[s]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.pk_empty[p]);
+    }
+    if constexpr (F != kW8) {
+      // epilogue: TMEM lane quadrant = warp % 4
+      const int q = warp & 3;
+      if (ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
+        tc_fence_after();
+        const int m = m_tile * kBM + 32 * q + lane;
+        const int n0 = n_tile * kBN;
+#pragma unroll
+        for (int cb = 0; cb < kBN / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * cb, r);
+          if (m < a.M) {
+            uint32_t pk16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            const int n = n0 + 32 * cb;
+            uint16_t* dst = a.Y + (int64_t)m * a.N + n;
+            // N is a multiple of 64 rows (the device image pads row groups), so a 32-column
+            // slice is either fully inside or fully outside the output
+            if (n + 32 <= a.N) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+            }
+          }
+        }
+      }
+    }
+  } else if constexpr (F == kW8) {
+    // ------------------------------------------------------------------ exact int32 drain + epilogue
+    pdl_wait();
+    const int q = warp & 3;
+    int32_t acc[kBN];
+#pragma unroll
+    for (int i = 0; i < kBN; ++i) acc[i] = 0;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      if (!mbar_wait(&sm.ch_full[c & 1], (uint32_t)(c / 2) & 1u, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < kBN / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c & 1) * 128u + 32u * cb, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 * cb + i] += __float2int_rn(__uint_as_float(r[i]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ch_empty[c & 1]);
+    }
+    const int m = m_tile * kBM + 32 * q + lane;
+    if (ok && m < a.M) {
+      const int n0 = n_tile * kBN;
+      // N is a multiple of 64, so each 64-column half of the tile is fully in or out
+      if (a.acc_out) {
+#pragma unroll
+        for (int i = 0; i < kBN; i += 4)
+          if (n0 + i < a.N)
+            *reinterpret_cast<int4*>(a.acc_out + (int64_t)m * a.N + n0 + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+      } else {
+        const float sxm = a.sx[m];
+        uint16_t* dst = a.Y + (int64_t)m * a.N + n0;
+#pragma unroll
+        for (int i = 0; i < kBN; i += 2) {
+          if (n0 + i < a.N) {
+            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[i]), sxm), a.sw[n0 + i]);
+            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[i + 1]), sxm), a.sw[n0 + i + 1]);
+            *reinterpret_cast<uint32_t*>(dst + i) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    const uint32_t cols = F == kW8 ? 256u : 128u;
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int F>
+int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
+  auto enc = get_encode();
+  if (!enc) return (int)cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.M};
+  const cuuint64_t strides[1] = {(cuuint64_t)args.K * 2};
+  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = F == kW8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(Xop), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+  const size_t smem = sizeof(TcSmem<F>) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((args.N + kBN - 1) / kBN), (unsigned)((args.M + kBM - 1) / kBM));
+  cfg.blockDim = dim3(F == kW8 ? 320 : 192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, tc_gemm_kernel<F>, map, args);
+}
+
+}  // namespace
+
+int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
+  TcArgs a{v.units, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.G};
+  return launch_tc<kW4>(X, a, stream);
+}
+
+int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
+  TcArgs a{v.units, v.offs, v.ents, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.S};
+  return launch_tc<kSpqr>(X, a, stream);
+}
+
+int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc, int M,
+                      int32_t* status, void* stream) {
+  TcArgs a{v.units, nullptr, nullptr, v.sw, sx, Y, acc, status, M, v.N, v.K, v.RG, v.KB};
+  return launch_tc<kW8>(q16, a, stream);
+}
+
+}  // namespace qlin

@@ -878,6 +878,14 @@ qlin_status qlin_bind(qlin_handle h, void* dev_weights, size_t bytes, qlin_strea
   return QLIN_OK;
 }
 
+qlin_status qlin_attach(qlin_handle h, void* dev_weights, size_t bytes) {
+  if (!h || !dev_weights) return QLIN_ERR_INVALID_ARG;
+  if (bytes < h->image.size() || ((uintptr_t)dev_weights & 255u)) return QLIN_ERR_INVALID_ARG;
+  h->dev = (uint8_t*)dev_weights;
+  h->dev_bytes = bytes;
+  return QLIN_OK;
+}
+
 qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int max_M, qlin_stream stream) {
   if (!h || !dev_ws || max_M < 0 || ((uintptr_t)dev_ws & 255u)) return QLIN_ERR_INVALID_ARG;
   WsLayout w = ws_layout(h, max_M);
@@ -903,7 +911,7 @@ static qlin_status check_forward(qlin_handle h, const void* X, const void* Y, in
   if (M == 0) return QLIN_OK;
   if (!X || !Y || ((uintptr_t)X & 15u) || ((uintptr_t)Y & 15u)) return QLIN_ERR_INVALID_ARG;
   if (!h->dev) return QLIN_ERR_NOT_BOUND;
-  if (!h->ws || (h->format == QLIN_FMT_W8A8 && std::min(M, 16) > h->ws_maxM)) return QLIN_ERR_WORKSPACE;
+  if (!h->ws || (h->format == QLIN_FMT_W8A8 && M > h->ws_maxM)) return QLIN_ERR_WORKSPACE;
   return QLIN_OK;
 }
 
@@ -929,19 +937,34 @@ static qlin_status run_decode(qlin_handle h, const uint16_t* X, uint16_t* Y, int
   return e ? QLIN_ERR_CUDA : QLIN_OK;
 }
 
+// Prefill (M > 16): tensor-core kernels, one launch (two for W8A8: act-quant + GEMM).
+static qlin_status run_prefill(qlin_handle h, const uint16_t* X, uint16_t* Y, int32_t* acc, int M, cudaStream_t s) {
+  int e = 0;
+  switch (h->format) {
+    case QLIN_FMT_W4G128:
+      e = launch_w4_prefill(w4view(h), X, Y, M, h->wsv.status, s);
+      break;
+    case QLIN_FMT_SPQR:
+      e = launch_spqr_prefill(spqrview(h), X, Y, M, h->wsv.status, s);
+      break;
+    case QLIN_FMT_W8A8: {
+      uint16_t* q16 = reinterpret_cast<uint16_t*>(h->wsv.qx);
+      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, M, s);
+      if (!e) e = launch_w8_prefill(w8view(h), q16, h->wsv.sx, Y, acc, M, h->wsv.status, s);
+      break;
+    }
+    default:
+      return QLIN_ERR_INVALID_ARG;
+  }
+  return e ? QLIN_ERR_CUDA : QLIN_OK;
+}
+
 qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream) {
   qlin_status st = check_forward(h, X, Y, M);
   if (st != QLIN_OK || M == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const uint16_t* x = (const uint16_t*)X;
-  uint16_t* y = (uint16_t*)Y;
-  // rows beyond 16 run as 16-row decode slices
-  for (int m0 = 0; m0 < M; m0 += 16) {
-    const int mm = std::min(16, M - m0);
-    st = run_decode(h, x + (size_t)m0 * h->K, y + (size_t)m0 * h->N, nullptr, mm, s);
-    if (st != QLIN_OK) return st;
-  }
-  return QLIN_OK;
+  if (M > 16) return run_prefill(h, (const uint16_t*)X, (uint16_t*)Y, nullptr, M, s);
+  return run_decode(h, (const uint16_t*)X, (uint16_t*)Y, nullptr, M, s);
 }
 
 qlin_status qlin_forward_host(qlin_handle h, const void* X_host, void* Y_host, void* X_dev,
@@ -973,12 +996,8 @@ qlin_status qlin_forward_acc(qlin_handle h, const void* X, int32_t* acc, int M, 
   qlin_status st = check_forward(h, X, acc, M);
   if (st != QLIN_OK || M == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  for (int m0 = 0; m0 < M; m0 += 16) {
-    const int mm = std::min(16, M - m0);
-    st = run_decode(h, (const uint16_t*)X + (size_t)m0 * h->K, nullptr, acc + (size_t)m0 * h->N, mm, s);
-    if (st != QLIN_OK) return st;
-  }
-  return QLIN_OK;
+  if (M > 16) return run_prefill(h, (const uint16_t*)X, nullptr, acc, M, s);
+  return run_decode(h, (const uint16_t*)X, nullptr, acc, M, s);
 }
 
 qlin_status qlin_dequant_device(qlin_handle h, void* out, qlin_stream stream) {
@@ -1072,9 +1091,9 @@ const char* qlin_status_string(qlin_status s) {
 
 int qlin_sm_count(void) { return sm_count_cached(); }
 
-qlin_status qlin_debug_wait_timeout(int32_t* status, int spins, qlin_stream stream) {
-  if (!status || spins <= 0) return QLIN_ERR_INVALID_ARG;
-  return launch_debug_wait_timeout(status, spins, stream) ? QLIN_ERR_CUDA : QLIN_OK;
+qlin_status qlin_debug_wait_timeout(int32_t* status, int limit_us, qlin_stream stream) {
+  if (!status || limit_us <= 0 || limit_us > 10000000) return QLIN_ERR_INVALID_ARG;
+  return launch_debug_wait_timeout(status, limit_us, stream) ? QLIN_ERR_CUDA : QLIN_OK;
 }
 
 }  // extern "C"

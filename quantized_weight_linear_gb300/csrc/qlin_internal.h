@@ -103,9 +103,14 @@ int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, f
                             void* stream);
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y,
                      int32_t* acc_out, int M, const Workspace& ws, int grid, void* stream);
+int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream);
+int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status,
+                        void* stream);
+int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc,
+                      int M, int32_t* status, void* stream);
 int launch_w4_dequant(const W4View& v, float* out, void* stream);
 int launch_spqr_dequant(const SpqrView& v, float* out, void* stream);
 int launch_w8_export(const W8View& v, int8_t* out, void* stream);
-int launch_debug_wait_timeout(int32_t* status, int spins, void* stream);
+int launch_debug_wait_timeout(int32_t* status, int limit_us, void* stream);
 
 }  // namespace qlin

@@ -88,18 +88,32 @@ def test_spqr_forward_tolerance(qlin, N, K, frac, M):
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
 
 
-def test_spqr_one_hot_rows_bit_exact(qlin):
+def test_spqr_one_hot_rows(qlin):
+    """M == 1 accumulates exact integer products per (row, group): one-hot rows are bit-exact.
+    M >= 2 dequantizes to bf16 in registers (one bf16 FMA of s^ and -s^ z^ per pair), so there
+    the bar is the stated tolerance -- here at most 2^-7 relative plus the bf16 rounding of the
+    s^ z^ term."""
     N, K = 128, 512
     W = synth.student_t3(17, 0.02, (N, K))
     layer = qlin.QLinear.from_spqr(W, 0.02).to("cuda")
-    w_hat = spqr.pack(W, 0.02)["w_hat"]
-    for ks in ([0], [3, 100, 255, 256, 511]):
-        X = np.zeros((len(ks), K), dtype=np.float32)
-        for i, k in enumerate(ks):
-            X[i, k] = 1.0
-        y = _y(layer, synth.f32_to_bf16(X), len(ks))
-        for i, k in enumerate(ks):
-            assert np.array_equal(y[i], bf16_round(w_hat[:, k])), (ks, k)
+    p = spqr.pack(W, 0.02)
+    w_hat = p["w_hat"]
+    for k in (0, 3, 100, 255, 256, 511):
+        X = np.zeros((1, K), dtype=np.float32)
+        X[0, k] = 1.0
+        y = _y(layer, synth.f32_to_bf16(X), 1)
+        assert np.array_equal(y[0], bf16_round(w_hat[:, k])), k
+    ks = [3, 100, 255, 256, 511]
+    X = np.zeros((len(ks), K), dtype=np.float32)
+    for i, k in enumerate(ks):
+        X[i, k] = 1.0
+    y = _y(layer, synth.f32_to_bf16(X), len(ks))
+    sh = np.repeat(np.abs(p["s_hat"]).astype(np.float64), 16, axis=1)
+    zh = np.repeat(np.abs(p["z_hat"]).astype(np.float64), 16, axis=1)
+    for i, k in enumerate(ks):
+        ref = w_hat[:, k].astype(np.float64)
+        bound = 2.0 ** -7 * (np.abs(ref) + sh[:, k] * (7 + zh[:, k])) + 1e-9
+        assert np.all(np.abs(y[i] - ref) <= bound), k
 
 
 # ----------------------------------------------------------------------------- W8A8
@@ -154,7 +168,7 @@ def test_zero_weights_and_zero_activations(qlin):
 
 def test_device_wait_limit_reports_timeout(qlin):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    qlin.qlin_debug_wait_timeout(status, 2000)
+    qlin.qlin_debug_wait_timeout(status, 20000)  # 20 ms
     torch.cuda.synchronize()
     assert int(status.item()) == qlin.QLIN_ERR_TIMEOUT
     # the context is still usable afterwards

@@ -381,3 +381,16 @@ def test_bf16_rounding_and_ulp():
     assert ok
     ok, _ = forward.within_tolerance(np.array([1.0]), np.array([1.0 + 2 ** -6]), np.array([0.0]))
     assert not ok
+
+
+def test_spqr_threshold_selection_equals_sorted_selection():
+    W = synth.student_t3(9, 0.02, (96, 512))
+    W.ravel()[::97] = 0.05  # many exact ties
+    for f in (0.0, 0.003, 0.01, 0.02, 0.3):
+        assert np.array_equal(spqr.select_outliers(W, f), spqr.select_outliers_by_threshold(W, f))
+    # row subsets reproduce the full pack row for row
+    p = spqr.pack(W, 0.01)
+    rows = np.array([5, 0, 77])
+    sub = spqr.quantize_rows(W, 0.01, rows)
+    assert np.array_equal(sub["q"], p["q"][rows]) and np.array_equal(sub["D"], p["D"][rows])
+    assert np.array_equal(spqr.dequantize(sub), p["w_hat"][rows])
