@@ -302,8 +302,51 @@ def _extra_configs(q, torch, stream, l2):
         t = ms / steps / 1e3
         out["w8a8_4096x4096_M16"] = {"GB/s": round(nbytes / t / 1e9, 1), "us_per_forward": round(t * 1e6, 3),
                                      "TOPS": round(2 * 16 * 4096 * 4096 / t / 1e12, 2), "weight_bytes": nbytes}
+        del rot, layer
     except Exception as e:  # extra lines must never break the headline
         out["error"] = repr(e)[:300]
+    out.update(_prefill_configs(q, torch, stream))
+    return out
+
+
+def _prefill_configs(q, torch, stream):
+    """Prefill M=4096 on K=8192, N=28672 for the three formats (tensor-core path): TFLOP/s."""
+    import qlin_synth as synth
+    out = {}
+    M, K, N = 4096, 8192, 28672
+    flops = 2.0 * M * N * K
+    for fmt in ("w4g128", "spqr1pct", "w8a8"):
+        try:
+            if fmt == "w8a8":
+                W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
+                layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)
+            elif fmt == "w4g128":
+                W, X = synth.gptq_layer(N, K, M, seed=0)
+                layer = q.QLinear.from_w4g128(W).to("cuda")
+            else:
+                W, X = synth.spqr_layer(N, K, M, seed=0)
+                layer = q.QLinear.from_spqr(W, 0.01).to("cuda")
+            del W
+            Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            for _ in range(3):
+                q.qlin_forward(layer.handle, Xd, Y, M, stream)
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 10
+            ev0.record(stream)
+            for _ in range(reps):
+                q.qlin_forward(layer.handle, Xd, Y, M, stream)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            t = ev0.elapsed_time(ev1) / reps / 1e3
+            out[f"prefill_{fmt}_M4096_K8192_N28672"] = {"TFLOP/s": round(flops / t / 1e12, 1),
+                                                         "ms_per_forward": round(t * 1e3, 3),
+                                                         "pipe": "fp16 tensor (exact int8 codes)" if fmt == "w8a8"
+                                                         else "bf16 tensor"}
+            del layer, Xd, Y
+        except Exception as e:
+            out[f"prefill_{fmt}_error"] = repr(e)[:300]
     return out
 
 

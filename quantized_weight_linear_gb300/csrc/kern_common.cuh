@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "qlin_internal.h"
@@ -79,18 +80,33 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Bounded wait on the phase with the given parity: gives up after `limit_ns` of wall time
 // (default 2 s), records the timeout in *status (if non-null) and returns false.
+// QLIN_WAIT_HINT_NS: suspend-time hint of each poll (0 = the hardware's default limit).
+#ifndef QLIN_WAIT_HINT_NS
+#define QLIN_WAIT_HINT_NS 0
+#endif
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity, 10000u)) return true;
+    if (QLIN_WAIT_HINT_NS > 0 ? mbar_try_wait_hint(bar, parity, QLIN_WAIT_HINT_NS) : mbar_try_wait(bar, parity))
+      return true;
     if (global_ns() - t0 > limit_ns) break;
   }
   if (status) atomicExch(status, kStatusTimeout);
   return false;
 }
+
+// Upper bound on the CTAs per SM the decode launches use (their occupancy allows up to 4).
+#ifndef QLIN_DECODE_CPS_MAX
+#define QLIN_DECODE_CPS_MAX 4
+#endif
+
+// Programmatic dependent launch for the decode and prefill kernels (1 = on).
+#ifndef QLIN_USE_PDL
+#define QLIN_USE_PDL 1
+#endif
 
 // global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

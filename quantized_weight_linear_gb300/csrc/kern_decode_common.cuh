@@ -19,50 +19,76 @@ struct ConsumerSync {
   }
 };
 
-// Completion of one row group (64 rows x up to 16 tokens).  `vals[i]` is the value of
-// entry idx[i] = row_in_group * 16 + token held by this thread (nv entries, invalid ones
-// flagged by idx < 0).  T is float or int (integer sums are exact).
-// Returns false if a bounded wait gave up.  If the row group belongs to this CTA alone,
-// `done` is called with the finished values straight away; otherwise the values go to
-// the CTA's slot and the last contributor calls `done` with the sums.
-template <typename T, int NV, typename Done>
-__device__ __forceinline__ bool finish_row_group(int64_t rg, int64_t per_rg, int64_t units, int64_t grid,
-                                                 int64_t cta, const T (&vals)[NV], const int (&idx)[NV],
-                                                 const Workspace& ws, ConsumerSync& cs, int* flag,
-                                                 Done done) {
-  const SplitInfo si = split_info(rg, per_rg, units, grid);
-  if (si.first_cta == si.last_cta) {
-    done(vals);
+// Completion of row groups (64 rows x up to 16 tokens) whose units are split between CTAs.
+// A CTA's contiguous unit range can split at most two row groups (its first and its last);
+// every other row group it touches is whole and is written straight away.
+//
+// stage(): a whole row group goes to `done` at once; a split one is stored into this CTA's
+// partial slot (plain stores, nothing waits).  finish(), once at the end of the range: one
+// fence, one arrival per split row group on its counter, and the last contributor sums all
+// slots in CTA order (deterministic) and hands the sums to `done`, then resets the counter
+// for the next forward.  So no consumer ever stalls on another CTA in the middle of its
+// stream.  `vals[i]` is the value of entry idx[i] = row_in_group * 16 + token (idx < 0:
+// unused).  T is float or int (integer sums are exact).
+template <typename T, int NV>
+struct RowGroupFinisher {
+  int64_t per_rg, units, grid, cta;
+  const Workspace* ws;
+  int64_t pend[2];
+  int npend;
+
+  __device__ __forceinline__ RowGroupFinisher(int64_t per_rg_, int64_t units_, int64_t grid_, int64_t cta_,
+                                              const Workspace* ws_)
+      : per_rg(per_rg_), units(units_), grid(grid_), cta(cta_), ws(ws_), npend(0) {}
+
+  template <typename Done>
+  __device__ __forceinline__ void stage(int64_t rg, const T (&vals)[NV], const int (&idx)[NV], Done done) {
+    const SplitInfo si = split_info(rg, per_rg, units, grid);
+    if (si.first_cta == si.last_cta) {
+      done(rg, vals);
+      return;
+    }
+    const int side = split_side(cta, rg, per_rg, units, grid);
+    T* slot = reinterpret_cast<T*>(ws->partials) + (cta * 2 + side) * (kRowGroup * 16);
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (idx[i] >= 0) slot[idx[i]] = vals[i];
+    if (npend < 2) pend[npend++] = rg;
+  }
+
+  // Returns false if a bounded wait gave up.  `flags` is a 2-int shared array.
+  template <typename Done>
+  __device__ __forceinline__ bool finish(const int (&idx)[NV], ConsumerSync& cs, int* flags, Done done) {
+    if (npend == 0) return true;  // uniform: every consumer thread walks the same row groups
+    __threadfence();
+    if (!cs.sync()) return false;
+    if (threadIdx.x == 0) {
+      for (int p = 0; p < npend; ++p) {
+        const SplitInfo si = split_info(pend[p], per_rg, units, grid);
+        const unsigned old = atomicAdd(&ws->counters[pend[p]], 1u);
+        flags[p] = (old == (unsigned)(si.last_cta - si.first_cta)) ? 1 : 0;
+      }
+    }
+    if (!cs.sync()) return false;
+    for (int p = 0; p < npend; ++p) {
+      if (!flags[p]) continue;
+      __threadfence();
+      const SplitInfo si = split_info(pend[p], per_rg, units, grid);
+      T sum[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) sum[i] = T(0);
+      for (int64_t c = si.first_cta; c <= si.last_cta; ++c) {
+        const int sd = split_side(c, pend[p], per_rg, units, grid);
+        const T* sl = reinterpret_cast<const T*>(ws->partials) + (c * 2 + sd) * (kRowGroup * 16);
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (idx[i] >= 0) sum[i] += __ldcg(sl + idx[i]);
+      }
+      done(pend[p], sum);
+      if (threadIdx.x == 0) ws->counters[pend[p]] = 0u;
+    }
     return true;
   }
-  const int side = split_side(cta, rg, per_rg, units, grid);
-  T* slot = reinterpret_cast<T*>(ws.partials) + (cta * 2 + side) * (kRowGroup * 16);
-#pragma unroll
-  for (int i = 0; i < NV; ++i)
-    if (idx[i] >= 0) slot[idx[i]] = vals[i];
-  __threadfence();
-  if (!cs.sync()) return false;
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(&ws.counters[rg], 1u);
-    *flag = (old == (unsigned)(si.last_cta - si.first_cta)) ? 1 : 0;
-  }
-  if (!cs.sync()) return false;
-  if (*flag) {
-    __threadfence();
-    T sum[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) sum[i] = T(0);
-    for (int64_t c = si.first_cta; c <= si.last_cta; ++c) {
-      const int sd = split_side(c, rg, per_rg, units, grid);
-      const T* sl = reinterpret_cast<const T*>(ws.partials) + (c * 2 + sd) * (kRowGroup * 16);
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (idx[i] >= 0) sum[i] += __ldcg(sl + idx[i]);
-    }
-    done(sum);
-    if (threadIdx.x == 0) ws.counters[rg] = 0u;
-  }
-  return cs.sync();
-}
+};
 
 }  // namespace qlin

@@ -25,10 +25,10 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesSp = 6;
+constexpr int kStagesSp = 4;
 constexpr int kXStrideSp = 264;    // 256 bf16 + 8 pad
 constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
-constexpr int kOffsCap = 4096 + 16;  // offsets staged per CTA
+constexpr int kOffsCap = 1024 + 16;  // offsets staged per CTA
 
 template <int XR>  // staged X rows (1 for the M == 1 kernel, 8 or 16 otherwise)
 struct SpSmem {
@@ -42,7 +42,7 @@ struct SpSmem {
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
   uint64_t cons_bar;
-  int flag;
+  int flags[2];
 };
 
 // bucket bounds of unit u, row tile rt, from the staged offsets
@@ -91,7 +91,7 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
 }
 
 template <int MODE, int MT>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
     spqr_decode_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -183,48 +183,53 @@ __global__ void __launch_bounds__(160, 1)
   __syncwarp();
   int64_t cur_rg = u0 / S;
 
-  auto flush = [&](int64_t rg) -> bool {
+  constexpr int NV = (MODE == 1) ? 2 : NACC;
+  int idx[NV];
+  if constexpr (MODE == 1) {
+    idx[0] = t == 0 ? (rt * 16 + g) * 16 : -1;
+    idx[1] = t == 0 ? (rt * 16 + g + 8) * 16 : -1;
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = g + ((i & 2) ? 8 : 0);
+        const int m = 2 * t + (i & 1) + 8 * mt;
+        idx[mt * 4 + i] = (m < M) ? (rt * 16 + r) * 16 + m : -1;
+      }
+  }
+  auto done = [&](int64_t rg, const float (&out)[NV]) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (idx[j] < 0) continue;
+      const int64_t n = rg * kRowGroup + idx[j] / 16;
+      const int m = idx[j] % 16;
+      if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+    }
+  };
+  RowGroupFinisher<float, NV> fin(S, U, grid, cta, &ws);
+  auto flush = [&](int64_t rg) {
     __syncwarp();
+    float vals[NV];
     if constexpr (MODE == 1) {
       float r0 = acc[0] + acc[1], r1 = acc[2] + acc[3];
       r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
       r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-      float vals[2] = {r0 + sm.rowacc[rt][g][0], r1 + sm.rowacc[rt][g + 8][0]};
-      int idx[2] = {t == 0 ? (rt * 16 + g) * 16 : -1, t == 0 ? (rt * 16 + g + 8) * 16 : -1};
-      auto done = [&](const float (&out)[2]) {
-        for (int j = 0; j < 2; ++j) {
-          if (idx[j] < 0) continue;
-          const int64_t n = rg * kRowGroup + idx[j] / 16;
-          if (n < v.N) Y[n] = f2bf(out[j]);
-        }
-      };
-      return finish_row_group<float, 2>(rg, S, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+      vals[0] = r0 + sm.rowacc[rt][g][0];
+      vals[1] = r1 + sm.rowacc[rt][g + 8][0];
     } else {
-      float vals[NACC];
-      int idx[NACC];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = g + ((i & 2) ? 8 : 0);
           const int m = 2 * t + (i & 1) + 8 * mt;
-          const bool ok = m < M;
-          vals[mt * 4 + i] = acc[mt * 4 + i] + (ok ? sm.rowacc[rt][r][m] : 0.f);
-          idx[mt * 4 + i] = ok ? (rt * 16 + r) * 16 + m : -1;
+          vals[mt * 4 + i] = acc[mt * 4 + i] + (m < M ? sm.rowacc[rt][r][m] : 0.f);
         }
-      auto done = [&](const float (&out)[NACC]) {
-#pragma unroll
-        for (int j = 0; j < NACC; ++j) {
-          if (idx[j] < 0) continue;
-          const int64_t n = rg * kRowGroup + idx[j] / 16;
-          const int m = idx[j] % 16;
-          if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
-        }
-      };
-      return finish_row_group<float, NACC>(rg, S, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
     }
+    fin.stage(rg, vals, idx, done);
   };
 
   for (int it = 0; it < n_units; ++it) {
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(160, 1)
     const int64_t u = u0 + it;
     const int64_t rg = u / S;
     if (rg != cur_rg) {
-      if (!flush(cur_rg)) return;
+      flush(cur_rg);
 #pragma unroll
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
       __syncwarp();
@@ -266,6 +271,17 @@ __global__ void __launch_bounds__(160, 1)
         sb += __shfl_xor_sync(0xffffffffu, sb, 1);
       }
       const float bsum = 128.f * sa + 16.f * sb, xsum = sa + sb;
+      // per-field constants of the (qs, qz) decode: pair i uses row g (i < 2) or g + 8;
+      // qs sits at bit 6i of the lane's 24-bit field, qz at bit 6i of the field shifted by 3
+      float kcs[4], kms[4], kcz[4], kmz[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float ps = (float)(1u << (6 * i)), pz = ps;
+        kcs[i] = 8388608.f + (i < 2 ? zsA : zsB) * ps;
+        kms[i] = (i < 2 ? ssA : ssB) * (1.f / ps);
+        kcz[i] = 8388608.f + (i < 2 ? zzA : zzB) * pz;
+        kmz[i] = (i < 2 ? szA : szB) * (1.f / pz);
+      }
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
@@ -285,16 +301,17 @@ __global__ void __launch_bounds__(160, 1)
         const uint4 by1 = *reinterpret_cast<const uint4*>(pb1 == sm.zeros ? sm.zeros : pb1 + 4);
         const uint32_t b0v[8] = {bx0.x, bx0.y, bx0.z, bx0.w, by0.x, by0.y, by0.z, by0.w};
         const uint32_t b1v[8] = {bx1.x, bx1.y, bx1.z, bx1.w, by1.x, by1.y, by1.z, by1.w};
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // two independent accumulator chains (even / odd j) keep the MMA pipe busy
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t a[4];
         spqr_frag<0>(w, a); mma_bf16(c, a, b0v[0], b1v[0]);
-        spqr_frag<1>(w, a); mma_bf16(c, a, b0v[1], b1v[1]);
+        spqr_frag<1>(w, a); mma_bf16(d, a, b0v[1], b1v[1]);
         spqr_frag<2>(w, a); mma_bf16(c, a, b0v[2], b1v[2]);
-        spqr_frag<3>(w, a); mma_bf16(c, a, b0v[3], b1v[3]);
+        spqr_frag<3>(w, a); mma_bf16(d, a, b0v[3], b1v[3]);
         spqr_frag<4>(w, a); mma_bf16(c, a, b0v[4], b1v[4]);
-        spqr_frag<5>(w, a); mma_bf16(c, a, b0v[5], b1v[5]);
+        spqr_frag<5>(w, a); mma_bf16(d, a, b0v[5], b1v[5]);
         spqr_frag<6>(w, a); mma_bf16(c, a, b0v[6], b1v[6]);
-        spqr_frag<7>(w, a); mma_bf16(c, a, b0v[7], b1v[7]);
+        spqr_frag<7>(w, a); mma_bf16(d, a, b0v[7], b1v[7]);
         // group sums of the two accumulator groups 2t, 2t+1 of this block
         const int l0 = 2 * (blk * 8 + 2 * t);
         const float B0 = __shfl_sync(0xffffffffu, bsum, l0), S0 = __shfl_sync(0xffffffffu, xsum, l0);
@@ -302,16 +319,18 @@ __global__ void __launch_bounds__(160, 1)
         const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(qarea);
         const int bit = 24 * lane;
-        const uint32_t f24 = __funnelshift_r(qw[bit >> 5], qw[(bit >> 5) + 1], bit & 31);
+        const uint32_t f24 = __funnelshift_r(qw[bit >> 5], qw[(bit >> 5) + 1], bit & 31) & 0xFFFFFFu;
+        const uint32_t z24 = f24 >> 3;  // qz fields at bits 6i: every field stays below bit 23
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float qs = (float)((f24 >> (6 * i)) & 7u), qz = (float)((f24 >> (6 * i + 3)) & 7u);
-          const float ss = i < 2 ? ssA : ssB, zs = i < 2 ? zsA : zsB;
-          const float sz = i < 2 ? szA : szB, zz = i < 2 ? zzA : zzB;
-          const float sh = __fmul_rn(__fsub_rn(qs, zs), ss);
-          const float zh = __fmul_rn(__fsub_rn(qz, zz), sz);
+          // field at bit p <= 18, OR-ed under the exponent of 2^23: the float 2^23 + q 2^p, exact;
+          // subtracting 2^23 + z 2^p and scaling by s 2^-p gives (q - z) s with one rounding
+          const float xs = __uint_as_float((f24 & (7u << (6 * i))) | 0x4B000000u);
+          const float xz = __uint_as_float((z24 & (7u << (6 * i))) | 0x4B000000u);
+          const float sh = __fmul_rn(__fsub_rn(xs, kcs[i]), kms[i]);
+          const float zh = __fmul_rn(__fsub_rn(xz, kcz[i]), kmz[i]);
           const float Bg = (i & 1) ? B1 : B0, Sg = (i & 1) ? S1 : S0;
-          acc[i] += sh * (c[i] - Bg - zh * Sg);
+          acc[i] += sh * ((c[i] + d[i]) - Bg - zh * Sg);
         }
       }
     } else {
@@ -388,7 +407,10 @@ __global__ void __launch_bounds__(160, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
-  if (n_units > 0) flush(cur_rg);
+  if (n_units > 0) {
+    flush(cur_rg);
+    fin.finish(idx, cs, sm.flags, done);
+  }
 }
 
 template <int MODE, int MT>
@@ -410,7 +432,7 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT>, v, X, Y, M, ws);
@@ -418,12 +440,20 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
 
 }  // namespace
 
+int spqr_decode_grid(const SpqrView& v, int M, int sms) {
+  // several CTAs per SM hide the unpack latency; every CTA stages its slice of the bucket
+  // offsets, so ranges stay below kOffsCap entries
+  const int64_t U = (int64_t)v.RG * v.S;
+  const int cps = std::min(M == 1 ? 4 : 2, QLIN_DECODE_CPS_MAX);
+  int64_t grid = std::min<int64_t>(U, (int64_t)cps * sms);
+  const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
+  if (grid < need) grid = std::min<int64_t>(U, need);
+  return (int)std::min<int64_t>(grid, 1 << 30);
+}
+
 int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                        void* stream) {
-  // every CTA stages its slice of the bucket offsets: keep ranges below kOffsCap entries
-  const int64_t U = (int64_t)v.RG * v.S;
-  const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
-  if (grid < need) grid = (int)need;
+  grid = spqr_decode_grid(v, M, ws.sms);
   if (grid > ws.grid) return (int)cudaErrorInvalidValue;
   if (M == 1) return launch_spqr_t<1, 1>(v, X, Y, M, ws, grid, stream);
   if (M <= 8) return launch_spqr_t<2, 1>(v, X, Y, M, ws, grid, stream);

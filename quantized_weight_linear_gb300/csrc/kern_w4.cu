@@ -19,7 +19,7 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesW4 = 8;
+constexpr int kStagesW4 = 4;
 constexpr int kXStrideW4 = 136;  // staged X row: 128 bf16 + 8 pad (bank-conflict free B loads)
 
 template <int MT>
@@ -29,11 +29,11 @@ struct W4Smem {
   uint64_t full[kStagesW4];
   uint64_t empty[kStagesW4];
   uint64_t cons_bar;
-  int flag;
+  int flags[2];
 };
 
 template <int MT>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, 4)
     w4_decode_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_raw);
@@ -96,28 +96,32 @@ __global__ void __launch_bounds__(160, 1)
     for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
   int64_t cur_rg = u0 / G;
 
-  auto flush = [&](int64_t rg) -> bool {
+  int idx[MT * 4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
+      const int m = 2 * t + (i & 1) + 8 * mt;
+      idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
+    }
+  auto done = [&](int64_t rg, const float (&out)[MT * 4]) {
+#pragma unroll
+    for (int j = 0; j < MT * 4; ++j) {
+      if (idx[j] < 0) continue;
+      const int64_t n = rg * kRowGroup + idx[j] / 16;
+      const int m = idx[j] % 16;
+      if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+    }
+  };
+  RowGroupFinisher<float, MT * 4> fin(G, U, grid, cta, &ws);
+  auto flush = [&](int64_t rg) {
     float vals[MT * 4];
-    int idx[MT * 4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
-        const int m = 2 * t + (i & 1) + 8 * mt;
-        vals[mt * 4 + i] = acc[mt][i];
-        idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
-      }
-    auto done = [&](const float (&out)[MT * 4]) {
-#pragma unroll
-      for (int j = 0; j < MT * 4; ++j) {
-        if (idx[j] < 0) continue;
-        const int64_t n = rg * kRowGroup + idx[j] / 16;
-        const int m = idx[j] % 16;
-        if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
-      }
-    };
-    return finish_row_group<float, MT * 4>(rg, G, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+      for (int i = 0; i < 4; ++i) vals[mt * 4 + i] = acc[mt][i];
+    fin.stage(rg, vals, idx, done);
   };
 
   for (int i = 0; i < n_units; ++i) {
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(160, 1)
     const uint32_t ph = (uint32_t)(i / kStagesW4) & 1u;
     const int64_t rg = (u0 + i) / G;
     if (rg != cur_rg) {
-      if (!flush(cur_rg)) return;
+      flush(cur_rg);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -140,9 +144,10 @@ __global__ void __launch_bounds__(160, 1)
     const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
     const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0);
     const uint32_t zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
-    float c[MT][4];
+    // two accumulator chains per tile (even / odd k16 step) keep the MMA pipe busy
+    float c[2 * MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int mt = 0; mt < 2 * MT; ++mt)
 #pragma unroll
       for (int q = 0; q < 4; ++q) c[mt][q] = 0.f;
 #pragma unroll
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(160, 1)
           const uint16_t* xr = &sm.x[s][g + 8 * mt][0];
           const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + kk);
           const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + kk + 8);
-          mma_bf16(c[mt], a, b0, b1);
+          mma_bf16(c[2 * mt + (j & 1)], a, b0, b1);
         }
       }
     }
@@ -171,13 +176,16 @@ __global__ void __launch_bounds__(160, 1)
     if (lane == 0) mbar_arrive(&sm.empty[s]);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      acc[mt][0] += s0 * c[mt][0];
-      acc[mt][1] += s0 * c[mt][1];
-      acc[mt][2] += s1 * c[mt][2];
-      acc[mt][3] += s1 * c[mt][3];
+      acc[mt][0] += s0 * (c[2 * mt][0] + c[2 * mt + 1][0]);
+      acc[mt][1] += s0 * (c[2 * mt][1] + c[2 * mt + 1][1]);
+      acc[mt][2] += s1 * (c[2 * mt][2] + c[2 * mt + 1][2]);
+      acc[mt][3] += s1 * (c[2 * mt][3] + c[2 * mt + 1][3]);
     }
   }
-  if (n_units > 0) flush(cur_rg);
+  if (n_units > 0) {
+    flush(cur_rg);
+    fin.finish(idx, cs, sm.flags, done);
+  }
 }
 
 template <int MT>
@@ -197,7 +205,7 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT>, v, X, Y, M, ws);
@@ -207,6 +215,7 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
 
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
+  grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms);
   if (M <= 8) return launch_w4_mt<1>(v, X, Y, M, ws, grid, stream);
   return launch_w4_mt<2>(v, X, Y, M, ws, grid, stream);
 }

@@ -20,7 +20,7 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesW8 = 8;
+constexpr int kStagesW8 = 4;
 constexpr int kXStrideW8 = 72;  // staged qx row: 64 fp16 + 8 pad
 
 template <bool F16OUT>
@@ -93,7 +93,7 @@ struct W8Smem {
   uint64_t full[kStagesW8];
   uint64_t empty[kStagesW8];
   uint64_t cons_bar;
-  int flag;
+  int flags[2];
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -103,7 +103,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     w8_decode_kernel(W8View v, const uint16_t* __restrict__ q16, const float* __restrict__ sx,
                      uint16_t* __restrict__ Y, int32_t* __restrict__ acc_out, int M, Workspace ws) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -181,35 +181,39 @@ __global__ void __launch_bounds__(160, 1)
   };
   int64_t cur_rg = u0 / KB;
 
-  auto flush = [&](int64_t rg) -> bool {
+  int idx[MT * 4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
+      const int m = 2 * t + (i & 1) + 8 * mt;
+      idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
+    }
+  auto done = [&](int64_t rg, const int (&out)[MT * 4]) {
+#pragma unroll
+    for (int j = 0; j < MT * 4; ++j) {
+      if (idx[j] < 0) continue;
+      const int64_t n = rg * kRowGroup + idx[j] / 16;
+      const int m = idx[j] % 16;
+      if (n >= v.N) continue;
+      if (acc_out) {
+        acc_out[(int64_t)m * v.N + n] = out[j];
+      } else {
+        const float y = __fmul_rn(__fmul_rn(__int2float_rn(out[j]), sx[m]), v.sw[n]);
+        Y[(int64_t)m * v.N + n] = f2bf(y);
+      }
+    }
+  };
+  RowGroupFinisher<int, MT * 4> fin(KB, U, grid, cta, &ws);
+  auto flush = [&](int64_t rg) {
     drain();
     int vals[MT * 4];
-    int idx[MT * 4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
-        const int m = 2 * t + (i & 1) + 8 * mt;
-        vals[mt * 4 + i] = iacc[mt][i];
-        idx[mt * 4 + i] = (m < M) ? r * 16 + m : -1;
-      }
-    auto done = [&](const int (&out)[MT * 4]) {
-#pragma unroll
-      for (int j = 0; j < MT * 4; ++j) {
-        if (idx[j] < 0) continue;
-        const int64_t n = rg * kRowGroup + idx[j] / 16;
-        const int m = idx[j] % 16;
-        if (n >= v.N) continue;
-        if (acc_out) {
-          acc_out[(int64_t)m * v.N + n] = out[j];
-        } else {
-          const float y = __fmul_rn(__fmul_rn(__int2float_rn(out[j]), sx[m]), v.sw[n]);
-          Y[(int64_t)m * v.N + n] = f2bf(y);
-        }
-      }
-    };
-    return finish_row_group<int, MT * 4>(rg, KB, U, grid, cta, vals, idx, ws, cs, &sm.flag, done);
+      for (int i = 0; i < 4; ++i) vals[mt * 4 + i] = iacc[mt][i];
+    fin.stage(rg, vals, idx, done);
   };
 
   for (int i = 0; i < n_units; ++i) {
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(160, 1)
     const uint32_t ph = (uint32_t)(i / kStagesW8) & 1u;
     const int64_t rg = (u0 + i) / KB;
     if (rg != cur_rg) {
-      if (!flush(cur_rg)) return;
+      flush(cur_rg);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -250,7 +254,10 @@ __global__ void __launch_bounds__(160, 1)
     if (lane == 0) mbar_arrive(&sm.empty[s]);
     if (++since_drain == 16) drain();
   }
-  if (n_units > 0) flush(cur_rg);
+  if (n_units > 0) {
+    flush(cur_rg);
+    fin.finish(idx, cs, sm.flags, done);
+  }
 }
 
 template <int MT>
@@ -270,7 +277,7 @@ int launch_w8_mt(const W8View& v, const uint16_t* q16, const float* sx, uint16_t
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return (int)cudaLaunchKernelEx(&cfg, w8_decode_kernel<MT>, v, q16, sx, Y, acc, M, ws);
@@ -285,7 +292,7 @@ int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, flo
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx);
@@ -303,8 +310,9 @@ int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, f
 
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc_out, int M,
                      const Workspace& ws, int grid, void* stream) {
-  if (M <= 8) return launch_w8_mt<1>(v, q16, sx, Y, acc_out, M, ws, grid, stream);
-  return launch_w8_mt<2>(v, q16, sx, Y, acc_out, M, ws, grid, stream);
+  const int64_t U = (int64_t)v.RG * v.KB;
+  if (M <= 8) return launch_w8_mt<1>(v, q16, sx, Y, acc_out, M, ws, (int)std::min<int64_t>(U, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms), stream);
+  return launch_w8_mt<2>(v, q16, sx, Y, acc_out, M, ws, (int)std::min<int64_t>(U, (int64_t)std::min(3, QLIN_DECODE_CPS_MAX) * ws.sms), stream);
 }
 
 }  // namespace qlin

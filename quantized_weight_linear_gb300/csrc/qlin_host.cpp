@@ -903,6 +903,7 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
   h->wsv.qx = h->ws + w.qx;
   h->wsv.sx = reinterpret_cast<float*>(h->ws + w.sx);
   h->wsv.grid = h->grid;
+  h->wsv.sms = sm_count_cached();
   return QLIN_OK;
 }
 

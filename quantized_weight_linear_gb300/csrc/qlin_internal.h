@@ -89,8 +89,11 @@ struct Workspace {
   uint32_t* counters;  // [RG] arrival counters of split row groups
   void* qx;            // W8A8: fp16 activation codes [maxM][K]
   float* sx;           // W8A8: [maxM]
-  int grid;            // decode grid the partial slots were sized for
+  int grid;            // largest decode grid the partial slots were sized for
+  int sms;             // SM count of the device
 };
+
+constexpr int kMaxCtasPerSm = 4;  // decode kernels run up to 4 CTAs per SM
 
 // ---- kernel launchers (kern_*.cu); all asynchronous, return cudaError_t as int ----
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws,
