@@ -146,6 +146,23 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
  * (1 <= M <= 16) runs the fused dequant GEMV kernels; larger M runs the tensor-core path. */
 qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream);
 
+/* The SpQR decode forward (format SPQR, 1 <= M <= 16) without any workspace: for callers
+ * that are given only X and Y and may not allocate device memory -- a layer inside an engine
+ * that reserves all device memory for its own pools and hands plugins no workspace, or a
+ * service that forbids device allocation once it is serving.  The pages have no counterpart;
+ * this is a deployment form of qlin_forward, same kernel, same results.
+ * The scratch (partial sums of split row groups, their counters, a status word) is a fixed
+ * array inside the library, about 5.3 MB, held on every GPU that loads the library until the
+ * process exits; its address is looked up on the first call on each device, so make that
+ * first call before any stream capture.  Limits: at most 640 CTAs (the grid the kernel picks
+ * for the device) and N <= 524288; beyond them the call returns QLIN_ERR_WORKSPACE.  Each call
+ * clears the counters and status it uses first; the array is shared by every call, so calls
+ * whose kernels overlap on the GPU (other streams, other threads) race and must be
+ * serialized by the caller.  Device-side wait limits are enforced but not reported here
+ * (qlin_poll_status reads the handle's own workspace).  Allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library call. */
+qlin_status qlin_forward_spqr_static(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream);
+
 /* End-to-end form: copies X from host memory (X_host, pinned for full speed) into X_dev,
  * runs qlin_forward, copies Y_dev back into Y_host and waits for the stream. */
 qlin_status qlin_forward_host(qlin_handle h, const void* X_host, void* Y_host, void* X_dev,

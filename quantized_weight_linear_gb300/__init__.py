@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "qlin_pack_w4g128", "qlin_pack_spqr", "qlin_pack_w8", "qlin_device_bytes", "qlin_workspace_bytes",
     "qlin_bind", "qlin_attach", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
     "qlin_forward_acc", "qlin_dequant_device", "qlin_poll_status", "qlin_export", "qlin_info",
-    "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout",
+    "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout", "qlin_forward_spqr_static",
 )
 
 
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
             "qlin_status_string": ([i32], ctypes.c_char_p),
             "qlin_sm_count": ([], i32),
             "qlin_debug_wait_timeout": ([vp, i32, vp], i32),
+            "qlin_forward_spqr_static": ([H, vp, vp, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -218,6 +219,12 @@ def qlin_set_workspace(h: Handle, dev_ws, nbytes: int, max_M: int, stream=None):
 
 def qlin_forward(h: Handle, X, Y, M: int, stream=None):
     _check(lib().qlin_forward(h.ptr, _vp(X), _vp(Y), M, _stream(stream)), "qlin_forward")
+
+
+def qlin_forward_spqr_static(h: Handle, X, Y, M: int, stream=None):
+    """SpQR decode forward (1 <= M <= 16) that uses the library's fixed scratch array instead
+    of a workspace: for callers that may not allocate device memory (see include/qlin.h)."""
+    _check(lib().qlin_forward_spqr_static(h.ptr, _vp(X), _vp(Y), M, _stream(stream)), "qlin_forward_spqr_static")
 
 
 def qlin_forward_host(h: Handle, X_host, Y_host, X_dev, Y_dev, M: int, stream=None):

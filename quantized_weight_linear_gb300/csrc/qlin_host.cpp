@@ -724,9 +724,16 @@ static W8View w8view(const qlin_layer* L) {
                 reinterpret_cast<const float*>(L->dev + L->sec_sinv), L->N, L->K, L->RG, L->KU};
 }
 
+int qlin_spqr_view_of(qlin_layer* h, SpqrView* out) {
+  if (!h || !out || h->format != QLIN_FMT_SPQR) return QLIN_ERR_INVALID_ARG;
+  if (!h->dev) return QLIN_ERR_NOT_BOUND;
+  *out = spqrview(h);
+  return QLIN_OK;
+}
+
 static int decode_grid(const qlin_layer* L) {
   const int64_t units = (int64_t)L->RG * L->KU;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(units, sm_count_cached()));
+  return (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)kMaxCtasPerSm * sm_count_cached()));
 }
 
 // workspace carve-up

@@ -111,6 +111,16 @@ int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M
                         void* stream);
 int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc,
                       int M, int32_t* status, void* stream);
+int spqr_decode_grid(const SpqrView& v, int M, int sms);
+
+}  // namespace qlin
+
+// The SpQR device view of a bound handle: QLIN_OK, QLIN_ERR_INVALID_ARG (another format)
+// or QLIN_ERR_NOT_BOUND.  Defined with the handle in qlin_host.cpp.
+struct qlin_layer;
+int qlin_spqr_view_of(struct qlin_layer* h, qlin::SpqrView* out);
+
+namespace qlin {
 int launch_w4_dequant(const W4View& v, float* out, void* stream);
 int launch_spqr_dequant(const SpqrView& v, float* out, void* stream);
 int launch_w8_export(const W8View& v, int8_t* out, void* stream);
