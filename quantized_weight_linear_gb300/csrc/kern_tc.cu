@@ -5,17 +5,20 @@
 // batch grows the layer becomes compute-bound and the dequantization overhead is what
 // erodes weight-only speedups; W8A8 keeps both operands on the tensor cores.  Design:
 //
-// * CTA tile 128 (tokens, MMA M) x 128 (output rows, MMA N), K in blocks of 64;
+// * CTA tile: 128 output rows (MMA N) x 256 tokens (two 128-row MMAs that share each
+//   dequantized B tile, halving the dequantization per FLOP) for W4 / SpQR, x 128 tokens
+//   for W8A8; K in blocks of 64;
 // * warp 0: TMA producer -- X tiles through a 2-D tensor map (128B swizzle) and the packed
-//   weight units of the tile (the same device image the decode kernels stream) through
-//   cp.async.bulk into a packed ring;
+//   weight units of the tile (the device image the decode kernels stream; SpQR: plus the
+//   unit's outlier buckets) through cp.async.bulk into a packed ring;
 // * warp 1: allocates TMEM and issues tcgen05.mma (kind::f16, bf16 or fp16 operands, fp32
-//   accumulator in TMEM) from one elected thread, committing each k-block back to its
+//   accumulators in TMEM) from one elected thread, committing each k-block back to its
 //   shared-memory stage;
-// * warps 2-5: converters -- turn packed codes into the bf16 / fp16 K-major 128B-swizzled
-//   B operand, then run the epilogue (tcgen05.ld -> bf16 -> Y);
-// * W8A8 only, warps 6-9: exactness drain -- int8 x int8 products are exact in fp16 MMA and
-//   every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (two TMEM
+// * converter warps (8 for W4 / SpQR, 4 for W8A8): turn packed codes into the bf16 / fp16
+//   K-major 128B-swizzled B operand; for W4 / SpQR they then run the epilogue
+//   (tcgen05.ld -> bf16 -> Y);
+// * W8A8 only, 4 more warps: exactness drain -- int8 x int8 products are exact in the fp16
+//   MMA and every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (two TMEM
 //   regions, double-buffered) are exact integers; these warps add them into int32 registers
 //   while the MMA runs the next chunk, and write y = bf16((acc * sx) * sw) (or acc).
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
@@ -27,11 +30,12 @@
 namespace qlin {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kNST = 4;     // A/B operand stages
-constexpr int kNPK = 2;     // packed-weight stages
-constexpr int kTileBytes = kBM * kBK * 2;  // 16 KB, one operand tile
+constexpr int kBN = 128, kBK = 64;
+constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
+constexpr int kNPK = 2;                    // packed-weight stages
 constexpr int kChunkBlocks = 16;           // W8A8: 16 k-blocks = 1024 K per exact chunk
+constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
+constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
 
 enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 
@@ -39,31 +43,34 @@ template <int F>
 struct TcCfg;
 template <>
 struct TcCfg<kW4> {
-  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2;
+  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = 3;
   static constexpr uint32_t kAType = 1;  // bf16
 };
 template <>
 struct TcCfg<kSpqr> {
-  static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4;
+  static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4, kMH = 2, kConv = 8, kStages = 3;
   static constexpr uint32_t kAType = 1;
 };
 template <>
 struct TcCfg<kW8> {
-  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1;
+  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 1, kConv = 4, kStages = 4;
   static constexpr uint32_t kAType = 0;  // fp16
 };
 
 template <int F>
 struct TcSmem {
-  __align__(1024) uint8_t a[kNST][kTileBytes];
-  __align__(1024) uint8_t b[kNST][kTileBytes];
-  __align__(16) uint8_t pk[kNPK][2 * TcCfg<F>::kUnitBytes];
-  uint64_t ab_full[kNST], ab_empty[kNST];
+  using C = TcCfg<F>;
+  __align__(1024) uint8_t a[C::kStages][C::kMH * kTileBytes];
+  __align__(1024) uint8_t b[C::kStages][kTileBytes];
+  __align__(16) uint8_t pk[kNPK][2 * C::kUnitBytes];
+  __align__(16) uint32_t out[F == kSpqr ? kNPK : 1][2][F == kSpqr ? kOutCapTc + 8 : 4];
+  __align__(16) uint32_t offs[2][F == kSpqr ? kOffsCapTc : 4];
+  uint64_t ab_full[C::kStages], ab_empty[C::kStages];
   uint64_t pk_full[kNPK], pk_empty[kNPK];
+  uint64_t offs_bar;
   uint64_t acc_full;
   uint64_t ch_full[2], ch_empty[2];
   uint32_t tmem;
-  int abort;
 };
 
 struct TcArgs {
@@ -179,138 +186,131 @@ __device__ __forceinline__ void sp_write_j(uint8_t* bt, const uint32_t (&w)[6], 
   sts32(bt, sw128(rowB, k), vB);
 }
 
-// ---- converters: one 32-row slice of the 128-row B tile for k-block kb of the packed stage
+// ---- converters: one 16-row tile of the 128-row B tile for k-block kb of the packed stage
 
 template <int F>
-__device__ __forceinline__ void convert_block(uint8_t* bt, const uint8_t* pk, int kb, int cw, int lane, bool rg_valid) {
+__device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, int kb, int rt, int row0, int lane,
+                                             bool valid) {
   const int g = lane >> 2, t = lane & 3;
-  const int rg_local = cw >> 1;
-  const uint8_t* unit = pk + rg_local * TcCfg<F>::kUnitBytes;
+  if (!valid) {  // rows past N: zero operand
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int rt = 2 * (cw & 1) + h;                // row tile inside the unit's row group
-    const int row0 = 32 * cw + 16 * h;              // first tile row in the B tile
-    if (!rg_valid) {
-      // rows past N: zero operand
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
+      for (int kk = 0; kk < 8; ++kk) sts32(bt, sw128(row0 + g + 8 * r, 8 * kk + 2 * t), 0u);
+    return;
+  }
+  if constexpr (F == kW4) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + kb) * 32 + lane) * 16);
+    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+    const uint32_t* st = reinterpret_cast<const uint32_t*>(unit + kW4CodeBytes);
+    const uint32_t sz0 = st[rt * 16 + g], sz1 = st[rt * 16 + g + 8];
+    const float s0 = h2f_dev((uint16_t)(sz0 & 0xFFFFu)), s1 = h2f_dev((uint16_t)(sz1 & 0xFFFFu));
+    const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
+    const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0), zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
+    const uint32_t sp0 = pack_bf16x2(s0, s0), sp1 = pack_bf16x2(s1, s1);
+    const uint32_t zero = 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) sts32(bt, sw128(row0 + g + 8 * r, 8 * kk + 2 * t), 0u);
-      continue;
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w = words[j];
+      const int k = 16 * j + 2 * t;
+      sts32(bt, sw128(row0 + g, k), bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+      sts32(bt, sw128(row0 + g + 8, k), bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
+      sts32(bt, sw128(row0 + g, k + 8), bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+      sts32(bt, sw128(row0 + g + 8, k + 8),
+            bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
     }
-    if constexpr (F == kW4) {
-      const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + kb) * 32 + lane) * 16);
-      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-      const uint32_t* st = reinterpret_cast<const uint32_t*>(unit + kW4CodeBytes);
-      const uint32_t sz0 = st[rt * 16 + g], sz1 = st[rt * 16 + g + 8];
-      const float s0 = h2f_dev((uint16_t)(sz0 & 0xFFFFu)), s1 = h2f_dev((uint16_t)(sz1 & 0xFFFFu));
-      const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
-      const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0), zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
-      const uint32_t sp0 = pack_bf16x2(s0, s0), sp1 = pack_bf16x2(s1, s1);
-      const uint32_t zero = 0u;
+  } else if constexpr (F == kW8) {
+    const uint8_t* src = unit + (rt * 32 + lane) * 32;
+    const uint4 w01 = *reinterpret_cast<const uint4*>(src);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(src + 16);
+    const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+    const uint32_t magic = 0x64646464u, off = 0x64806480u;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t w = words[j];
-        const int k = 16 * j + 2 * t;
-        sts32(bt, sw128(row0 + g, k), bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
-        sts32(bt, sw128(row0 + g + 8, k),
-              bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
-        sts32(bt, sw128(row0 + g, k + 8),
-              bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
-        sts32(bt, sw128(row0 + g + 8, k + 8),
-              bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
-      }
-    } else if constexpr (F == kW8) {
-      const uint8_t* src = unit + (rt * 32 + lane) * 32;
-      const uint4 w01 = *reinterpret_cast<const uint4*>(src);
-      const uint4 w23 = *reinterpret_cast<const uint4*>(src + 16);
-      const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
-      const uint32_t magic = 0x64646464u, off = 0x64806480u;
+    for (int j = 0; j < 4; ++j) {
+      const int k = 16 * j + 2 * t;
+      uint32_t d;
+      asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+      sts32(bt, sw128(row0 + g, k), f16x2_sub(d, off));
+      asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+      sts32(bt, sw128(row0 + g + 8, k), f16x2_sub(d, off));
+      asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+      sts32(bt, sw128(row0 + g, k + 8), f16x2_sub(d, off));
+      asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+      sts32(bt, sw128(row0 + g + 8, k + 8), f16x2_sub(d, off));
+    }
+  } else {  // SpQR: k-block kb of the 256-wide unit = block kb/2, groups 4*(kb%2) .. +3
+    const int blk = kb >> 1, half = kb & 1;
+    const uint32_t* cw6 = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
+    uint32_t w[6];
+    {
+      const uint2 p0 = *reinterpret_cast<const uint2*>(cw6);
+      const uint2 p1 = *reinterpret_cast<const uint2*>(cw6 + 2);
+      const uint2 p2 = *reinterpret_cast<const uint2*>(cw6 + 4);
+      w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
+    }
+    const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+    const uint16_t* sgst = reinterpret_cast<const uint16_t*>(unit + kSpqrCodeBytes + kSpqrQsqzBytes);
+    uint32_t sh[2], ch[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k = 16 * j + 2 * t;
-        uint32_t d;
-        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
-        sts32(bt, sw128(row0 + g, k), f16x2_sub(d, off));
-        asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
-        sts32(bt, sw128(row0 + g + 8, k), f16x2_sub(d, off));
-        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
-        sts32(bt, sw128(row0 + g, k + 8), f16x2_sub(d, off));
-        asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
-        sts32(bt, sw128(row0 + g + 8, k + 8), f16x2_sub(d, off));
-      }
-    } else {  // SpQR: k-block kb of the 256-wide unit = block kb/2, groups 4*(kb%2) .. +3
-      const int blk = kb >> 1, half = kb & 1;
-      const uint32_t* cw6 = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
-      uint32_t w[6];
-#pragma unroll
-      for (int x = 0; x < 6; ++x) w[x] = cw6[x];
-      const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
-      const uint16_t* sgst = reinterpret_cast<const uint16_t*>(unit + kSpqrCodeBytes + kSpqrQsqzBytes);
-      uint32_t sh[2], ch[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = g + 8 * r, gb = t + 4 * half;
-        const uint16_t* st = sgst + (rt * 16 + row) * 4;
-        const uint32_t e = sp_qsqz(qarea, row, gb);
-        const float s_hat = __fmul_rn(__fsub_rn((float)(e & 7u), h2f_dev(st[1])), h2f_dev(st[0]));
-        const float z_hat = __fmul_rn(__fsub_rn((float)(e >> 3), h2f_dev(st[3])), h2f_dev(st[2]));
-        sh[r] = pack_bf16x2(s_hat, s_hat);
-        const float c = -s_hat * z_hat;
-        ch[r] = pack_bf16x2(c, c);
-      }
-      const int rowA = row0 + g, rowB = row0 + g + 8;
-      if (half == 0) {
-        sp_write_j<0, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<1, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<2, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<3, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<4, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<5, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<6, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<7, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      } else {
-        sp_write_j<0, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<1, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<2, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<3, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<4, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<5, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<6, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-        sp_write_j<7, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      }
+    for (int r = 0; r < 2; ++r) {
+      const int row = g + 8 * r, gb = t + 4 * half;
+      const uint16_t* st = sgst + (rt * 16 + row) * 4;
+      const uint32_t e = sp_qsqz(qarea, row, gb);
+      const float s_hat = __fmul_rn(__fsub_rn((float)(e & 7u), h2f_dev(st[1])), h2f_dev(st[0]));
+      const float z_hat = __fmul_rn(__fsub_rn((float)(e >> 3), h2f_dev(st[3])), h2f_dev(st[2]));
+      sh[r] = pack_bf16x2(s_hat, s_hat);
+      const float c = -s_hat * z_hat;
+      ch[r] = pack_bf16x2(c, c);
+    }
+    const int rowA = row0 + g, rowB = row0 + g + 8;
+    if (half == 0) {
+      sp_write_j<0, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<1, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<2, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<3, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<4, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<5, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<6, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<7, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+    } else {
+      sp_write_j<0, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<1, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<2, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<3, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<4, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<5, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<6, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<7, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
     }
   }
 }
 
-// SpQR outliers of a (row group, supergroup) unit that fall into k-block kb, for the two
-// row tiles rt0, rt0 + 1 a converter warp owns: added onto the dequantized bf16 operand
-// (D + s, rounded once more to bf16).  Only the warp that wrote those rows touches them.
-__device__ __forceinline__ void spqr_outliers_block(uint8_t* bt, const TcArgs& a, int64_t rg, int64_t sg, int kb,
-                                                    int rt0, int rows_base, int lane) {
-  const int64_t u = rg * a.KU + sg;
-  const uint32_t e0 = __ldg(a.offs + 4 * u + rt0), emid = __ldg(a.offs + 4 * u + rt0 + 1);
-  const uint32_t e1 = __ldg(a.offs + 4 * u + rt0 + 2);
-  for (uint32_t p = e0 + lane; p < e1; p += 32) {
-    const uint32_t e = __ldg(a.ents + p);
+// SpQR outliers of one (unit, row tile) bucket that fall into k-block kb, added onto the
+// dequantized bf16 operand (D + s rounded once more to bf16).  Entries come from the staged
+// copy when the unit's buckets fit, else from global memory.  Only the warp that wrote
+// those rows touches them, and every outlier position is unique, so the read-modify-write
+// is race free.
+__device__ __forceinline__ void spqr_outliers_tile(uint8_t* bt, const uint32_t* staged, uint32_t stage_base,
+                                                   const uint32_t* ents, uint32_t b0, uint32_t b1, int kb, int row0,
+                                                   int lane) {
+  for (uint32_t p = b0 + lane; p < b1; p += 32) {
+    const uint32_t e = staged ? staged[p - stage_base] : __ldg(ents + p);
     const int kin = (int)((e >> 4) & 255u);
     if ((kin >> 6) != kb) continue;
-    const int row = rows_base + (p >= emid ? 16 : 0) + (int)(e & 15u);
-    const uint32_t off = sw128(row, kin & 63);
-    uint16_t* dst = reinterpret_cast<uint16_t*>(bt + off);
-    // each outlier position is unique, so plain read-modify-write is race free
-    const float v = __fadd_rn(bf2f(*dst), h2f_dev((uint16_t)(e >> 16)));
-    *dst = f2bf(v);
+    const int row = row0 + (int)(e & 15u);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(bt + sw128(row, kin & 63));
+    *dst = f2bf(__fadd_rn(bf2f(*dst), h2f_dev((uint16_t)(e >> 16))));
   }
 }
 
 template <int F>
-__global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+__global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcSmem<F>& sm = *reinterpret_cast<TcSmem<F>*>(base);
   using C = TcCfg<F>;
+  constexpr int MH = C::kMH, NCONV = C::kConv, NST = C::kStages;
+  constexpr int BM = 128 * MH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, m_tile = blockIdx.y;
   const int64_t rg0 = (int64_t)n_tile * 2;  // two 64-row groups per 128-row tile
@@ -318,31 +318,41 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
   const int bpu = C::kBlocksPerUnit;
   const int nunits = nkb / bpu;
   const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
-  constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, kBM);
-  constexpr int nconv = 4;
+  constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, 128);
+  constexpr uint32_t tmem_cols = F == kW8 ? 256u : 128u * MH;
+  // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
+  int64_t off_base[2] = {0, 0};
+  uint32_t off_len[2] = {0, 0};
+  if constexpr (F == kSpqr) {
+    for (int r = 0; r < 2; ++r) {
+      const int64_t b = ((rg0 + r) * a.KU * 4) & ~int64_t(3);
+      const int64_t e = ((rg0 + r) * a.KU * 4 + 4 * a.KU + 1 + 3) & ~int64_t(3);
+      off_base[r] = b;
+      off_len[r] = (rg0 + r < a.RG) ? (uint32_t)(e - b) : 0u;
+    }
+  }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNST; ++s) {
-      mbar_init(&sm.ab_full[s], 1 + nconv);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.ab_full[s], 1 + NCONV);
       mbar_init(&sm.ab_empty[s], 1);
     }
     for (int s = 0; s < kNPK; ++s) {
       mbar_init(&sm.pk_full[s], 1);
-      mbar_init(&sm.pk_empty[s], nconv);
+      mbar_init(&sm.pk_empty[s], NCONV);
     }
+    mbar_init(&sm.offs_bar, 1);
     mbar_init(&sm.acc_full, 1);
     for (int r = 0; r < 2; ++r) {
       mbar_init(&sm.ch_full[r], 1);
       mbar_init(&sm.ch_empty[r], 4);
     }
-    sm.abort = 0;
     fence_mbar_init();
     pdl_launch_dependents();
   }
   if (warp == 1) {
-    const uint32_t cols = F == kW8 ? 256u : 128u;
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
-                 "r"(cols)
+                 "r"(tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -351,22 +361,47 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
   bool ok = true;
+  auto soffs = [&](int r, int64_t gi) -> uint32_t { return sm.offs[r][gi - off_base[r]]; };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
+      if constexpr (F == kSpqr) {
+        uint32_t bytes = 0;
+        for (int r = 0; r < 2; ++r) bytes += off_len[r] * 4;
+        mbar_arrive_expect_tx(&sm.offs_bar, bytes);
+        for (int r = 0; r < 2; ++r)
+          if (off_len[r]) bulk_g2s(sm.offs[r], a.offs + off_base[r], off_len[r] * 4, &sm.offs_bar);
+        ok = mbar_wait(&sm.offs_bar, 0, a.status);
+      }
       auto load_units = [&](int ui) -> bool {
         const int p = ui % kNPK;
         const uint32_t ph = (uint32_t)(ui / kNPK) & 1u;
         if (!mbar_wait(&sm.pk_empty[p], ph ^ 1u, a.status)) return false;
         uint32_t bytes = 0;
-        for (int r = 0; r < 2; ++r)
-          if (rg0 + r < a.RG) bytes += C::kUnitBytes;
+        uint32_t e_lo[2] = {0, 0}, e_hi[2] = {0, 0};
+        for (int r = 0; r < 2; ++r) {
+          if (rg0 + r >= a.RG) continue;
+          bytes += C::kUnitBytes;
+          if constexpr (F == kSpqr) {
+            const int64_t u = (rg0 + r) * a.KU + ui;
+            const uint32_t e0 = soffs(r, 4 * u), e1 = soffs(r, 4 * u + 4);
+            if (e1 > e0 && e1 - e0 <= (uint32_t)kOutCapTc) {
+              e_lo[r] = e0 & ~3u;
+              e_hi[r] = (e1 + 3u) & ~3u;
+              bytes += (e_hi[r] - e_lo[r]) * 4;
+            }
+          }
+        }
         mbar_arrive_expect_tx(&sm.pk_full[p], bytes);
-        for (int r = 0; r < 2; ++r)
-          if (rg0 + r < a.RG)
-            bulk_g2s(sm.pk[p] + r * C::kUnitBytes, a.units + ((rg0 + r) * a.KU + ui) * (int64_t)C::kUnitBytes,
-                     C::kUnitBytes, &sm.pk_full[p]);
+        for (int r = 0; r < 2; ++r) {
+          if (rg0 + r >= a.RG) continue;
+          bulk_g2s(sm.pk[p] + r * C::kUnitBytes, a.units + ((rg0 + r) * a.KU + ui) * (int64_t)C::kUnitBytes,
+                   C::kUnitBytes, &sm.pk_full[p]);
+          if constexpr (F == kSpqr) {
+            if (e_hi[r] > e_lo[r]) bulk_g2s(sm.out[p][r], a.ents + e_lo[r], (e_hi[r] - e_lo[r]) * 4, &sm.pk_full[p]);
+          }
+        }
         return true;
       };
       // weights do not depend on the previous kernel: prefetch before the dependency wait
@@ -379,14 +414,14 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
           ++next_unit;
           if (!ok) break;
         }
-        const int s = i % kNST;
-        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        const int s = i % NST;
+        const uint32_t ph = (uint32_t)(i / NST) & 1u;
         if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.ab_full[s], kTileBytes);
-        tma_load_2d(sm.a[s], &xmap, i * kBK, m_tile * kBM, &sm.ab_full[s]);
+        mbar_arrive_expect_tx(&sm.ab_full[s], MH * kTileBytes);
+        tma_load_2d(sm.a[s], &xmap, i * kBK, m_tile * BM, &sm.ab_full[s]);
       }
     }
   } else if (warp == 1) {
@@ -394,8 +429,8 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
     pdl_wait();
     if (lane == 0) {
       for (int i = 0; i < nkb && ok; ++i) {
-        const int s = i % kNST;
-        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        const int s = i % NST;
+        const uint32_t ph = (uint32_t)(i / NST) & 1u;
         uint32_t dcol = 0;
         bool first = (i == 0);
         if constexpr (F == kW8) {
@@ -414,11 +449,15 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t da = umma_desc_sw128(sm.a[s]);
         const uint64_t db = umma_desc_sw128(sm.b[s]);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_f16(tmem + dcol, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        for (int mh = 0; mh < MH; ++mh) {
+          const uint64_t da = umma_desc_sw128(sm.a[s] + mh * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16(tmem + dcol + 128u * mh, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc,
+                     (first && kk == 0) ? 0u : 1u);
+        }
         umma_commit(&sm.ab_empty[s]);
         if constexpr (F == kW8) {
           if ((i % kChunkBlocks) == kChunkBlocks - 1 || i == nkb - 1) umma_commit(&sm.ch_full[(i / kChunkBlocks) & 1]);
@@ -427,30 +466,45 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
       umma_commit(&sm.acc_full);
     }
     __syncwarp();
-  } else if (warp < 2 + nconv) {
-    // ------------------------------------------------------------------ converters + epilogue
+  } else if (warp < 2 + NCONV) {
+    // ------------------------------------------------------------------ converters (+ epilogue)
     pdl_wait();
     const int cw = warp - 2;
-    const bool rg_valid = rg0 + (cw >> 1) < a.RG;
+    constexpr int RPW = 128 / NCONV;  // rows per converter warp: 16 or 32
+    const int rg_local = (cw * RPW) / 64;
+    const bool rg_valid = rg0 + rg_local < a.RG;
+    if constexpr (F == kSpqr) {
+      if (!mbar_wait(&sm.offs_bar, 0, a.status)) ok = false;
+    }
     for (int ui = 0; ui < nunits && ok; ++ui) {
       const int p = ui % kNPK;
       if (!mbar_wait(&sm.pk_full[p], (uint32_t)(ui / kNPK) & 1u, a.status)) {
         ok = false;
         break;
       }
+      const uint8_t* unit = sm.pk[p] + rg_local * C::kUnitBytes;
       for (int b = 0; b < bpu; ++b) {
         const int i = ui * bpu + b;
-        const int s = i % kNST;
-        const uint32_t ph = (uint32_t)(i / kNST) & 1u;
+        const int s = i % NST;
+        const uint32_t ph = (uint32_t)(i / NST) & 1u;
         if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
           ok = false;
           break;
         }
-        convert_block<F>(sm.b[s], sm.pk[p], b, cw, lane, rg_valid);
-        if constexpr (F == kSpqr) {
-          if (rg_valid) {
-            __syncwarp();
-            spqr_outliers_block(sm.b[s], a, rg0 + (cw >> 1), ui, b, 2 * (cw & 1), 32 * cw, lane);
+#pragma unroll
+        for (int h = 0; h < RPW / 16; ++h) {
+          const int row0 = cw * RPW + 16 * h;
+          const int rt = (row0 % 64) / 16;
+          convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid);
+          if constexpr (F == kSpqr) {
+            if (rg_valid) {
+              __syncwarp();
+              const int64_t u = (rg0 + rg_local) * a.KU + ui;
+              const uint32_t e0 = soffs(rg_local, 4 * u), e1 = soffs(rg_local, 4 * u + 4);
+              const bool staged = e1 > e0 && e1 - e0 <= (uint32_t)kOutCapTc;
+              spqr_outliers_tile(sm.b[s], staged ? sm.out[p][rg_local] : nullptr, e0 & ~3u, a.ents,
+                                 soffs(rg_local, 4 * u + rt), soffs(rg_local, 4 * u + rt + 1), b, row0, lane);
+            }
           }
         }
         fence_proxy_async_smem();
@@ -461,29 +515,29 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
       if (lane == 0) mbar_arrive(&sm.pk_empty[p]);
     }
     if constexpr (F != kW8) {
-      // epilogue: TMEM lane quadrant = warp % 4
+      // epilogue: TMEM lane quadrant q = warp % 4; the two warps of a quadrant take one
+      // 128-token half each
       const int q = warp & 3;
+      const int mh = cw / 4;
       if (ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
         tc_fence_after();
-        const int m = m_tile * kBM + 32 * q + lane;
+        const int m = m_tile * BM + 128 * mh + 32 * q + lane;
         const int n0 = n_tile * kBN;
 #pragma unroll
         for (int cb = 0; cb < kBN / 32; ++cb) {
           uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * cb, r);
-          if (m < a.M) {
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128u * mh + 32u * cb, r);
+          // N is a multiple of 64 rows (the device image pads row groups), so a 32-column
+          // slice is either fully inside or fully outside the output
+          const int n = n0 + 32 * cb;
+          if (m < a.M && n + 32 <= a.N) {
             uint32_t pk16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            const int n = n0 + 32 * cb;
             uint16_t* dst = a.Y + (int64_t)m * a.N + n;
-            // N is a multiple of 64 rows (the device image pads row groups), so a 32-column
-            // slice is either fully inside or fully outside the output
-            if (n + 32 <= a.N) {
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
-            }
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
           }
         }
       }
@@ -512,7 +566,7 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.ch_empty[c & 1]);
     }
-    const int m = m_tile * kBM + 32 * q + lane;
+    const int m = m_tile * BM + 32 * q + lane;
     if (ok && m < a.M) {
       const int n0 = n_tile * kBN;
       // N is a multiple of 64, so each 64-column half of the tile is fully in or out
@@ -540,8 +594,7 @@ __global__ void __launch_bounds__(F == kW8 ? 320 : 192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    const uint32_t cols = F == kW8 ? 256u : 128u;
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
 }
 
@@ -559,12 +612,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 template <int F>
 int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
+  using C = TcCfg<F>;
+  constexpr int BM = 128 * C::kMH;
+  if constexpr (F == kSpqr) {
+    if (4 * (int64_t)args.KU + 8 > kOffsCapTc) return (int)cudaErrorInvalidValue;  // K > 65536: not staged
+  }
   auto enc = get_encode();
   if (!enc) return (int)cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.M};
   const cuuint64_t strides[1] = {(cuuint64_t)args.K * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t box[2] = {kBK, (cuuint32_t)BM};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = F == kW8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(&map, dt, 2, const_cast<void*>(Xop), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -578,8 +636,8 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((args.N + kBN - 1) / kBN), (unsigned)((args.M + kBM - 1) / kBM));
-  cfg.blockDim = dim3(F == kW8 ? 320 : 192);
+  cfg.gridDim = dim3((unsigned)((args.N + kBN - 1) / kBN), (unsigned)((args.M + BM - 1) / BM));
+  cfg.blockDim = dim3(320);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
