@@ -56,9 +56,12 @@ struct RowGroupFinisher {
     if (npend < 2) pend[npend++] = rg;
   }
 
-  // Returns false if a bounded wait gave up.  `flags` is a 2-int shared array.
-  template <typename Done>
-  __device__ __forceinline__ bool finish(const int (&idx)[NV], ConsumerSync& cs, int* flags, Done done) {
+  // Returns false if a bounded wait gave up.  `flags` is a 2-int shared array.  The last
+  // contributor reduces with all 128 consumer threads: thread j takes entries j, j + 128, ...
+  // of the 64 x M outputs and loads the contributors' slots eight at a time (one round trip
+  // per eight CTAs), summing them in CTA order.  `put(rg, entry, value)` stores one output.
+  template <typename Put>
+  __device__ __forceinline__ bool finish(int M, ConsumerSync& cs, int* flags, Put put) {
     if (npend == 0) return true;  // uniform: every consumer thread walks the same row groups
     __threadfence();
     if (!cs.sync()) return false;
@@ -73,19 +76,27 @@ struct RowGroupFinisher {
     for (int p = 0; p < npend; ++p) {
       if (!flags[p]) continue;
       __threadfence();
-      const SplitInfo si = split_info(pend[p], per_rg, units, grid);
-      T sum[NV];
+      const int64_t rg = pend[p];
+      const SplitInfo si = split_info(rg, per_rg, units, grid);
+      const T* base = reinterpret_cast<const T*>(ws->partials);
+      for (int lin = threadIdx.x; lin < kRowGroup * M; lin += 128) {
+        const int e = (lin / M) * 16 + lin % M;
+        T s = T(0);
+        for (int64_t c0 = si.first_cta; c0 <= si.last_cta; c0 += 8) {
+          T v[8];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) sum[i] = T(0);
-      for (int64_t c = si.first_cta; c <= si.last_cta; ++c) {
-        const int sd = split_side(c, pend[p], per_rg, units, grid);
-        const T* sl = reinterpret_cast<const T*>(ws->partials) + (c * 2 + sd) * (kRowGroup * 16);
+          for (int u = 0; u < 8; ++u) {
+            const int64_t c = c0 + u;
+            v[u] = T(0);
+            if (c <= si.last_cta)
+              v[u] = __ldcg(base + (c * 2 + split_side(c, rg, per_rg, units, grid)) * (kRowGroup * 16) + e);
+          }
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-          if (idx[i] >= 0) sum[i] += __ldcg(sl + idx[i]);
+          for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        put(rg, e, s);
       }
-      done(pend[p], sum);
-      if (threadIdx.x == 0) ws->counters[pend[p]] = 0u;
+      if (threadIdx.x == 0) ws->counters[rg] = 0u;
     }
     return true;
   }

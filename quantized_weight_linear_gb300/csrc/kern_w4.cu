@@ -184,7 +184,10 @@ __global__ void __launch_bounds__(160, 4)
   }
   if (n_units > 0) {
     flush(cur_rg);
-    fin.finish(idx, cs, sm.flags, done);
+    fin.finish(M, cs, sm.flags, [&](int64_t rg, int e, float val) {
+      const int64_t n = rg * kRowGroup + e / 16;
+      if (n < v.N) Y[(int64_t)(e % 16) * v.N + n] = f2bf(val);
+    });
   }
 }
 

@@ -256,7 +256,16 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
   }
   if (n_units > 0) {
     flush(cur_rg);
-    fin.finish(idx, cs, sm.flags, done);
+    fin.finish(M, cs, sm.flags, [&](int64_t rg, int e, int val) {
+      const int64_t n = rg * kRowGroup + e / 16;
+      const int m = e % 16;
+      if (n >= v.N) return;
+      if (acc_out) {
+        acc_out[(int64_t)m * v.N + n] = val;
+      } else {
+        Y[(int64_t)m * v.N + n] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn(val), sx[m]), v.sw[n]));
+      }
+    });
   }
 }
 
