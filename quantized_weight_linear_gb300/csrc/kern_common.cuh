@@ -98,6 +98,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   return false;
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// 16-byte load through L2 only (data written by other SMs in this launch)
+__device__ __forceinline__ void ldcg4(const float* p, float (&v)[4]) {
+  const float4 q = __ldcg(reinterpret_cast<const float4*>(p));
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+__device__ __forceinline__ void ldcg4(const int* p, int (&v)[4]) {
+  const int4 q = __ldcg(reinterpret_cast<const int4*>(p));
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+
 // Upper bound on the CTAs per SM the decode launches use (their occupancy allows up to 4).
 #ifndef QLIN_DECODE_CPS_MAX
 #define QLIN_DECODE_CPS_MAX 4

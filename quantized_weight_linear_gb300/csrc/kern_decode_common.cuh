@@ -19,84 +19,140 @@ struct ConsumerSync {
   }
 };
 
-// Completion of row groups (64 rows x up to 16 tokens) whose units are split between CTAs.
-// A CTA's contiguous unit range can split at most two row groups (its first and its last);
-// every other row group it touches is whole and is written straight away.
-//
-// stage(): a whole row group goes to `done` at once; a split one is stored into this CTA's
-// partial slot (plain stores, nothing waits).  finish(), once at the end of the range: one
-// fence, one arrival per split row group on its counter, and the last contributor sums all
-// slots in CTA order (deterministic) and hands the sums to `done`, then resets the counter
-// for the next forward.  So no consumer ever stalls on another CTA in the middle of its
-// stream.  `vals[i]` is the value of entry idx[i] = row_in_group * 16 + token (idx < 0:
-// unused).  T is float or int (integer sums are exact).
-template <typename T, int NV>
-struct RowGroupFinisher {
-  int64_t per_rg, units, grid, cta;
-  const Workspace* ws;
-  int64_t pend[2];
-  int npend;
+// Row group of the current unit in a CTA's contiguous range, advanced without a division.
+struct UnitCursor {
+  int64_t rg;
+  int k;    // unit index inside the row group
+  int per;  // units per row group
+  __device__ __forceinline__ void next() {
+    if (++k == per) {
+      k = 0;
+      ++rg;
+    }
+  }
+};
 
-  __device__ __forceinline__ RowGroupFinisher(int64_t per_rg_, int64_t units_, int64_t grid_, int64_t cta_,
+// Completion of row groups (64 rows x up to 16 tokens) whose units are split between CTAs.
+// A CTA's contiguous unit range can share at most two row groups with other CTAs (its first
+// and its last); every other row group it touches is whole and is written straight away.
+// Which of the two are shared, by how many CTAs, and where the first contributor keeps its
+// partial sums is worked out once, when the finisher is built (before the stream starts).
+//
+// stage(): a whole row group goes to `done` at once; a shared one is stored into this CTA's
+// partial slot (plain stores, nothing waits).  finish(), once at the end of the range: one
+// arrival per shared row group on its counter, and the CTA that arrives last sums all slots
+// in CTA order (deterministic) and hands the sums to `put`, then resets the counter for the
+// next forward.  So no consumer ever stalls on another CTA in the middle of its stream.
+// `vals[i]` is the value of entry idx[i] = row_in_group * 16 + token (idx < 0: unused).
+// T is float or int (integer sums are exact).  kRedBatch contributors are loaded per L2
+// round trip in the reduction.
+template <typename T, int NV, int kRedBatch = 8>
+struct RowGroupFinisher {
+  const Workspace* ws;
+  int cta;
+  int rg[2];          // shared row groups: [0] the first of the range, [1] the last (-1: none)
+  int first_cta[2];   // their first contributor
+  int first_slot[2];  // and the slot that contributor stored into
+  int ncontrib[2];    // number of contributors
+  int pend;           // bit s: rg[s] has been staged
+
+  __device__ __forceinline__ RowGroupFinisher(int64_t per_rg, int64_t units, int64_t grid, int64_t cta_,
                                               const Workspace* ws_)
-      : per_rg(per_rg_), units(units_), grid(grid_), cta(cta_), ws(ws_), npend(0) {}
+      : ws(ws_), cta((int)cta_), pend(0) {
+    const int64_t u0 = split_start(cta_, units, grid), u1 = split_start(cta_ + 1, units, grid);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      rg[s] = -1;
+      first_cta[s] = first_slot[s] = ncontrib[s] = 0;
+      if (u1 <= u0) continue;
+      const int64_t r = (s == 0 ? u0 : u1 - 1) / per_rg;
+      if (s == 1 && r == u0 / per_rg) continue;
+      const SplitInfo si = split_info(r, per_rg, units, grid);
+      if (si.first_cta == si.last_cta) continue;
+      rg[s] = (int)r;
+      first_cta[s] = (int)si.first_cta;
+      ncontrib[s] = (int)(si.last_cta - si.first_cta + 1);
+      // only the first contributor can have the row group as its second one (slot side 1)
+      first_slot[s] = (int)(si.first_cta * 2 + (split_start(si.first_cta, units, grid) < r * per_rg ? 1 : 0));
+    }
+  }
 
   template <typename Done>
-  __device__ __forceinline__ void stage(int64_t rg, const T (&vals)[NV], const int (&idx)[NV], Done done) {
-    const SplitInfo si = split_info(rg, per_rg, units, grid);
-    if (si.first_cta == si.last_cta) {
-      done(rg, vals);
+  __device__ __forceinline__ void stage(int64_t r, const T (&vals)[NV], const int (&idx)[NV], Done done) {
+    const int s = (r == rg[0]) ? 0 : (r == rg[1]) ? 1 : -1;
+    if (s < 0) {
+      done(r, vals);
       return;
     }
-    const int side = split_side(cta, rg, per_rg, units, grid);
-    T* slot = reinterpret_cast<T*>(ws->partials) + (cta * 2 + side) * (kRowGroup * 16);
+    T* slot = reinterpret_cast<T*>(ws->partials) + (int64_t)(cta * 2 + s) * (kRowGroup * 16);
 #pragma unroll
     for (int i = 0; i < NV; ++i)
       if (idx[i] >= 0) slot[idx[i]] = vals[i];
-    if (npend < 2) pend[npend++] = rg;
+    pend |= 1 << s;
   }
 
-  // Returns false if a bounded wait gave up.  `flags` is a 2-int shared array.  The last
-  // contributor reduces with all 128 consumer threads: thread j takes entries j, j + 128, ...
-  // of the 64 x M outputs and loads the contributors' slots eight at a time (one round trip
-  // per eight CTAs), summing them in CTA order.  `put(rg, entry, value)` stores one output.
+  // Returns false if a bounded wait gave up.  `flags` is a 2-int shared array.
+  //
+  // Ordering: the consumer barrier orders every consumer's slot stores before thread 0's
+  // arrival, which is an acq_rel atomic at GPU scope (release: this CTA's slots become
+  // visible before the count; acquire, for the last arriver: the other contributors' slots
+  // are visible to it), and the second barrier passes that on to the other consumers, which
+  // read the slots from L2 (ld.cg).
+  //
+  // The last contributor reduces with all 128 consumer threads, both of its row groups at
+  // once: work item j is the 16-byte quad (row, tokens 4i..4i+3) of one row group, and its
+  // contributors' quads are loaded kRedBatch at a time and summed in CTA order.
+  // `put(rg, entry, value)` stores one output.
   template <typename Put>
   __device__ __forceinline__ bool finish(int M, ConsumerSync& cs, int* flags, Put put) {
-    if (npend == 0) return true;  // uniform: every consumer thread walks the same row groups
-    __threadfence();
+    if (pend == 0) return true;  // uniform: every consumer thread staged the same row groups
     if (!cs.sync()) return false;
     if (threadIdx.x == 0) {
-      for (int p = 0; p < npend; ++p) {
-        const SplitInfo si = split_info(pend[p], per_rg, units, grid);
-        const unsigned old = atomicAdd(&ws->counters[pend[p]], 1u);
-        flags[p] = (old == (unsigned)(si.last_cta - si.first_cta)) ? 1 : 0;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        int last = 0;
+        if (pend & (1 << s)) {
+          const unsigned old = atom_add_acq_rel_gpu(&ws->counters[rg[s]], 1u);
+          last = (old == (unsigned)(ncontrib[s] - 1)) ? 1 : 0;
+        }
+        flags[s] = last;
       }
     }
     if (!cs.sync()) return false;
-    for (int p = 0; p < npend; ++p) {
-      if (!flags[p]) continue;
-      __threadfence();
-      const int64_t rg = pend[p];
-      const SplitInfo si = split_info(rg, per_rg, units, grid);
-      const T* base = reinterpret_cast<const T*>(ws->partials);
-      for (int lin = threadIdx.x; lin < kRowGroup * M; lin += 128) {
-        const int e = (lin / M) * 16 + lin % M;
-        T s = T(0);
-        for (int64_t c0 = si.first_cta; c0 <= si.last_cta; c0 += 8) {
-          T v[8];
+    const int f0 = flags[0], f1 = flags[1];
+    const int qm = (M + 3) >> 2, per = kRowGroup * qm;
+    const T* base = reinterpret_cast<const T*>(ws->partials);
+    for (int w = threadIdx.x; w < (f0 + f1) * per; w += 128) {
+      const int s = (f0 && w < per) ? 0 : 1;
+      const int lin = w - ((f0 && s == 1) ? per : 0);
+      const int e = (lin / qm) * 16 + (lin % qm) * 4;
+      const int C = ncontrib[s], fc = first_cta[s], fs = first_slot[s];
+      T acc[4] = {T(0), T(0), T(0), T(0)};
+      for (int c0 = 0; c0 < C; c0 += kRedBatch) {
+        T v[kRedBatch][4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int64_t c = c0 + u;
-            v[u] = T(0);
-            if (c <= si.last_cta)
-              v[u] = __ldcg(base + (c * 2 + split_side(c, rg, per_rg, units, grid)) * (kRowGroup * 16) + e);
+        for (int u = 0; u < kRedBatch; ++u) {
+          const int c = c0 + u;
+          if (c < C) {
+            const int slot = (c == 0) ? fs : (fc + c) * 2;
+            ldcg4(base + (int64_t)slot * (kRowGroup * 16) + e, v[u]);
+          } else {
+            v[u][0] = v[u][1] = v[u][2] = v[u][3] = T(0);
           }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) s += v[u];
         }
-        put(rg, e, s);
+#pragma unroll
+        for (int u = 0; u < kRedBatch; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[j] += v[u][j];
       }
-      if (threadIdx.x == 0) ws->counters[rg] = 0u;
+      const int m0 = (lin % qm) * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (m0 + j < M) put((int64_t)rg[s], e + j, acc[j]);
+    }
+    if (threadIdx.x == 0) {
+      if (f0) ws->counters[rg[0]] = 0u;
+      if (f1) ws->counters[rg[1]] = 0u;
     }
     return true;
   }

@@ -147,8 +147,10 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       return 0u;
     };
     const int xm = MODE == 1 ? 1 : M;
-    auto load_x = [&](int s, int64_t u) {
-      const int64_t k0 = (u % S) * kSpqrSuper;
+    int kx = (int)(u0 % S);  // supergroup of the next X slice (units are issued in order)
+    auto load_x = [&](int s) {
+      const int64_t k0 = (int64_t)kx * kSpqrSuper;
+      if (++kx == (int)S) kx = 0;
       for (int m = 0; m < xm; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
     };
     const int pro = n_units < kStagesSp ? n_units : kStagesSp;
@@ -157,20 +159,19 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       weights(i, u0 + i);
     }
     pdl_wait();
-    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = 0; i < pro; ++i) load_x(i);
     for (int i = kStagesSp; i < n_units; ++i) {
       const int s = i % kStagesSp;
       const uint32_t ph = (uint32_t)(i / kStagesSp) & 1u;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
       mbar_arrive_expect_tx(&sm.full[s], kSpqrUnitBytes + out_bytes(u0 + i) + (uint32_t)xm * xbytes);
       weights(s, u0 + i);
-      load_x(s, u0 + i);
+      load_x(s);
     }
     return;
   }
 
   // ---------------------------------------------------------------- consumers
-  pdl_wait();
   const int g = lane >> 2, t = lane & 3;
   const int rt = warp;
   ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
   for (int i = lane; i < 16 * XR; i += 32) (&sm.rowacc[rt][0][0])[i] = 0.f;
   __syncwarp();
   int64_t cur_rg = u0 / S;
+  UnitCursor cur{cur_rg, (int)(u0 - cur_rg * S), (int)S};
 
   constexpr int NV = (MODE == 1) ? 2 : NACC;
   int idx[NV];
@@ -232,11 +234,14 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
     fin.stage(rg, vals, idx, done);
   };
 
+  // the previous kernel on the stream may still read this launch's outputs or workspace
+  pdl_wait();
   for (int it = 0; it < n_units; ++it) {
     const int s = it % kStagesSp;
     const uint32_t ph = (uint32_t)(it / kStagesSp) & 1u;
     const int64_t u = u0 + it;
-    const int64_t rg = u / S;
+    const int64_t rg = cur.rg;
+    cur.next();
     if (rg != cur_rg) {
       flush(cur_rg);
 #pragma unroll
@@ -262,11 +267,14 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
         const int gl = lane >> 1, h = lane & 1;
         const uint4 xv = *reinterpret_cast<const uint4*>(x0 + gl * 16 + h * 8);
         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        float xf[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xf = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-          if (h * 8 + e < 10) sa += xf; else sb += xf;
-        }
+        for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
+        // fields 0..9 of a group have base 128, fields 10..15 base 16
+        const float s01 = xf[0] + xf[1];
+        const float shi = ((xf[2] + xf[3]) + (xf[4] + xf[5])) + (xf[6] + xf[7]);
+        sa = h ? s01 : s01 + shi;
+        sb = h ? shi : 0.f;
         sa += __shfl_xor_sync(0xffffffffu, sa, 1);
         sb += __shfl_xor_sync(0xffffffffu, sb, 1);
       }
@@ -301,8 +309,13 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
         const uint4 by1 = *reinterpret_cast<const uint4*>(pb1 == sm.zeros ? sm.zeros : pb1 + 4);
         const uint32_t b0v[8] = {bx0.x, bx0.y, bx0.z, bx0.w, by0.x, by0.y, by0.z, by0.w};
         const uint32_t b1v[8] = {bx1.x, bx1.y, bx1.z, bx1.w, by1.x, by1.y, by1.z, by1.w};
-        // two independent accumulator chains (even / odd j) keep the MMA pipe busy
-        float c[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
+        // group sums of the two accumulator columns 2t, 2t+1 of this block
+        const int l0 = 2 * (blk * 8 + 2 * t);
+        const float B0 = __shfl_sync(0xffffffffu, bsum, l0), S0 = __shfl_sync(0xffffffffu, xsum, l0);
+        const float B1 = __shfl_sync(0xffffffffu, bsum, l0 + 2), S1 = __shfl_sync(0xffffffffu, xsum, l0 + 2);
+        // two independent accumulator chains (even / odd j) keep the MMA pipe busy; the even
+        // chain starts at -sum(base x) of its column's group
+        float c[4] = {-B0, -B1, -B0, -B1}, d[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t a[4];
         spqr_frag<0>(w, a); mma_bf16(c, a, b0v[0], b1v[0]);
         spqr_frag<1>(w, a); mma_bf16(d, a, b0v[1], b1v[1]);
@@ -312,10 +325,6 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
         spqr_frag<5>(w, a); mma_bf16(d, a, b0v[5], b1v[5]);
         spqr_frag<6>(w, a); mma_bf16(c, a, b0v[6], b1v[6]);
         spqr_frag<7>(w, a); mma_bf16(d, a, b0v[7], b1v[7]);
-        // group sums of the two accumulator groups 2t, 2t+1 of this block
-        const int l0 = 2 * (blk * 8 + 2 * t);
-        const float B0 = __shfl_sync(0xffffffffu, bsum, l0), S0 = __shfl_sync(0xffffffffu, xsum, l0);
-        const float B1 = __shfl_sync(0xffffffffu, bsum, l0 + 2), S1 = __shfl_sync(0xffffffffu, xsum, l0 + 2);
         const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(qarea);
         const int bit = 24 * lane;
@@ -329,8 +338,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
           const float xz = __uint_as_float((z24 & (7u << (6 * i))) | 0x4B000000u);
           const float sh = __fmul_rn(__fsub_rn(xs, kcs[i]), kms[i]);
           const float zh = __fmul_rn(__fsub_rn(xz, kcz[i]), kmz[i]);
-          const float Bg = (i & 1) ? B1 : B0, Sg = (i & 1) ? S1 : S0;
-          acc[i] += sh * ((c[i] + d[i]) - Bg - zh * Sg);
+          const float Sg = (i & 1) ? S1 : S0;
+          acc[i] += sh * ((c[i] + d[i]) - zh * Sg);
         }
       }
     } else {

@@ -63,9 +63,11 @@ __global__ void __launch_bounds__(160, 4)
     if (lane != 0) return;
     const uint32_t xbytes = kW4Group * 2;
     const uint32_t tx = kW4UnitBytes + (uint32_t)M * xbytes;
-    auto load_x = [&](int s, int64_t u) {
-      const int64_t k0 = (u % G) * kW4Group;
+    int kx = (int)(u0 % G);  // K group of the next X slice (units are issued in order)
+    auto load_x = [&](int s) {
+      const int64_t k0 = (int64_t)kx * kW4Group;
       for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+      if (++kx == (int)G) kx = 0;
     };
     const int pro = n_units < kStagesW4 ? n_units : kStagesW4;
     for (int i = 0; i < pro; ++i) {
@@ -73,20 +75,19 @@ __global__ void __launch_bounds__(160, 4)
       bulk_g2s(sm.unit[i], v.units + (u0 + i) * (int64_t)kW4UnitBytes, kW4UnitBytes, &sm.full[i]);
     }
     pdl_wait();  // X is written by the previous kernel on the stream
-    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = 0; i < pro; ++i) load_x(i);
     for (int i = kStagesW4; i < n_units; ++i) {
       const int s = i % kStagesW4;
       const uint32_t ph = (uint32_t)(i / kStagesW4) & 1u;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
       mbar_arrive_expect_tx(&sm.full[s], tx);
       bulk_g2s(sm.unit[s], v.units + (u0 + i) * (int64_t)kW4UnitBytes, kW4UnitBytes, &sm.full[s]);
-      load_x(s, u0 + i);
+      load_x(s);
     }
     return;
   }
 
   // ---------------------------------------------------------------- consumers
-  pdl_wait();
   const int g = lane >> 2, t = lane & 3;
   ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
   float acc[MT][4];
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(160, 4)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
   int64_t cur_rg = u0 / G;
+  UnitCursor cur{cur_rg, (int)(u0 - cur_rg * G), (int)G};
 
   int idx[MT * 4];
 #pragma unroll
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(160, 4)
       if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
     }
   };
-  RowGroupFinisher<float, MT * 4> fin(G, U, grid, cta, &ws);
+  RowGroupFinisher<float, MT * 4, MT == 1 ? 16 : 8> fin(G, U, grid, cta, &ws);
   auto flush = [&](int64_t rg) {
     float vals[MT * 4];
 #pragma unroll
@@ -124,10 +126,13 @@ __global__ void __launch_bounds__(160, 4)
     fin.stage(rg, vals, idx, done);
   };
 
+  // the previous kernel on the stream may still read this launch's outputs or workspace
+  pdl_wait();
   for (int i = 0; i < n_units; ++i) {
     const int s = i % kStagesW4;
     const uint32_t ph = (uint32_t)(i / kStagesW4) & 1u;
-    const int64_t rg = (u0 + i) / G;
+    const int64_t rg = cur.rg;
+    cur.next();
     if (rg != cur_rg) {
       flush(cur_rg);
 #pragma unroll

@@ -134,9 +134,11 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     if (lane != 0) return;
     const uint32_t xbytes = kW8Block * 2;
     const uint32_t tx = kW8UnitBytes + (uint32_t)M * xbytes;
-    auto load_x = [&](int s, int64_t u) {
-      const int64_t k0 = (u % KB) * kW8Block;
+    int kx = (int)(u0 % KB);  // K block of the next X slice (units are issued in order)
+    auto load_x = [&](int s) {
+      const int64_t k0 = (int64_t)kx * kW8Block;
       for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], q16 + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+      if (++kx == (int)KB) kx = 0;
     };
     const int pro = n_units < kStagesW8 ? n_units : kStagesW8;
     for (int i = 0; i < pro; ++i) {
@@ -144,19 +146,19 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
       bulk_g2s(sm.unit[i], v.units + (u0 + i) * (int64_t)kW8UnitBytes, kW8UnitBytes, &sm.full[i]);
     }
     pdl_wait();  // the activation codes come from the act-quant kernel
-    for (int i = 0; i < pro; ++i) load_x(i, u0 + i);
+    for (int i = 0; i < pro; ++i) load_x(i);
     for (int i = kStagesW8; i < n_units; ++i) {
       const int s = i % kStagesW8;
       const uint32_t ph = (uint32_t)(i / kStagesW8) & 1u;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
       mbar_arrive_expect_tx(&sm.full[s], tx);
       bulk_g2s(sm.unit[s], v.units + (u0 + i) * (int64_t)kW8UnitBytes, kW8UnitBytes, &sm.full[s]);
-      load_x(s, u0 + i);
+      load_x(s);
     }
     return;
   }
 
-  pdl_wait();
+  // ---------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
   ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
   int32_t iacc[MT][4];
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     since_drain = 0;
   };
   int64_t cur_rg = u0 / KB;
+  UnitCursor cur{cur_rg, (int)(u0 - cur_rg * KB), (int)KB};
 
   int idx[MT * 4];
 #pragma unroll
@@ -216,10 +219,13 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     fin.stage(rg, vals, idx, done);
   };
 
+  // the previous kernel on the stream may still read this launch's outputs or workspace
+  pdl_wait();
   for (int i = 0; i < n_units; ++i) {
     const int s = i % kStagesW8;
     const uint32_t ph = (uint32_t)(i / kStagesW8) & 1u;
-    const int64_t rg = (u0 + i) / KB;
+    const int64_t rg = cur.rg;
+    cur.next();
     if (rg != cur_rg) {
       flush(cur_rg);
 #pragma unroll
