@@ -57,21 +57,25 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def _sources_sha256(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "quantized_weight_linear_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic(kernel_key: str):
-    """dram bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources are unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         with open(p) as f:
             d = json.load(f).get(kernel_key)
-        if not d:
+        if not d or _sources_sha256(d["sources"]) != d["sources_sha256"]:
             return None
-        import hashlib
-        src = os.path.join(ROOT, "quantized_weight_linear_gb300", "csrc", d["source"])
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
-                return None
         return float(d["dram_bytes_per_launch"])
     except Exception:
         return None
