@@ -19,7 +19,10 @@
 // * M >= 2: the same A pairs are dequantized to bf16 s^ (q - z^) in registers and the
 //   MMA columns carry the tokens;
 // * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
-//   fp16 value) and adds value * x[k] into per-row shared accumulators.
+//   fp16 value; sorted by row, then k).  Lane L owns row L % 16: it finds where its row's run
+//   starts by bisection and accumulates value * x[k] in registers, so no two lanes ever add
+//   into the same sum (no atomics; the page's warning about the sparse part is about exactly
+//   this scattered accumulation).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
@@ -180,8 +183,16 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
   float acc[NACC];
 #pragma unroll
   for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
-  for (int i = lane; i < 16 * XR; i += 32) (&sm.rowacc[rt][0][0])[i] = 0.f;
-  __syncwarp();
+  // outlier sums: lane L owns row L % 16 of the tile.  With one token, or up to eight, the two
+  // lanes of a row take alternate outliers of the row and every token; with up to sixteen
+  // tokens each takes every outlier of the row and eight of the tokens.
+  constexpr int OT = (MODE == 1) ? 1 : 8;
+  constexpr bool kSplitEntries = (MODE == 1) || (MT == 1);
+  const int orow = lane & 15, ohalf = lane >> 4;
+  const int otok0 = kSplitEntries ? 0 : 8 * ohalf;
+  float oacc[OT];
+#pragma unroll
+  for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
   int64_t cur_rg = u0 / S;
   UnitCursor cur{cur_rg, (int)(u0 - cur_rg * S), (int)S};
 
@@ -219,9 +230,20 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-      vals[0] = r0 + sm.rowacc[rt][g][0];
-      vals[1] = r1 + sm.rowacc[rt][g + 8][0];
+      const float ot = oacc[0] + __shfl_xor_sync(0xffffffffu, oacc[0], 16);  // row orow's outliers
+      vals[0] = r0 + __shfl_sync(0xffffffffu, ot, g);
+      vals[1] = r1 + __shfl_sync(0xffffffffu, ot, g + 8);
     } else {
+      if constexpr (kSplitEntries) {
+#pragma unroll
+        for (int j = 0; j < OT; ++j) oacc[j] += __shfl_xor_sync(0xffffffffu, oacc[j], 16);
+      }
+      if (!kSplitEntries || ohalf == 0) {
+#pragma unroll
+        for (int j = 0; j < OT; ++j)
+          if (otok0 + j < M) sm.rowacc[rt][orow][otok0 + j] = oacc[j];
+      }
+      __syncwarp();
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -246,8 +268,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       flush(cur_rg);
 #pragma unroll
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
-      __syncwarp();
-      for (int i = lane; i < 16 * XR; i += 32) (&sm.rowacc[rt][0][0])[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
       __syncwarp();
       cur_rg = rg;
     }
@@ -396,21 +418,32 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       }
     }
 
-    // outliers of this row tile in this unit
+    // outliers of this row tile in this unit: the bucket is sorted by row (then k), so lane
+    // q <= 16 finds where row q starts by bisection and each lane walks its row's run
     {
       const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
       const uint32_t b0 = offs(4 * u + rt), b1 = offs(4 * u + rt + 1);
       const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
-      const uint32_t a0 = e0 & ~3u;
-      for (uint32_t p = b0 + lane; p < b1; p += 32) {
-        const uint32_t e = staged ? sm.out[s][p - a0] : __ldg(v.ents + p);
-        const int r = (int)(e & 15u), k = (int)((e >> 4) & 255u);
-        const float val = h2f_dev((uint16_t)(e >> 16));
-        if constexpr (MODE == 1) {
-          atomicAdd(&sm.rowacc[rt][r][0], val * bf2f(sm.x[s][0][k]));
-        } else {
-          for (int m = 0; m < M; ++m) atomicAdd(&sm.rowacc[rt][r][m], val * bf2f(sm.x[s][m][k]));
+      const uint32_t* bs = sm.out[s] + (b0 - (e0 & ~3u));  // staged bucket
+      const uint32_t* bg = v.ents + b0;                     // the same bucket in global memory
+      auto ent = [&](int i) -> uint32_t { return staged ? bs[i] : __ldg(bg + i); };
+      const int n = (int)(b1 - b0);
+      int lo = 0;
+      if (n > 0) {
+        int hi = n;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if ((int)(ent(mid) & 15u) < lane) lo = mid + 1; else hi = mid;
         }
+      }
+      const int beg = __shfl_sync(0xffffffffu, lo, orow), end = __shfl_sync(0xffffffffu, lo, orow + 1);
+      for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
+        const uint32_t e = ent(p);
+        const int k = (int)((e >> 4) & 255u);
+        const float val = h2f_dev((uint16_t)(e >> 16));
+#pragma unroll
+        for (int j = 0; j < OT; ++j)
+          if (otok0 + j < (MODE == 1 ? 1 : M)) oacc[j] += val * bf2f(sm.x[s][otok0 + j][k]);
       }
     }
     __syncwarp();
