@@ -48,7 +48,8 @@ struct UnitCursor {
 // round trip in the reduction.
 template <typename T, int NV, int kRedBatch = 8>
 struct RowGroupFinisher {
-  const Workspace* ws;
+  float* partials;     // the workspace's slots and counters, copied: taking the address of
+  uint32_t* counters;  // a kernel parameter would move the parameter to local memory
   int cta;
   int rg[2];          // shared row groups: [0] the first of the range, [1] the last (-1: none)
   int first_cta[2];   // their first contributor
@@ -57,8 +58,8 @@ struct RowGroupFinisher {
   int pend;           // bit s: rg[s] has been staged
 
   __device__ __forceinline__ RowGroupFinisher(int64_t per_rg, int64_t units, int64_t grid, int64_t cta_,
-                                              const Workspace* ws_)
-      : ws(ws_), cta((int)cta_), pend(0) {
+                                              float* partials_, uint32_t* counters_)
+      : partials(partials_), counters(counters_), cta((int)cta_), pend(0) {
     const int64_t u0 = split_start(cta_, units, grid), u1 = split_start(cta_ + 1, units, grid);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -84,7 +85,7 @@ struct RowGroupFinisher {
       done(r, vals);
       return;
     }
-    T* slot = reinterpret_cast<T*>(ws->partials) + (int64_t)(cta * 2 + s) * (kRowGroup * 16);
+    T* slot = reinterpret_cast<T*>(partials) + (int64_t)(cta * 2 + s) * (kRowGroup * 16);
 #pragma unroll
     for (int i = 0; i < NV; ++i)
       if (idx[i] >= 0) slot[idx[i]] = vals[i];
@@ -112,7 +113,7 @@ struct RowGroupFinisher {
       for (int s = 0; s < 2; ++s) {
         int last = 0;
         if (pend & (1 << s)) {
-          const unsigned old = atom_add_acq_rel_gpu(&ws->counters[rg[s]], 1u);
+          const unsigned old = atom_add_acq_rel_gpu(&counters[rg[s]], 1u);
           last = (old == (unsigned)(ncontrib[s] - 1)) ? 1 : 0;
         }
         flags[s] = last;
@@ -121,7 +122,7 @@ struct RowGroupFinisher {
     if (!cs.sync()) return false;
     const int f0 = flags[0], f1 = flags[1];
     const int qm = (M + 3) >> 2, per = kRowGroup * qm;
-    const T* base = reinterpret_cast<const T*>(ws->partials);
+    const T* base = reinterpret_cast<const T*>(partials);
     for (int w = threadIdx.x; w < (f0 + f1) * per; w += 128) {
       const int s = (f0 && w < per) ? 0 : 1;
       const int lin = w - ((f0 && s == 1) ? per : 0);
@@ -151,8 +152,8 @@ struct RowGroupFinisher {
         if (m0 + j < M) put((int64_t)rg[s], e + j, acc[j]);
     }
     if (threadIdx.x == 0) {
-      if (f0) ws->counters[rg[0]] = 0u;
-      if (f1) ws->counters[rg[1]] = 0u;
+      if (f0) counters[rg[0]] = 0u;
+      if (f1) counters[rg[1]] = 0u;
     }
     return true;
   }

@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
   SpSmem<XR>& sm = *reinterpret_cast<SpSmem<XR>*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t grid = gridDim.x, cta = blockIdx.x;
+  // scalars of the view as locals: lambdas capture them, and capturing the kernel parameter
+  // itself would move it to local memory
+  const int64_t vN = v.N, vK = v.K;
   const int64_t S = v.S, U = (int64_t)v.RG * S;
   const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
   const int n_units = (int)(u1 - u0);
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
     auto load_x = [&](int s) {
       const int64_t k0 = (int64_t)kx * kSpqrSuper;
       if (++kx == (int)S) kx = 0;
-      for (int m = 0; m < xm; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+      for (int m = 0; m < xm; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * vK + k0, xbytes, &sm.full[s]);
     };
     const int pro = n_units < kStagesSp ? n_units : kStagesSp;
     for (int i = 0; i < pro; ++i) {
@@ -217,10 +220,10 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       if (idx[j] < 0) continue;
       const int64_t n = rg * kRowGroup + idx[j] / 16;
       const int m = idx[j] % 16;
-      if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+      if (n < vN) Y[(int64_t)m * vN + n] = f2bf(out[j]);
     }
   };
-  RowGroupFinisher<float, NV> fin(S, U, grid, cta, &ws);
+  RowGroupFinisher<float, NV> fin(S, U, grid, cta, ws.partials, ws.counters);
   auto flush = [&](int64_t rg) {
     __syncwarp();
     float vals[NV];
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
     flush(cur_rg);
     fin.finish(M, cs, sm.flags, [&](int64_t rg, int e, float val) {
       const int64_t n = rg * kRowGroup + e / 16;
-      if (n < v.N) Y[(int64_t)(e % 16) * v.N + n] = f2bf(val);
+      if (n < vN) Y[(int64_t)(e % 16) * vN + n] = f2bf(val);
     });
   }
 }

@@ -6,8 +6,7 @@
 // erodes weight-only speedups; W8A8 keeps both operands on the tensor cores.  Design:
 //
 // * CTA tile: 128 output rows (MMA N) x 256 tokens (two 128-row MMAs that share each
-//   dequantized B tile, halving the dequantization per FLOP) for W4 / SpQR, x 128 tokens
-//   for W8A8; K in blocks of 64;
+//   dequantized B tile, halving the dequantization per FLOP); K in blocks of 64;
 // * warp 0: TMA producer -- X tiles through a 2-D tensor map (128B swizzle) and the packed
 //   weight units of the tile (the device image the decode kernels stream; SpQR: plus the
 //   unit's outlier buckets) through cp.async.bulk into a packed ring;
@@ -17,10 +16,11 @@
 // * converter warps (8 for W4 / SpQR, 4 for W8A8): turn packed codes into the bf16 / fp16
 //   K-major 128B-swizzled B operand; for W4 / SpQR they then run the epilogue
 //   (tcgen05.ld -> bf16 -> Y);
-// * W8A8 only, 4 more warps: exactness drain -- int8 x int8 products are exact in the fp16
-//   MMA and every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (two TMEM
-//   regions, double-buffered) are exact integers; these warps add them into int32 registers
-//   while the MMA runs the next chunk, and write y = bf16((acc * sx) * sw) (or acc).
+// * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
+//   MMA and every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (TMEM
+//   columns 0..255) hold exact integers; after each chunk these warps add them into int32
+//   partial sums kept in the other half of TMEM (columns 256..511), release the accumulator
+//   to the next chunk, and after the last one write y = bf16((acc * sx) * sw) (or acc).
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,7 +53,7 @@ struct TcCfg<kSpqr> {
 };
 template <>
 struct TcCfg<kW8> {
-  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 1, kConv = 4, kStages = 4;
+  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = 3;
   static constexpr uint32_t kAType = 0;  // fp16
 };
 
@@ -304,7 +304,24 @@ __device__ __forceinline__ void spqr_outliers_tile(uint8_t* bt, const uint32_t* 
 }
 
 template <int F>
-__global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+constexpr int tc_threads() {  // producer + MMA + converters (+ W8A8 drain warps)
+  return 32 * (2 + TcCfg<F>::kConv + (F == kW8 ? 8 : 0));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <int F>
+__global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcSmem<F>& sm = *reinterpret_cast<TcSmem<F>*>(base);
@@ -319,7 +336,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
   const int nunits = nkb / bpu;
   const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
   constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, 128);
-  constexpr uint32_t tmem_cols = F == kW8 ? 256u : 128u * MH;
+  constexpr uint32_t tmem_cols = F == kW8 ? 512u : 128u * MH;  // W8A8: fp32 chunk sums + int32 partials
   // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
   int64_t off_base[2] = {0, 0};
   uint32_t off_len[2] = {0, 0};
@@ -345,7 +362,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
     mbar_init(&sm.acc_full, 1);
     for (int r = 0; r < 2; ++r) {
       mbar_init(&sm.ch_full[r], 1);
-      mbar_init(&sm.ch_empty[r], 4);
+      mbar_init(&sm.ch_empty[r], 8);
     }
     fence_mbar_init();
     pdl_launch_dependents();
@@ -434,14 +451,15 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
         uint32_t dcol = 0;
         bool first = (i == 0);
         if constexpr (F == kW8) {
+          // one fp32 accumulator: chunk c starts once the drain has read chunk c - 1
           const int c = i / kChunkBlocks;
-          dcol = (uint32_t)(c & 1) * 128u;
           first = (i % kChunkBlocks) == 0;
-          if (first && c >= 2) {
-            if (!mbar_wait(&sm.ch_empty[c & 1], (uint32_t)((c / 2) - 1) & 1u, a.status)) {
+          if (first && c >= 1) {
+            if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(c - 1) & 1u, a.status)) {
               ok = false;
               break;
             }
+            tc_fence_after();
           }
         }
         if (!mbar_wait(&sm.ab_full[s], ph, a.status)) {
@@ -460,7 +478,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
         }
         umma_commit(&sm.ab_empty[s]);
         if constexpr (F == kW8) {
-          if ((i % kChunkBlocks) == kChunkBlocks - 1 || i == nkb - 1) umma_commit(&sm.ch_full[(i / kChunkBlocks) & 1]);
+          if ((i % kChunkBlocks) == kChunkBlocks - 1 || i == nkb - 1) umma_commit(&sm.ch_full[0]);
         }
       }
       umma_commit(&sm.acc_full);
@@ -544,48 +562,68 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
     }
   } else if constexpr (F == kW8) {
     // ------------------------------------------------------------------ exact int32 drain + epilogue
+    // warps 6..13: TMEM lane quadrant q = warp % 4 (tokens 32q..32q+31 of an M half), M half
+    // mh = (warp - 6) / 4 (accumulator columns 128 mh.., int32 partials 256 + 128 mh..)
     pdl_wait();
     const int q = warp & 3;
-    int32_t acc[kBN];
-#pragma unroll
-    for (int i = 0; i < kBN; ++i) acc[i] = 0;
+    const int mh = (warp - 2 - NCONV) / 4;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const uint32_t fcol = 128u * mh, icol = 256u + 128u * mh;
+    const int m = m_tile * BM + 128 * mh + 32 * q + lane;
+    const int n0 = n_tile * kBN;
     for (int c = 0; c < nchunks && ok; ++c) {
-      if (!mbar_wait(&sm.ch_full[c & 1], (uint32_t)(c / 2) & 1u, a.status)) {
+      if (!mbar_wait(&sm.ch_full[0], (uint32_t)c & 1u, a.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll
+      const bool last = c == nchunks - 1;
+#pragma unroll 1
       for (int cb = 0; cb < kBN / 32; ++cb) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c & 1) * 128u + 32u * cb, r);
+        tmem_ld32(tmem + lane_base + fcol + 32u * cb, r);
+        if (c > 0) {
+          uint32_t p[32];
+          tmem_ld32(tmem + lane_base + icol + 32u * cb, p);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 * cb + i] += __float2int_rn(__uint_as_float(r[i]));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.ch_empty[c & 1]);
-    }
-    const int m = m_tile * BM + 32 * q + lane;
-    if (ok && m < a.M) {
-      const int n0 = n_tile * kBN;
-      // N is a multiple of 64, so each 64-column half of the tile is fully in or out
-      if (a.acc_out) {
+          for (int i = 0; i < 32; ++i) r[i] = (uint32_t)((int32_t)p[i] + __float2int_rn(__uint_as_float(r[i])));
+        } else {
 #pragma unroll
-        for (int i = 0; i < kBN; i += 4)
-          if (n0 + i < a.N)
-            *reinterpret_cast<int4*>(a.acc_out + (int64_t)m * a.N + n0 + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-      } else {
-        const float sxm = a.sx[m];
-        uint16_t* dst = a.Y + (int64_t)m * a.N + n0;
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
-          if (n0 + i < a.N) {
-            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[i]), sxm), a.sw[n0 + i]);
-            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[i + 1]), sxm), a.sw[n0 + i + 1]);
-            *reinterpret_cast<uint32_t*>(dst + i) = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
-          }
+          for (int i = 0; i < 32; ++i) r[i] = (uint32_t)__float2int_rn(__uint_as_float(r[i]));
         }
+        if (!last) {
+          tmem_st32(tmem + lane_base + icol + 32u * cb, r);
+          continue;
+        }
+        // N is a multiple of 64 rows (the device image pads row groups), so a 32-column slice
+        // is either fully inside or fully outside the output
+        const int n = n0 + 32 * cb;
+        if (m >= a.M || n + 32 > a.N) continue;
+        if (a.acc_out) {
+          int32_t* dst = a.acc_out + (int64_t)m * a.N + n;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<int4*>(dst)[v] =
+                make_int4((int)r[4 * v], (int)r[4 * v + 1], (int)r[4 * v + 2], (int)r[4 * v + 3]);
+        } else {
+          const float sxm = a.sx[m];
+          uint32_t pk16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[2 * i]), sxm), a.sw[n + 2 * i]);
+            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[2 * i + 1]), sxm), a.sw[n + 2 * i + 1]);
+            pk16[i] = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
+          }
+          uint16_t* dst = a.Y + (int64_t)m * a.N + n;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+        }
+      }
+      if (!last) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ch_empty[0]);
       }
     }
   }
@@ -637,7 +675,7 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((args.N + kBN - 1) / kBN), (unsigned)((args.M + BM - 1) / BM));
-  cfg.blockDim = dim3(320);
+  cfg.blockDim = dim3(tc_threads<F>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];

@@ -39,6 +39,9 @@ __global__ void __launch_bounds__(160, 4)
   W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t grid = gridDim.x, cta = blockIdx.x;
+  // scalars of the view as locals: lambdas capture them, and capturing the kernel parameter
+  // itself would move it to local memory
+  const int64_t vN = v.N, vK = v.K;
   const int64_t G = v.G, U = (int64_t)v.RG * G;
   const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
   const int n_units = (int)(u1 - u0);
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(160, 4)
     int kx = (int)(u0 % G);  // K group of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
       const int64_t k0 = (int64_t)kx * kW4Group;
-      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * vK + k0, xbytes, &sm.full[s]);
       if (++kx == (int)G) kx = 0;
     };
     const int pro = n_units < kStagesW4 ? n_units : kStagesW4;
@@ -113,10 +116,10 @@ __global__ void __launch_bounds__(160, 4)
       if (idx[j] < 0) continue;
       const int64_t n = rg * kRowGroup + idx[j] / 16;
       const int m = idx[j] % 16;
-      if (n < v.N) Y[(int64_t)m * v.N + n] = f2bf(out[j]);
+      if (n < vN) Y[(int64_t)m * vN + n] = f2bf(out[j]);
     }
   };
-  RowGroupFinisher<float, MT * 4, MT == 1 ? 16 : 8> fin(G, U, grid, cta, &ws);
+  RowGroupFinisher<float, MT * 4, MT == 1 ? 16 : 8> fin(G, U, grid, cta, ws.partials, ws.counters);
   auto flush = [&](int64_t rg) {
     float vals[MT * 4];
 #pragma unroll
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(160, 4)
     flush(cur_rg);
     fin.finish(M, cs, sm.flags, [&](int64_t rg, int e, float val) {
       const int64_t n = rg * kRowGroup + e / 16;
-      if (n < v.N) Y[(int64_t)(e % 16) * v.N + n] = f2bf(val);
+      if (n < vN) Y[(int64_t)(e % 16) * vN + n] = f2bf(val);
     });
   }
 }
