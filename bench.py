@@ -254,14 +254,18 @@ def _e2e(q, layer, rot, M, steps_e2e):
 
 
 class DistCtx:
-    def __init__(self):
+    """One process per GPU (torchrun env); replicas only: the only collectives are the timing
+    barrier and the max over ranks.  backend: "nccl" on GPUs, "gloo" for the CPU tests."""
+
+    def __init__(self, backend: str = "nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.backend = backend
         self.pg = None
         if self.world > 1:
             import torch.distributed as dist
-            dist.init_process_group("nccl")
+            dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -272,13 +276,19 @@ class DistCtx:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if self.backend == "nccl" else "cpu")
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def whole_job_gbs(nbytes: int, ms_max: float, steps: int, world: int) -> float:
+    """Weight GB/s of the whole job: every rank streams its own copy of the layer once per
+    step, and the job takes as long as its slowest rank (ms_max over `steps` steps)."""
+    return world * nbytes / (ms_max / steps / 1e3) / 1e9
 
 
 def _extra_configs(q, torch, stream, l2):
@@ -394,8 +404,7 @@ def run_gpu(args):
         if st != 0:
             raise RuntimeError(f"device status {st} after the timed region")
         ms_max = dist_ctx.max(ms)
-        t_step = ms_max / steps / 1e3
-        value = dist_ctx.world * nbytes / t_step / 1e9
+        value = whole_job_gbs(nbytes, ms_max, steps, dist_ctx.world)
         e2e_t, h2d, d2h = _e2e(q, layer, rot, M_, args.e2e_steps)
         e2e_t = dist_ctx.max(e2e_t)
         extra = _extra_configs(q, torch, stream, l2) if (dist_ctx.rank == 0 and not args.no_extra) else {}

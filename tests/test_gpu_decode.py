@@ -88,6 +88,19 @@ def test_spqr_forward_tolerance(qlin, N, K, frac, M):
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
 
 
+@pytest.mark.parametrize("M", [1, 5, 16, 40])
+def test_spqr_outliers_crowded_into_few_rows(qlin, M):
+    """Four rows carry weights 100x larger, so most outliers sit in them: row runs of
+    hundreds of entries inside one bucket, and units whose outliers overflow the staged copy
+    (read from global memory instead).  M = 40 runs the same layer through the prefill path."""
+    N, K, frac = 128, 1024, 0.04
+    W = synth.student_t3(23, 0.02, (N, K))
+    W[[5, 6, 7, 70]] *= 100.0
+    X = synth.activations_bf16(23, M, K)
+    layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
+    _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
+
+
 def test_spqr_one_hot_rows(qlin):
     """M == 1 accumulates exact integer products per (row, group): one-hot rows are bit-exact.
     M >= 2 dequantizes to bf16 in registers (one bf16 FMA of s^ and -s^ z^ per pair), so there
