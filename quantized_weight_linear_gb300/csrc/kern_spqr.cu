@@ -19,10 +19,11 @@
 // * M >= 2: the same A pairs are dequantized to bf16 s^ (q - z^) in registers and the
 //   MMA columns carry the tokens;
 // * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
-//   fp16 value; sorted by row, then k).  Lane L owns row L % 16: it finds where its row's run
-//   starts by bisection and accumulates value * x[k] in registers, so no two lanes ever add
-//   into the same sum (no atomics; the page's warning about the sparse part is about exactly
-//   this scattered accumulation).
+//   fp16 value; sorted by row, then k, so every row's outliers form one run).  M == 1: a
+//   segmented warp sum over the runs of 32 entries at a time; M >= 2: lane L owns row L % 16,
+//   finds its run by bisection and accumulates value * x[k] in registers.  Either way no two
+//   lanes ever add into the same sum (no atomics; the page's warning about the sparse part
+//   is about exactly this scattered accumulation).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
@@ -41,6 +42,7 @@ struct SpSmem {
   __align__(16) uint32_t offs[kOffsCap];
   __align__(16) uint32_t zeros[8];
   float rowacc[4][16][XR];
+  float orow[4][16];  // M == 1: outlier sums per row of each tile
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -186,9 +188,10 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
   float acc[NACC];
 #pragma unroll
   for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
-  // outlier sums: lane L owns row L % 16 of the tile.  With one token, or up to eight, the two
-  // lanes of a row take alternate outliers of the row and every token; with up to sixteen
-  // tokens each takes every outlier of the row and eight of the tokens.
+  // outlier sums.  M == 1: per row of the tile in shared memory (orow).  M >= 2: lane L owns
+  // row L % 16 of the tile in registers; with up to eight tokens the two lanes of a row take
+  // alternate outliers of the row and every token, with up to sixteen each takes every
+  // outlier of the row and eight of the tokens.
   constexpr int OT = (MODE == 1) ? 1 : 8;
   constexpr bool kSplitEntries = (MODE == 1) || (MT == 1);
   const int orow = lane & 15, ohalf = lane >> 4;
@@ -196,6 +199,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
   float oacc[OT];
 #pragma unroll
   for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
+  if (lane < 16) sm.orow[rt][lane] = 0.f;
+  __syncwarp();
   int64_t cur_rg = u0 / S;
   UnitCursor cur{cur_rg, (int)(u0 - cur_rg * S), (int)S};
 
@@ -233,9 +238,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-      const float ot = oacc[0] + __shfl_xor_sync(0xffffffffu, oacc[0], 16);  // row orow's outliers
-      vals[0] = r0 + __shfl_sync(0xffffffffu, ot, g);
-      vals[1] = r1 + __shfl_sync(0xffffffffu, ot, g + 8);
+      vals[0] = r0 + sm.orow[rt][g];
+      vals[1] = r1 + sm.orow[rt][g + 8];
     } else {
       if constexpr (kSplitEntries) {
 #pragma unroll
@@ -273,6 +277,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
+      __syncwarp();
+      if (lane < 16) sm.orow[rt][lane] = 0.f;
       __syncwarp();
       cur_rg = rg;
     }
@@ -421,8 +427,10 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       }
     }
 
-    // outliers of this row tile in this unit: the bucket is sorted by row (then k), so lane
-    // q <= 16 finds where row q starts by bisection and each lane walks its row's run
+    // outliers of this row tile in this unit; the bucket is sorted by row (then k), so each
+    // row's outliers form one run.  M == 1: 32 entries at a time, a segmented sum over the
+    // runs, the run's last lane adds it to the row (no atomics, no divergence).  M >= 2: lane
+    // q <= 16 finds where row q starts by bisection and each lane walks its row's run.
     {
       const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
       const uint32_t b0 = offs(4 * u + rt), b1 = offs(4 * u + rt + 1);
@@ -431,6 +439,26 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
       const uint32_t* bg = v.ents + b0;                     // the same bucket in global memory
       auto ent = [&](int i) -> uint32_t { return staged ? bs[i] : __ldg(bg + i); };
       const int n = (int)(b1 - b0);
+      if constexpr (MODE == 1) {
+        // chunks of 32 entries: segmented sum over each row's run (runs are contiguous), and
+        // the last lane of a run adds it to the row's sum
+        for (int c0 = 0; c0 < n; c0 += 32) {
+          const int i = c0 + lane;
+          const bool valid = i < n;
+          const uint32_t e = valid ? ent(i) : 0u;
+          const int r = valid ? (int)(e & 15u) : 16;
+          float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][0][(e >> 4) & 255u]) : 0.f;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const float vu = __shfl_up_sync(0xffffffffu, vsum, d);
+            const int ru = __shfl_up_sync(0xffffffffu, r, d);
+            if (lane >= d && ru == r) vsum += vu;
+          }
+          const int rn = __shfl_down_sync(0xffffffffu, r, 1);
+          if ((lane == 31 || rn != r) && r < 16) sm.orow[rt][r] += vsum;
+          __syncwarp();
+        }
+      } else {
       int lo = 0;
       if (n > 0) {
         int hi = n;
@@ -447,6 +475,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
 #pragma unroll
         for (int j = 0; j < OT; ++j)
           if (otok0 + j < (MODE == 1 ? 1 : M)) oacc[j] += val * bf2f(sm.x[s][otok0 + j][k]);
+      }
       }
     }
     __syncwarp();
