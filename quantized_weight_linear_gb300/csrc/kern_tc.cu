@@ -147,6 +147,25 @@ __device__ __forceinline__ void sts32(uint8_t* base, uint32_t off, uint32_t v) {
   *reinterpret_cast<uint32_t*>(base + off) = v;
 }
 
+// Swizzled byte offsets of one converter lane's stores, computed once.  A converter writes
+// 16-row tiles whose first row is a multiple of 16, so for its rows g and g + 8 the row's
+// low three bits are g and sw128() reduces to XOR-ing the 16-byte chunk index with g: every
+// store address is then a per-lane base plus a compile-time constant.
+struct LaneSwz {
+  uint32_t c[8];  // W4 / W8: (row g, k = 8c + 2t) of a tile starting at row 0
+  uint32_t s[2];  // SpQR: (row g, k = 16t + 8h) for h = 0, 1
+};
+
+__device__ __forceinline__ LaneSwz lane_swz(int lane) {
+  const uint32_t g = (uint32_t)lane >> 2, t = (uint32_t)lane & 3u;
+  LaneSwz L;
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c) L.c[c] = g * 128u + (((c ^ g) & 7u) << 4) + 4u * t;
+#pragma unroll
+  for (uint32_t h = 0; h < 2; ++h) L.s[h] = g * 128u + ((((2u * t + h) ^ g) & 7u) << 4);
+  return L;
+}
+
 // SpQR A-pair extraction (same field map as the decode kernel)
 template <int J, int R>
 __device__ __forceinline__ uint32_t sp_pair(const uint32_t (&w)[6]) {
@@ -176,27 +195,28 @@ __device__ __forceinline__ uint32_t sp_qsqz(const uint8_t* area, int r, int gb) 
 }
 
 template <int J, int R0>
-__device__ __forceinline__ void sp_write_j(uint8_t* bt, const uint32_t (&w)[6], int rowA, int rowB, int t,
+__device__ __forceinline__ void sp_write_j(uint8_t* bt, const uint32_t (&w)[6], uint32_t offA,
                                            uint32_t shA, uint32_t chA, uint32_t shB, uint32_t chB) {
   constexpr uint32_t base = J <= 4 ? 0x43004300u : 0x41804180u;
-  const int k = 16 * t + 2 * J;
+  // (row g, k = 16 t + 2 J) at offA + 4 (J & 3); row g + 8 is 1024 bytes further
   const uint32_t vA = bf16x2_fma(bf16x2_sub(sp_pair<J, R0>(w), base), shA, chA);
   const uint32_t vB = bf16x2_fma(bf16x2_sub(sp_pair<J, R0 + 1>(w), base), shB, chB);
-  sts32(bt, sw128(rowA, k), vA);
-  sts32(bt, sw128(rowB, k), vB);
+  sts32(bt, offA + 4u * (J & 3), vA);
+  sts32(bt, offA + 1024u + 4u * (J & 3), vB);
 }
 
 // ---- converters: one 16-row tile of the 128-row B tile for k-block kb of the packed stage
 
 template <int F>
 __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, int kb, int rt, int row0, int lane,
-                                             bool valid) {
+                                             bool valid, const LaneSwz& L) {
   const int g = lane >> 2, t = lane & 3;
+  const uint32_t rb = (uint32_t)row0 * 128u;  // row0 is a multiple of 16
   if (!valid) {  // rows past N: zero operand
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) sts32(bt, sw128(row0 + g + 8 * r, 8 * kk + 2 * t), 0u);
+      for (int kk = 0; kk < 8; ++kk) sts32(bt, rb + 1024u * r + L.c[kk], 0u);
     return;
   }
   if constexpr (F == kW4) {
@@ -210,14 +230,13 @@ __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, i
     const uint32_t sp0 = pack_bf16x2(s0, s0), sp1 = pack_bf16x2(s1, s1);
     const uint32_t zero = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 4; ++j) {  // k = 16 j + 2 t (chunk 2 j) and k + 8 (chunk 2 j + 1)
       const uint32_t w = words[j];
-      const int k = 16 * j + 2 * t;
-      sts32(bt, sw128(row0 + g, k), bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
-      sts32(bt, sw128(row0 + g + 8, k), bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
-      sts32(bt, sw128(row0 + g, k + 8), bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
-      sts32(bt, sw128(row0 + g + 8, k + 8),
-            bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
+      const uint32_t o0 = rb + L.c[2 * j], o1 = rb + L.c[2 * j + 1];
+      sts32(bt, o0, bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+      sts32(bt, o0 + 1024u, bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
+      sts32(bt, o1, bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero));
+      sts32(bt, o1 + 1024u, bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
     }
   } else if constexpr (F == kW8) {
     const uint8_t* src = unit + (rt * 32 + lane) * 32;
@@ -226,17 +245,17 @@ __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, i
     const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
     const uint32_t magic = 0x64646464u, off = 0x64806480u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k = 16 * j + 2 * t;
+    for (int j = 0; j < 4; ++j) {  // k = 16 j + 2 t (chunk 2 j) and k + 8 (chunk 2 j + 1)
+      const uint32_t o0 = rb + L.c[2 * j], o1 = rb + L.c[2 * j + 1];
       uint32_t d;
       asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
-      sts32(bt, sw128(row0 + g, k), f16x2_sub(d, off));
+      sts32(bt, o0, f16x2_sub(d, off));
       asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
-      sts32(bt, sw128(row0 + g + 8, k), f16x2_sub(d, off));
+      sts32(bt, o0 + 1024u, f16x2_sub(d, off));
       asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
-      sts32(bt, sw128(row0 + g, k + 8), f16x2_sub(d, off));
+      sts32(bt, o1, f16x2_sub(d, off));
       asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
-      sts32(bt, sw128(row0 + g + 8, k + 8), f16x2_sub(d, off));
+      sts32(bt, o1 + 1024u, f16x2_sub(d, off));
     }
   } else {  // SpQR: k-block kb of the 256-wide unit = block kb/2, groups 4*(kb%2) .. +3
     const int blk = kb >> 1, half = kb & 1;
@@ -262,25 +281,25 @@ __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, i
       const float c = -s_hat * z_hat;
       ch[r] = pack_bf16x2(c, c);
     }
-    const int rowA = row0 + g, rowB = row0 + g + 8;
+    const uint32_t s0 = rb + L.s[0], s1 = rb + L.s[1];  // k = 16 t + 2 J: J < 4 -> s0, else s1
     if (half == 0) {
-      sp_write_j<0, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<1, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<2, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<3, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<4, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<5, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<6, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<7, 0>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<0, 0>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<1, 0>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<2, 0>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<3, 0>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<4, 0>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<5, 0>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<6, 0>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<7, 0>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
     } else {
-      sp_write_j<0, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<1, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<2, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<3, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<4, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<5, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<6, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
-      sp_write_j<7, 2>(bt, w, rowA, rowB, t, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<0, 2>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<1, 2>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<2, 2>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<3, 2>(bt, w, s0, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<4, 2>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<5, 2>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<6, 2>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
+      sp_write_j<7, 2>(bt, w, s1, sh[0], ch[0], sh[1], ch[1]);
     }
   }
 }
@@ -489,6 +508,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     pdl_wait();
     const int cw = warp - 2;
     constexpr int RPW = 128 / NCONV;  // rows per converter warp: 16 or 32
+    const LaneSwz swz = lane_swz(lane);
     const int rg_local = (cw * RPW) / 64;
     const bool rg_valid = rg0 + rg_local < a.RG;
     if constexpr (F == kSpqr) {
@@ -513,7 +533,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         for (int h = 0; h < RPW / 16; ++h) {
           const int row0 = cw * RPW + 16 * h;
           const int rt = (row0 % 64) / 16;
-          convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid);
+          convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid, swz);
           if constexpr (F == kSpqr) {
             if (rg_valid) {
               __syncwarp();
