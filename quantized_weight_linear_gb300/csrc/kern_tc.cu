@@ -44,16 +44,19 @@ struct TcCfg;
 template <>
 struct TcCfg<kW4> {
   static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = 3;
+  static constexpr int kConvGroups = 1;
   static constexpr uint32_t kAType = 1;  // bf16
 };
 template <>
 struct TcCfg<kSpqr> {
-  static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4, kMH = 2, kConv = 8, kStages = 3;
+  static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4, kMH = 2, kConv = 16, kStages = 3;
+  static constexpr int kConvGroups = 2;  // two groups of 8 converter warps take alternate k-blocks
   static constexpr uint32_t kAType = 1;
 };
 template <>
 struct TcCfg<kW8> {
   static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = 3;
+  static constexpr int kConvGroups = 1;
   static constexpr uint32_t kAType = 0;  // fp16
 };
 
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   TcSmem<F>& sm = *reinterpret_cast<TcSmem<F>*>(base);
   using C = TcCfg<F>;
   constexpr int MH = C::kMH, NCONV = C::kConv, NST = C::kStages;
+  constexpr int NGRP = C::kConvGroups, GCONV = NCONV / NGRP;  // converter warps per k-block
   constexpr int BM = 128 * MH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, m_tile = blockIdx.y;
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&sm.ab_full[s], 1 + NCONV);
+      mbar_init(&sm.ab_full[s], 1 + GCONV);
       mbar_init(&sm.ab_empty[s], 1);
     }
     for (int s = 0; s < kNPK; ++s) {
@@ -506,8 +510,9 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   } else if (warp < 2 + NCONV) {
     // ------------------------------------------------------------------ converters (+ epilogue)
     pdl_wait();
-    const int cw = warp - 2;
-    constexpr int RPW = 128 / NCONV;  // rows per converter warp: 16 or 32
+    const int grp = (warp - 2) / GCONV;  // this warp converts the k-blocks i with i % NGRP == grp
+    const int cw = (warp - 2) % GCONV;
+    constexpr int RPW = 128 / GCONV;  // rows per converter warp: 16 or 32
     const LaneSwz swz = lane_swz(lane);
     const int rg_local = (cw * RPW) / 64;
     const bool rg_valid = rg0 + rg_local < a.RG;
@@ -523,6 +528,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       const uint8_t* unit = sm.pk[p] + rg_local * C::kUnitBytes;
       for (int b = 0; b < bpu; ++b) {
         const int i = ui * bpu + b;
+        if (NGRP > 1 && i % NGRP != grp) continue;
         const int s = i % NST;
         const uint32_t ph = (uint32_t)(i / NST) & 1u;
         if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
@@ -553,11 +559,11 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       if (lane == 0) mbar_arrive(&sm.pk_empty[p]);
     }
     if constexpr (F != kW8) {
-      // epilogue: TMEM lane quadrant q = warp % 4; the two warps of a quadrant take one
-      // 128-token half each
+      // epilogue (first converter group): TMEM lane quadrant q = warp % 4; the two warps of a
+      // quadrant take one 128-token half each
       const int q = warp & 3;
       const int mh = cw / 4;
-      if (ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
+      if (grp == 0 && ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
         tc_fence_after();
         const int m = m_tile * BM + 128 * mh + 32 * q + lane;
         const int n0 = n_tile * kBN;
