@@ -5,10 +5,10 @@
 // dense 3-bit codes while it runs the sparse fp16 product, and the page warns that
 // register pressure and warp divergence are the cost of the hybrid.  Design here:
 //
-// * same persistent weight stream as the W4 kernel: one CTA per SM, equal contiguous
+// * same persistent weight stream as the W4 kernel: up to four CTAs per SM, equal contiguous
 //   ranges of (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group
 //   statistics and fp16 supergroup statistics), a producer warp with cp.async.bulk into a
-//   6-deep ring, the unit's outlier bucket and X slice staged alongside;
+//   3-deep ring per CTA, the unit's outlier bucket and X slice staged alongside;
 // * code words hold five 3-bit fields per 16-bit half; one AND/OR turns a field pair into
 //   bf16 (base + q) with base 128 or 16 depending on the field, no shifts for 2 of 5;
 // * M == 1: the eight MMA columns carry eight different 16-groups (block-diagonal B), so
@@ -29,7 +29,7 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesSp = 4;
+constexpr int kStagesSp = 3;
 constexpr int kXStrideSp = 264;    // 256 bf16 + 8 pad
 constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
 constexpr int kOffsCap = 1024 + 16;  // offsets staged per CTA

@@ -4,9 +4,9 @@
 // groups pay off at small batch because the layer is bound by weight bandwidth.  The
 // kernel is therefore a weight stream:
 //
-// * persistent grid of one CTA per SM, each owning an equal, contiguous range of
+// * persistent grid of up to four CTAs per SM, each owning an equal, contiguous range of
 //   (64-row group, 128-wide K group) units (4352 bytes of codes + statistics each);
-// * one producer warp streams units with cp.async.bulk into an 8-deep shared-memory
+// * one producer warp streams units with cp.async.bulk into a 4-deep shared-memory
 //   ring (mbarrier full/empty pairs) together with the matching 128-wide slice of X;
 // * four consumer warps (one 16-row tile each) turn code words into bf16 A fragments
 //   with one AND/OR per register pair (bf16 128 + q) and one bf16 subtract of 128 + z,
