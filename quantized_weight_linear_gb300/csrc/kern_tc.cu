@@ -17,7 +17,8 @@
 //   K-major 128B-swizzled B operand; for W4 / SpQR they then run the epilogue
 //   (tcgen05.ld -> bf16 -> Y);
 // * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
-//   MMA and every 1024-wide K chunk sums below 2^24, so the fp32 chunk accumulators (TMEM
+//   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds of
+//   sum |qx| that the act-quant kernel gathers), so the fp32 chunk accumulators (TMEM
 //   columns 0..255) hold exact integers; after each chunk these warps add them into int32
 //   partial sums kept in the other half of TMEM (columns 256..511), release the accumulator
 //   to the next chunk, and after the last one write y = bf16((acc * sx) * sw) (or acc).
@@ -33,7 +34,11 @@ namespace {
 constexpr int kBN = 128, kBK = 64;
 constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
 constexpr int kNPK = 2;                    // packed-weight stages
-constexpr int kChunkBlocks = 16;           // W8A8: 16 k-blocks = 1024 K per exact chunk
+// W8A8 exact chunks: a chunk of k-blocks is accumulated in fp32 as long as the sum of its
+// blocks' bounds (max over the tile's tokens of sum |qx| per block) stays <= kExactL1, so every
+// partial sum is an integer of magnitude <= 127 * kExactL1 < 2^24 and fp32 holds it exactly.
+// A block's bound is at most 64 * 127, so a chunk holds at least 16 blocks (1024 K).
+constexpr int kExactL1 = 132104;  // floor(2^24 / 127)
 constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
 constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
 
@@ -82,6 +87,7 @@ struct TcArgs {
   const uint32_t* ents;   // SpQR outlier entries
   const float* sw;        // W8: per-row scales
   const float* sx;        // W8: per-token scales
+  const int32_t* kbound;  // W8: [M tiles of 256][K / 64] per-block bounds of sum |qx|
   uint16_t* Y;
   int32_t* acc_out;
   int32_t* status;
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   const int nkb = a.K / kBK;
   const int bpu = C::kBlocksPerUnit;
   const int nunits = nkb / bpu;
-  const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
+  const int32_t* kb = F == kW8 ? a.kbound + (int64_t)m_tile * nkb : nullptr;  // this tile's block bounds
   constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, 128);
   constexpr uint32_t tmem_cols = F == kW8 ? 512u : 128u * MH;  // W8A8: fp32 chunk sums + int32 partials
   // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
@@ -468,22 +474,29 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     // ------------------------------------------------------------------ MMA issuer
     pdl_wait();
     if (lane == 0) {
+      int bound = 0, chunk = 0;  // W8A8: running bound of the current exact chunk, its index
       for (int i = 0; i < nkb && ok; ++i) {
         const int s = i % NST;
         const uint32_t ph = (uint32_t)(i / NST) & 1u;
         uint32_t dcol = 0;
         bool first = (i == 0);
+        bool chunk_end = false;
         if constexpr (F == kW8) {
           // one fp32 accumulator: chunk c starts once the drain has read chunk c - 1
-          const int c = i / kChunkBlocks;
-          first = (i % kChunkBlocks) == 0;
-          if (first && c >= 1) {
-            if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(c - 1) & 1u, a.status)) {
+          const int bi = kb[i];
+          if (i > 0 && bound + bi > kExactL1) {
+            first = true;
+            ++chunk;
+            if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(chunk - 1) & 1u, a.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            bound = bi;
+          } else {
+            bound += bi;
           }
+          chunk_end = i == nkb - 1 || bound + kb[i + 1] > kExactL1;
         }
         if (!mbar_wait(&sm.ab_full[s], ph, a.status)) {
           ok = false;
@@ -501,7 +514,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         }
         umma_commit(&sm.ab_empty[s]);
         if constexpr (F == kW8) {
-          if ((i % kChunkBlocks) == kChunkBlocks - 1 || i == nkb - 1) umma_commit(&sm.ch_full[0]);
+          if (chunk_end) umma_commit(&sm.ch_full[0]);
         }
       }
       umma_commit(&sm.acc_full);
@@ -597,6 +610,16 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     const uint32_t fcol = 128u * mh, icol = 256u + 128u * mh;
     const int m = m_tile * BM + 128 * mh + 32 * q + lane;
     const int n0 = n_tile * kBN;
+    int nchunks = 1;  // the MMA issuer's chunking, replayed
+    for (int i = 0, bound = 0; i < nkb; ++i) {
+      const int bi = kb[i];
+      if (i > 0 && bound + bi > kExactL1) {
+        ++nchunks;
+        bound = bi;
+      } else {
+        bound += bi;
+      }
+    }
     for (int c = 0; c < nchunks && ok; ++c) {
       if (!mbar_wait(&sm.ch_full[0], (uint32_t)c & 1u, a.status)) {
         ok = false;
@@ -715,18 +738,19 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
 }  // namespace
 
 int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
-  TcArgs a{v.units, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.G};
+  TcArgs a{v.units, nullptr, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.G};
   return launch_tc<kW4>(X, a, stream);
 }
 
 int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
-  TcArgs a{v.units, v.offs, v.ents, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.S};
+  TcArgs a{v.units, v.offs, v.ents, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.S};
   return launch_tc<kSpqr>(X, a, stream);
 }
 
-int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc, int M,
+int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, const int32_t* kbound, uint16_t* Y,
+                      int32_t* acc, int M,
                       int32_t* status, void* stream) {
-  TcArgs a{v.units, nullptr, nullptr, v.sw, sx, Y, acc, status, M, v.N, v.K, v.RG, v.KB};
+  TcArgs a{v.units, nullptr, nullptr, v.sw, sx, kbound, Y, acc, status, M, v.N, v.K, v.RG, v.KB};
   return launch_tc<kW8>(q16, a, stream);
 }
 

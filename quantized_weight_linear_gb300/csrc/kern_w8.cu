@@ -26,7 +26,8 @@ constexpr int kXStrideW8 = 72;  // staged qx row: 64 fp16 + 8 pad
 template <bool F16OUT>
 __global__ void __launch_bounds__(256)
     w8_act_quant_kernel(const uint16_t* __restrict__ X, const float* __restrict__ s_inv, int K,
-                        int8_t* __restrict__ q8, uint16_t* __restrict__ q16, float* __restrict__ sx) {
+                        int8_t* __restrict__ q8, uint16_t* __restrict__ q16, float* __restrict__ sx,
+                        int32_t* __restrict__ kbound) {
   __shared__ float red[8];
   __shared__ float scale_sh;
   pdl_wait();
@@ -65,6 +66,19 @@ __global__ void __launch_bounds__(256)
       const float x = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
       int q = __float2int_rn(__fdiv_rn(__fmul_rn(x, s_inv[k + e]), sc));
       qv[e] = q < -127 ? -127 : (q > 127 ? 127 : q);
+    }
+    if (kbound) {
+      // sum |q| of this token's 64-wide k-block (8 threads of 8 codes), max into its tile's bound
+      int l1 = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) l1 += qv[e] < 0 ? -qv[e] : qv[e];
+      // K is a multiple of 64, so the 8 lanes of a k-block are in the loop together (a warp's
+      // tail may not be)
+      const unsigned am = __activemask();
+      l1 += __shfl_xor_sync(am, l1, 1);
+      l1 += __shfl_xor_sync(am, l1, 2);
+      l1 += __shfl_xor_sync(am, l1, 4);
+      if ((threadIdx.x & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + k / 64, l1);
     }
     if constexpr (F16OUT) {
       uint32_t o[4];
@@ -303,7 +317,8 @@ int launch_w8_mt(const W8View& v, const uint16_t* q16, const float* sx, uint16_t
 }
 
 template <bool F16>
-int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, float* sx, int M, void* stream) {
+int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, float* sx, int32_t* kbound, int M,
+              void* stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M);
   cfg.blockDim = dim3(256);
@@ -314,17 +329,18 @@ int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, flo
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx);
+  return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx, kbound);
 }
 
 }  // namespace
 
 int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M, void* stream) {
-  return launch_aq<false>(v, X, qx, nullptr, sx, M, stream);
+  return launch_aq<false>(v, X, qx, nullptr, sx, nullptr, M, stream);
 }
 
-int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int M, void* stream) {
-  return launch_aq<true>(v, X, nullptr, q16, sx, M, stream);
+int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int32_t* kbound, int M,
+                            void* stream) {
+  return launch_aq<true>(v, X, nullptr, q16, sx, kbound, M, stream);
 }
 
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc_out, int M,

@@ -738,7 +738,7 @@ static int decode_grid(const qlin_layer* L) {
 
 // workspace carve-up
 struct WsLayout {
-  size_t status, partials, counters, qx, sx, total;
+  size_t status, partials, counters, qx, sx, kbound, total;
 };
 static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   WsLayout w{};
@@ -753,7 +753,10 @@ static WsLayout ws_layout(const qlin_layer* L, int maxM) {
     sx_bytes = align256((size_t)std::max(maxM, 1) * 4);
   }
   w.sx = w.qx + qx_bytes;
-  w.total = w.sx + sx_bytes;
+  size_t kb_bytes = 0;
+  if (L->format == QLIN_FMT_W8A8) kb_bytes = align256((size_t)((std::max(maxM, 1) + 255) / 256) * (L->K / 64) * 4);
+  w.kbound = w.sx + sx_bytes;
+  w.total = w.kbound + kb_bytes;
   return w;
 }
 
@@ -909,6 +912,7 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
   h->wsv.counters = reinterpret_cast<uint32_t*>(h->ws + w.counters);
   h->wsv.qx = h->ws + w.qx;
   h->wsv.sx = reinterpret_cast<float*>(h->ws + w.sx);
+  h->wsv.kbound = reinterpret_cast<int32_t*>(h->ws + w.kbound);
   h->wsv.grid = h->grid;
   h->wsv.sms = sm_count_cached();
   return QLIN_OK;
@@ -935,7 +939,7 @@ static qlin_status run_decode(qlin_handle h, const uint16_t* X, uint16_t* Y, int
       break;
     case QLIN_FMT_W8A8: {
       uint16_t* q16 = reinterpret_cast<uint16_t*>(h->wsv.qx);
-      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, M, s);
+      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, nullptr, M, s);
       if (!e) e = launch_w8_decode(w8view(h), q16, h->wsv.sx, Y, acc, M, h->wsv, h->grid, s);
       break;
     }
@@ -957,8 +961,11 @@ static qlin_status run_prefill(qlin_handle h, const uint16_t* X, uint16_t* Y, in
       break;
     case QLIN_FMT_W8A8: {
       uint16_t* q16 = reinterpret_cast<uint16_t*>(h->wsv.qx);
-      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, M, s);
-      if (!e) e = launch_w8_prefill(w8view(h), q16, h->wsv.sx, Y, acc, M, h->wsv.status, s);
+      // per-tile bounds of sum |qx| per k-block, gathered by the act-quant kernel with atomicMax
+      const size_t kb_bytes = (size_t)((M + 255) / 256) * (h->K / 64) * 4;
+      e = (int)cudaMemsetAsync(h->wsv.kbound, 0, kb_bytes, s);
+      if (!e) e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, h->wsv.kbound, M, s);
+      if (!e) e = launch_w8_prefill(w8view(h), q16, h->wsv.sx, h->wsv.kbound, Y, acc, M, h->wsv.status, s);
       break;
     }
     default:

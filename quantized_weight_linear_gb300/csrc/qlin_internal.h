@@ -90,6 +90,8 @@ struct Workspace {
   uint32_t* counters;  // [RG] arrival counters of split row groups
   void* qx;            // W8A8: fp16 activation codes [maxM][K]
   float* sx;           // W8A8: [maxM]
+  int32_t* kbound;     // W8A8 prefill: [ceil(maxM / 256)][K / 64] max over a 256-token tile of
+                       // sum |qx| over a 64-wide k-block (sizes the exact fp32 chunks)
   int grid;            // largest decode grid the partial slots were sized for
   int sms;             // SM count of the device
 };
@@ -103,15 +105,15 @@ int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M,
                        const Workspace& ws, int grid, void* stream);
 int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M,
                         void* stream);
-int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int M,
+int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int32_t* kbound, int M,
                             void* stream);
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y,
                      int32_t* acc_out, int M, const Workspace& ws, int grid, void* stream);
 int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream);
 int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status,
                         void* stream);
-int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc,
-                      int M, int32_t* status, void* stream);
+int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, const int32_t* kbound, uint16_t* Y,
+                      int32_t* acc, int M, int32_t* status, void* stream);
 int spqr_decode_grid(const SpqrView& v, int M, int sms);
 
 }  // namespace qlin

@@ -1,8 +1,8 @@
 """GPU parity of the tensor-core prefill path (M > 16) against the oracle, through the C ABI.
 
 W4 / SpQR: bf16 outputs within 1e-2 * sum |x w| + 1 ulp of the fp64 oracle.
-W8A8: int32 accumulators and bf16 outputs bit-exact (the fp16 MMA is exact on int8 codes
-and the 1024-wide K chunks are drained into int32).
+W8A8: int32 accumulators and bf16 outputs bit-exact (the fp16 MMA is exact on int8 codes,
+and K is cut into chunks whose sums stay below 2^24, drained into int32).
 """
 import numpy as np
 import pytest
@@ -49,6 +49,29 @@ def test_w8a8_prefill_bit_exact(qlin, N, K, M):
     layer = qlin.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)
     pk = smoothquant.quantize_weights(W, absmax, 0.85)
     y_ref, acc_ref, _, _ = smoothquant.forward(bits_to_f32(X), pk)
+    acc = layer.forward_acc(torch.from_numpy(X).cuda().view(torch.bfloat16)).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), acc_ref)
+    y = _y(layer, X)
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("K,M,sign", [(3072, 40, 1.0), (2048, 300, -1.0)])
+def test_w8a8_prefill_exact_at_largest_codes(qlin, K, M, sign):
+    """Every activation and weight code at +-127, so each 1024-wide chunk sums to 127^2 * 1024
+    (just under 2^24) and the whole row far above it: the chunking and the int32 drain must
+    still give the exact accumulator.  A few tokens of small codes ride along in the tile, and
+    M = 300 leaves a partial 256-token tile."""
+    N = 128
+    W = np.full((N, K), 0.02, dtype=np.float32)
+    W[1::2] *= sign
+    x = np.ones((M, K), dtype=np.float32)
+    x[::7] = 0.01 * synth.normal(5, synth.KEY_X, 1.0, (len(range(0, M, 7)), K))
+    X = synth.f32_to_bf16(x)
+    absmax = synth.channel_absmax(X)
+    layer = qlin.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)
+    pk = smoothquant.quantize_weights(W, absmax, 0.85)
+    y_ref, acc_ref, _, _ = smoothquant.forward(bits_to_f32(X), pk)
+    assert np.abs(acc_ref).max() > 2 ** 24  # the exactness limit of one fp32 accumulation
     acc = layer.forward_acc(torch.from_numpy(X).cuda().view(torch.bfloat16)).cpu().numpy()
     assert np.array_equal(acc.astype(np.int64), acc_ref)
     y = _y(layer, X)
