@@ -124,10 +124,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
   W8Smem<MT>& sm = *reinterpret_cast<W8Smem<MT>*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t grid = gridDim.x, cta = blockIdx.x;
-  // scalars of the view as locals: lambdas capture them, and capturing the kernel parameter
-  // itself would move it to local memory
-  const int64_t vN = v.N, vK = v.K;
-  const float* vsw = v.sw;
   const int64_t KB = v.KB, U = (int64_t)v.RG * KB;
   const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
   const int n_units = (int)(u1 - u0);
@@ -155,7 +151,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     int kx = (int)(u0 % KB);  // K block of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
       const int64_t k0 = (int64_t)kx * kW8Block;
-      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], q16 + (int64_t)m * vK + k0, xbytes, &sm.full[s]);
+      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], q16 + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
       if (++kx == (int)KB) kx = 0;
     };
     const int pro = n_units < kStagesW8 ? n_units : kStagesW8;
@@ -217,12 +213,12 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
       if (idx[j] < 0) continue;
       const int64_t n = rg * kRowGroup + idx[j] / 16;
       const int m = idx[j] % 16;
-      if (n >= vN) continue;
+      if (n >= v.N) continue;
       if (acc_out) {
-        acc_out[(int64_t)m * vN + n] = out[j];
+        acc_out[(int64_t)m * v.N + n] = out[j];
       } else {
-        const float y = __fmul_rn(__fmul_rn(__int2float_rn(out[j]), sx[m]), vsw[n]);
-        Y[(int64_t)m * vN + n] = f2bf(y);
+        const float y = __fmul_rn(__fmul_rn(__int2float_rn(out[j]), sx[m]), v.sw[n]);
+        Y[(int64_t)m * v.N + n] = f2bf(y);
       }
     }
   };
@@ -283,11 +279,11 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
     fin.finish(M, cs, sm.flags, [&](int64_t rg, int e, int val) {
       const int64_t n = rg * kRowGroup + e / 16;
       const int m = e % 16;
-      if (n >= vN) return;
+      if (n >= v.N) return;
       if (acc_out) {
-        acc_out[(int64_t)m * vN + n] = val;
+        acc_out[(int64_t)m * v.N + n] = val;
       } else {
-        Y[(int64_t)m * vN + n] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn(val), sx[m]), vsw[n]));
+        Y[(int64_t)m * v.N + n] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn(val), sx[m]), v.sw[n]));
       }
     });
   }
