@@ -432,8 +432,11 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
     // runs, the run's last lane adds it to the row (no atomics, no divergence).  M >= 2: lane
     // q <= 16 finds where row q starts by bisection and each lane walks its row's run.
     {
-      const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
-      const uint32_t b0 = offs(4 * u + rt), b1 = offs(4 * u + rt + 1);
+      // the unit's four bucket starts in one 16-byte load (the staged offsets start at 4 u0)
+      const uint4 o4 = *reinterpret_cast<const uint4*>(&sm.offs[4 * it]);
+      const uint32_t e0 = o4.x, e1 = offs(4 * u + 4);
+      const uint32_t b0 = rt == 0 ? o4.x : rt == 1 ? o4.y : rt == 2 ? o4.z : o4.w;
+      const uint32_t b1 = rt == 0 ? o4.y : rt == 1 ? o4.z : rt == 2 ? o4.w : e1;
       const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
       const uint32_t* bs = sm.out[s] + (b0 - (e0 & ~3u));  // staged bucket
       const uint32_t* bg = v.ents + b0;                     // the same bucket in global memory
@@ -448,14 +451,17 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
           const uint32_t e = valid ? ent(i) : 0u;
           const int r = valid ? (int)(e & 15u) : 16;
           float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][0][(e >> 4) & 255u]) : 0.f;
+          // runs from head flags: lane l's run starts at the last head at or below l
+          const int rprev = __shfl_up_sync(0xffffffffu, r, 1);
+          const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || rprev != r);
+          const int start = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
 #pragma unroll
           for (int d = 1; d < 32; d <<= 1) {
             const float vu = __shfl_up_sync(0xffffffffu, vsum, d);
-            const int ru = __shfl_up_sync(0xffffffffu, r, d);
-            if (lane >= d && ru == r) vsum += vu;
+            if (lane - d >= start) vsum += vu;
           }
-          const int rn = __shfl_down_sync(0xffffffffu, r, 1);
-          if ((lane == 31 || rn != r) && r < 16) sm.orow[rt][r] += vsum;
+          const bool run_end = lane == 31 || ((heads >> (lane + 1)) & 1u);
+          if (run_end && r < 16) sm.orow[rt][r] += vsum;
           __syncwarp();
         }
       } else {
