@@ -323,13 +323,13 @@ def _extra_configs(q, torch, stream, l2):
     return out
 
 
-def _prefill_configs(q, torch, stream):
+def _prefill_configs(q, torch, stream, fmts=("w4g128", "spqr1pct", "w8a8")):
     """Prefill M=4096 on K=8192, N=28672 for the three formats (tensor-core path): TFLOP/s."""
     import qlin_synth as synth
     out = {}
     M, K, N = 4096, 8192, 28672
     flops = 2.0 * M * N * K
-    for fmt in ("w4g128", "spqr1pct", "w8a8"):
+    for fmt in fmts:
         try:
             if fmt == "w8a8":
                 W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
@@ -464,9 +464,19 @@ def main():
     ap.add_argument("--no-extra", dest="no_extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
     ap.add_argument("--_oracle_only", dest="oracle_only", action="store_true")
+    ap.add_argument("--prefill-case", dest="prefill_case", choices=["w4g128", "spqr1pct", "w8a8"],
+                    help="time only this M=4096 prefill configuration (for profiling) and print its line")
     args = ap.parse_args()
     if args.oracle_only:
         print(json.dumps(_oracle_spqr_forward_time()))
+        return
+    if args.prefill_case:
+        import torch
+        import quantized_weight_linear_gb300 as q
+        from quantized_weight_linear_gb300.build import build
+        build()
+        q.lib()
+        print(json.dumps(_prefill_configs(q, torch, torch.cuda.Stream(), (args.prefill_case,))))
         return
     if args.warmup < 3:
         args.warmup = 3
