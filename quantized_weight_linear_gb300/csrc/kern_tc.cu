@@ -33,7 +33,6 @@ namespace {
 
 constexpr int kBN = 128, kBK = 64;
 constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
-constexpr int kNPK = 2;                    // packed-weight stages
 // W8A8 exact chunks: a chunk of k-blocks is accumulated in fp32 as long as the sum of its
 // blocks' bounds (max over the tile's tokens of sum |qx| per block) stays <= kExactL1, so every
 // partial sum is an integer of magnitude <= 127 * kExactL1 < 2^24 and fp32 holds it exactly.
@@ -44,24 +43,37 @@ constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row
 
 enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 
+#ifndef QLIN_W8_NPK
+#define QLIN_W8_NPK 4
+#endif
+#ifndef QLIN_W4_NPK
+#define QLIN_W4_NPK 2
+#endif
+#ifndef QLIN_SP_NPK
+#define QLIN_SP_NPK 2
+#endif
+
 template <int F>
 struct TcCfg;
 template <>
 struct TcCfg<kW4> {
   static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = 3;
   static constexpr int kConvGroups = 1;
+  static constexpr int kNPK = QLIN_W4_NPK;  // packed-unit stages (each covers kBlocksPerUnit k-blocks)
   static constexpr uint32_t kAType = 1;  // bf16
 };
 template <>
 struct TcCfg<kSpqr> {
   static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4, kMH = 2, kConv = 16, kStages = 3;
   static constexpr int kConvGroups = 2;  // two groups of 8 converter warps take alternate k-blocks
+  static constexpr int kNPK = QLIN_SP_NPK;
   static constexpr uint32_t kAType = 1;
 };
 template <>
 struct TcCfg<kW8> {
   static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = 3;
   static constexpr int kConvGroups = 1;
+  static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
 };
 
@@ -70,11 +82,11 @@ struct TcSmem {
   using C = TcCfg<F>;
   __align__(1024) uint8_t a[C::kStages][C::kMH * kTileBytes];
   __align__(1024) uint8_t b[C::kStages][kTileBytes];
-  __align__(16) uint8_t pk[kNPK][2 * C::kUnitBytes];
-  __align__(16) uint32_t out[F == kSpqr ? kNPK : 1][2][F == kSpqr ? kOutCapTc + 8 : 4];
+  __align__(16) uint8_t pk[C::kNPK][2 * C::kUnitBytes];
+  __align__(16) uint32_t out[F == kSpqr ? C::kNPK : 1][2][F == kSpqr ? kOutCapTc + 8 : 4];
   __align__(16) uint32_t offs[2][F == kSpqr ? kOffsCapTc : 4];
   uint64_t ab_full[C::kStages], ab_empty[C::kStages];
-  uint64_t pk_full[kNPK], pk_empty[kNPK];
+  uint64_t pk_full[C::kNPK], pk_empty[C::kNPK];
   uint64_t offs_bar;
   uint64_t acc_full;
   uint64_t ch_full[2], ch_empty[2];
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       mbar_init(&sm.ab_full[s], 1 + GCONV);
       mbar_init(&sm.ab_empty[s], 1);
     }
-    for (int s = 0; s < kNPK; ++s) {
+    for (int s = 0; s < C::kNPK; ++s) {
       mbar_init(&sm.pk_full[s], 1);
       mbar_init(&sm.pk_empty[s], NCONV);
     }
@@ -421,8 +433,8 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         ok = mbar_wait(&sm.offs_bar, 0, a.status);
       }
       auto load_units = [&](int ui) -> bool {
-        const int p = ui % kNPK;
-        const uint32_t ph = (uint32_t)(ui / kNPK) & 1u;
+        const int p = ui % C::kNPK;
+        const uint32_t ph = (uint32_t)(ui / C::kNPK) & 1u;
         if (!mbar_wait(&sm.pk_empty[p], ph ^ 1u, a.status)) return false;
         uint32_t bytes = 0;
         uint32_t e_lo[2] = {0, 0}, e_hi[2] = {0, 0};
@@ -452,10 +464,10 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       };
       // weights do not depend on the previous kernel: prefetch before the dependency wait
       int next_unit = 0;
-      for (; next_unit < kNPK && next_unit < nunits && ok; ++next_unit) ok = load_units(next_unit);
+      for (; next_unit < C::kNPK && next_unit < nunits && ok; ++next_unit) ok = load_units(next_unit);
       pdl_wait();
       for (int i = 0; i < nkb && ok; ++i) {
-        if (i % bpu == 0 && i / bpu + kNPK - 1 >= next_unit && next_unit < nunits) {
+        if (i % bpu == 0 && i / bpu + C::kNPK - 1 >= next_unit && next_unit < nunits) {
           ok = load_units(next_unit);
           ++next_unit;
           if (!ok) break;
@@ -533,8 +545,8 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       if (!mbar_wait(&sm.offs_bar, 0, a.status)) ok = false;
     }
     for (int ui = 0; ui < nunits && ok; ++ui) {
-      const int p = ui % kNPK;
-      if (!mbar_wait(&sm.pk_full[p], (uint32_t)(ui / kNPK) & 1u, a.status)) {
+      const int p = ui % C::kNPK;
+      if (!mbar_wait(&sm.pk_full[p], (uint32_t)(ui / C::kNPK) & 1u, a.status)) {
         ok = false;
         break;
       }
