@@ -43,8 +43,16 @@ constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row
 
 enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 
+// Ring depths (compile-time knobs; defaults measured on GB300 at M = 4096, K = 8192,
+// N = 28672): X/B operand stages and packed-unit stages per format.
 #ifndef QLIN_W8_NPK
 #define QLIN_W8_NPK 4
+#endif
+#ifndef QLIN_W4_ST
+#define QLIN_W4_ST 4
+#endif
+#ifndef QLIN_W8_ST
+#define QLIN_W8_ST 3
 #endif
 #ifndef QLIN_W4_NPK
 #define QLIN_W4_NPK 2
@@ -57,7 +65,7 @@ template <int F>
 struct TcCfg;
 template <>
 struct TcCfg<kW4> {
-  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = 3;
+  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = QLIN_W4_ST;
   static constexpr int kConvGroups = 1;
   static constexpr int kNPK = QLIN_W4_NPK;  // packed-unit stages (each covers kBlocksPerUnit k-blocks)
   static constexpr uint32_t kAType = 1;  // bf16
@@ -71,7 +79,7 @@ struct TcCfg<kSpqr> {
 };
 template <>
 struct TcCfg<kW8> {
-  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = 3;
+  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = QLIN_W8_ST;
   static constexpr int kConvGroups = 1;
   static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
