@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
 }
 
 template <int MODE, int MT>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT
-__global__ void __launch_bounds__(160, MODE == 1 ? 4 : 2)
+__global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     spqr_decode_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -527,7 +527,7 @@ int spqr_decode_grid(const SpqrView& v, int M, int sms) {
   // several CTAs per SM hide the unpack latency; every CTA stages its slice of the bucket
   // offsets, so ranges stay below kOffsCap entries
   const int64_t U = (int64_t)v.RG * v.S;
-  const int cps = std::min(M == 1 ? 4 : 2, QLIN_DECODE_CPS_MAX);
+  const int cps = std::min(M == 1 ? 4 : (M <= 8 ? 3 : 2), QLIN_DECODE_CPS_MAX);
   int64_t grid = std::min<int64_t>(U, (int64_t)cps * sms);
   const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
   if (grid < need) grid = std::min<int64_t>(U, need);
