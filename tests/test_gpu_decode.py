@@ -101,6 +101,24 @@ def test_spqr_outliers_crowded_into_few_rows(qlin, M):
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
 
 
+@pytest.mark.parametrize("M", [1, 5, 40])
+def test_spqr_widest_rows(qlin, M):
+    """K = 32768, the widest row the int16 outlier columns allow (128 supergroups per row
+    group, a long staged range of bucket offsets per CTA), decode and prefill."""
+    N, K = 96, 32768
+    W, X = synth.spqr_layer(N, K, M, seed=31)
+    layer = qlin.QLinear.from_spqr(W, 0.01).to("cuda")
+    _check(_y(layer, X, M), X, spqr.pack(W, 0.01)["w_hat"])
+
+
+@pytest.mark.parametrize("M", [1, 16, 40])
+def test_w4_widest_rows(qlin, M):
+    N, K = 96, 32768
+    W, X = synth.gptq_layer(N, K, M, seed=32)
+    layer = qlin.QLinear.from_w4g128(W).to("cuda")
+    _check(_y(layer, X, M), X, gptq_w4.pack(W)["w_hat"])
+
+
 def test_spqr_one_hot_rows(qlin):
     """M == 1 accumulates exact integer products per (row, group): one-hot rows are bit-exact.
     M >= 2 dequantizes to bf16 in registers (one bf16 FMA of s^ and -s^ z^ per pair), so there

@@ -81,6 +81,8 @@ def test_packers_reject_bad_input(qlin):
     with pytest.raises(qlin.QlinError):
         qlin.qlin_pack_spqr(np.zeros((8, 200), dtype=np.float32), 0.01)   # K % 256
     with pytest.raises(qlin.QlinError):
+        qlin.qlin_pack_spqr(np.zeros((2, 32768 + 256), dtype=np.float32), 0.01)   # int16 columns
+    with pytest.raises(qlin.QlinError):
         qlin.qlin_pack_spqr(W, 1.5)
     with pytest.raises(qlin.QlinError):
         qlin.qlin_pack_w8(W, np.ones(256, np.float32), 1.5)
