@@ -159,4 +159,123 @@ struct RowGroupFinisher {
   }
 };
 
+// Completion for one token (M == 1) without atomics: the CTA that holds the first unit of a
+// shared row group owns it -- it is the owner's last row group and every other contributor's
+// first, so a CTA owns at most one.  Contributors store their 64 partial sums as 8-byte words
+// (value bits, tag) into their slot of `tagged` and move on: no fence, no atomic, no wait.
+// The owner keeps its own sums in shared memory and, at the end of its range, reads the
+// contributors' words from L2 until every one carries the workspace's tag (an aligned 8-byte
+// word is written and read as one access, so a word with the tag holds its value), adds them
+// in CTA order (deterministic), writes the outputs and stores zero words back, so no slot
+// holds a valid-looking word between forwards.  Owners wait only on higher-numbered CTAs,
+// which never wait on lower ones, so the waits cannot form a cycle; every wait is bounded.
+// Same interface as RowGroupFinisher; entries are idx = row_in_group * 16.
+__device__ __forceinline__ void st_relaxed_b64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_b64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int NV>
+struct OwnerFinisher {
+  uint64_t* tagged;  // [grid][2][64] words (copied from the workspace, see RowGroupFinisher)
+  int32_t* status;
+  float* own;        // shared memory [64]: the owner's own partial sums
+  uint32_t tag;
+  int cta;
+  int rg[2];         // shared row groups: [0] the first of the range, [1] the last (-1: none)
+  int owned;         // side of the row group this CTA owns, -1 if none
+  int others;        // contributors after this CTA to the owned row group
+  int pend;          // 1 once the owned row group has been staged
+
+  __device__ __forceinline__ OwnerFinisher(int64_t per_rg, int64_t units, int64_t grid, int64_t cta_,
+                                           uint64_t* tagged_, uint32_t tag_, int32_t* status_, float* own_)
+      : tagged(tagged_), status(status_), own(own_), tag(tag_), cta((int)cta_), owned(-1), others(0), pend(0) {
+    const int64_t u0 = split_start(cta_, units, grid), u1 = split_start(cta_ + 1, units, grid);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      rg[s] = -1;
+      if (u1 <= u0) continue;
+      const int64_t r = (s == 0 ? u0 : u1 - 1) / per_rg;
+      if (s == 1 && r == u0 / per_rg) continue;
+      const SplitInfo si = split_info(r, per_rg, units, grid);
+      if (si.first_cta == si.last_cta) continue;
+      rg[s] = (int)r;
+      if (si.first_cta == cta_) {
+        owned = s;
+        others = (int)(si.last_cta - si.first_cta);
+      }
+    }
+  }
+
+  template <typename Done>
+  __device__ __forceinline__ void stage(int64_t r, const float (&vals)[NV], const int (&idx)[NV], Done done) {
+    const int s = (r == rg[0]) ? 0 : (r == rg[1]) ? 1 : -1;
+    if (s < 0) {
+      done(r, vals);
+      return;
+    }
+    if (s == owned) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (idx[i] >= 0) own[idx[i] >> 4] = vals[i];
+      pend = 1;
+      return;
+    }
+    uint64_t* slot = tagged + (int64_t)(cta * 2 + s) * kRowGroup;
+    const uint64_t hi = (uint64_t)tag << 32;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (idx[i] >= 0) st_relaxed_b64(slot + (idx[i] >> 4), hi | __float_as_uint(vals[i]));
+  }
+
+  // Only the owner works here; thread j < 64 finishes row j.  `put(rg, entry, value)`.
+  template <typename Put>
+  __device__ __forceinline__ bool finish(int M, ConsumerSync& cs, int* flags, Put put) {
+    (void)M;
+    (void)flags;
+    if (!pend) return true;  // uniform over the consumer threads
+    if (!cs.sync()) return false;
+    const int row = threadIdx.x;
+    if (row >= kRowGroup) return true;
+    float acc = own[row];
+    constexpr int B = 8;  // contributors loaded per L2 round trip
+    for (int c0 = 0; c0 < others; c0 += B) {
+      uint64_t v[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u)
+        if (c0 + u < others) v[u] = ld_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row);
+      // poll the whole batch: reload every word not yet tagged, one round trip per pass
+      uint64_t t0 = 0;
+      for (;;) {
+        unsigned missing = 0;
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+          if (c0 + u < others && (uint32_t)(v[u] >> 32) != tag) missing |= 1u << u;
+        if (!missing) break;
+        if (t0 == 0) {
+          t0 = global_ns();
+        } else if (global_ns() - t0 > kWaitLimitNs) {
+          atomicExch(status, kStatusTimeout);
+          return false;
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+          if (missing & (1u << u)) v[u] = ld_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row);
+      }
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        if (c0 + u >= others) continue;
+        acc += __uint_as_float((uint32_t)v[u]);
+        st_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row, 0ull);
+      }
+    }
+    put((int64_t)rg[owned], row * 16, acc);
+    return true;
+  }
+};
+
 }  // namespace qlin

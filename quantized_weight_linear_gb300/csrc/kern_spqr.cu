@@ -43,6 +43,7 @@ struct SpSmem {
   __align__(16) uint32_t zeros[8];
   float rowacc[4][16][XR];
   float orow[4][16];  // M == 1: outlier sums per row of each tile
+  float own[kRowGroup];  // M == 1: this CTA's partial sums of the row group it owns
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -228,7 +229,13 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       if (n < vN) Y[(int64_t)m * vN + n] = f2bf(out[j]);
     }
   };
-  RowGroupFinisher<float, NV> fin(S, U, grid, cta, ws.partials, ws.counters);
+  // one token: the owner-reduces completion (no atomics); more tokens: counted arrivals
+  auto fin = [&] {
+    if constexpr (MODE == 1)
+      return OwnerFinisher<NV>(S, U, grid, cta, ws.tagged, ws.tag, ws.status, sm.own);
+    else
+      return RowGroupFinisher<float, NV>(S, U, grid, cta, ws.partials, ws.counters);
+  }();
   auto flush = [&](int64_t rg) {
     __syncwarp();
     float vals[NV];

@@ -6,12 +6,12 @@
 // memory up front for its own pools and gives plugins no workspace, or a service that forbids
 // any device allocation after start-up because an allocation can stall or fail while
 // requests are in flight.  qlin_forward needs a workspace (split-row partial sums, their
-// arrival counters and the status word); this entry point takes that scratch from
+// arrival counters or tags, and the status word); this entry point takes that scratch from
 // `g_spqr_static_scratch` below.
 //
 // Limits of the fixed array: at most kStaticMaxGrid CTAs (4 per SM on up to 160 SMs) and
 // kStaticMaxRowGroups row groups of 64 output rows (N <= 524288); larger requests return
-// QLIN_ERR_WORKSPACE.  Every GPU that loads the library holds the array (about 5.3 MB) until
+// QLIN_ERR_WORKSPACE.  Every GPU that loads the library holds the array (about 6 MB) until
 // the process exits.
 #include <mutex>
 
@@ -25,17 +25,19 @@ constexpr int kStaticMaxGrid = 640;
 constexpr int kStaticMaxRowGroups = 8192;
 constexpr size_t kStaticPartialsOff = 256;
 constexpr size_t kStaticCountersOff = kStaticPartialsOff + (size_t)kStaticMaxGrid * 2 * kRowGroup * 16 * 4;
-constexpr size_t kStaticScratchBytes = kStaticCountersOff + (size_t)kStaticMaxRowGroups * 4;
+constexpr size_t kStaticTaggedOff = kStaticCountersOff + (size_t)kStaticMaxRowGroups * 4;
+constexpr size_t kStaticScratchBytes = kStaticTaggedOff + (size_t)kStaticMaxGrid * 2 * kRowGroup * 8;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_spqr_static_scratch[kStaticScratchBytes];
 
 std::mutex g_mu;
 void* g_dev_ptr[kMaxDevices];
+uint32_t g_tag[kMaxDevices];  // tag of the last call on each device
 
 // Device address of the scratch array on the current device; looked up once per device
 // (cudaGetSymbolAddress with that device current), then cached.
-qlin_status scratch_on_current_device(uint8_t** out, int* sms) {
+qlin_status scratch_on_current_device(uint8_t** out, int* sms, uint32_t* tag) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QLIN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -45,6 +47,8 @@ qlin_status scratch_on_current_device(uint8_t** out, int* sms) {
     g_dev_ptr[dev] = p;
   }
   *out = static_cast<uint8_t*>(g_dev_ptr[dev]);
+  if (++g_tag[dev] == 0u) g_tag[dev] = 1u;  // 0 marks a word as not written
+  *tag = g_tag[dev];
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return QLIN_ERR_CUDA;
   *sms = n;
@@ -65,12 +69,14 @@ extern "C" qlin_status qlin_forward_spqr_static(qlin_handle h, const void* X, vo
   if (!X || !Y || ((uintptr_t)X & 15u) || ((uintptr_t)Y & 15u)) return QLIN_ERR_INVALID_ARG;
   uint8_t* scratch = nullptr;
   int sms = 0;
-  qlin_status s = scratch_on_current_device(&scratch, &sms);
+  uint32_t tag = 0;
+  qlin_status s = scratch_on_current_device(&scratch, &sms, &tag);
   if (s != QLIN_OK) return s;
   const int grid = spqr_decode_grid(v, M, sms);
   if (grid > kStaticMaxGrid || v.RG > kStaticMaxRowGroups) return QLIN_ERR_WORKSPACE;
   // the array keeps the previous call's contents: clear the status word and the counters
-  // (partial slots are always written before they are read)
+  // (plain partial slots are always written before they are read, and tagged words carry a
+  // tag of this call's own)
   cudaStream_t cs = (cudaStream_t)stream;
   if (cudaMemsetAsync(scratch, 0, 256, cs) != cudaSuccess) return QLIN_ERR_CUDA;
   if (cudaMemsetAsync(scratch + kStaticCountersOff, 0, (size_t)v.RG * 4, cs) != cudaSuccess) return QLIN_ERR_CUDA;
@@ -78,6 +84,8 @@ extern "C" qlin_status qlin_forward_spqr_static(qlin_handle h, const void* X, vo
   ws.status = reinterpret_cast<int32_t*>(scratch);
   ws.partials = reinterpret_cast<float*>(scratch + kStaticPartialsOff);
   ws.counters = reinterpret_cast<uint32_t*>(scratch + kStaticCountersOff);
+  ws.tagged = reinterpret_cast<uint64_t*>(scratch + kStaticTaggedOff);
+  ws.tag = tag;
   ws.qx = nullptr;
   ws.sx = nullptr;
   ws.grid = kStaticMaxGrid;

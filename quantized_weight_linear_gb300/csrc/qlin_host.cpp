@@ -738,7 +738,7 @@ static int decode_grid(const qlin_layer* L) {
 
 // workspace carve-up
 struct WsLayout {
-  size_t status, partials, counters, qx, sx, kbound, total;
+  size_t status, partials, counters, tagged, qx, sx, kbound, total;
 };
 static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   WsLayout w{};
@@ -746,7 +746,8 @@ static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   w.status = 0;
   w.partials = 256;
   w.counters = w.partials + align256((size_t)grid * 2 * kRowGroup * 16 * 4);
-  w.qx = w.counters + align256((size_t)L->RG * 4);
+  w.tagged = w.counters + align256((size_t)L->RG * 4);
+  w.qx = w.tagged + align256((size_t)grid * 2 * kRowGroup * 8);
   size_t qx_bytes = 0, sx_bytes = 0;
   if (L->format == QLIN_FMT_W8A8) {
     qx_bytes = align256((size_t)std::max(maxM, 1) * L->K * 2);
@@ -910,6 +911,8 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
   h->wsv.status = reinterpret_cast<int32_t*>(h->ws + w.status);
   h->wsv.partials = reinterpret_cast<float*>(h->ws + w.partials);
   h->wsv.counters = reinterpret_cast<uint32_t*>(h->ws + w.counters);
+  h->wsv.tagged = reinterpret_cast<uint64_t*>(h->ws + w.tagged);
+  h->wsv.tag = 1u;
   h->wsv.qx = h->ws + w.qx;
   h->wsv.sx = reinterpret_cast<float*>(h->ws + w.sx);
   h->wsv.kbound = reinterpret_cast<int32_t*>(h->ws + w.kbound);
