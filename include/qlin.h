@@ -152,7 +152,7 @@ qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stre
  * service that forbids device allocation once it is serving.  The pages have no counterpart;
  * this is a deployment form of qlin_forward, same kernel, same results.
  * The scratch (partial sums of split row groups, their counters or tags, a status word) is a fixed
- * array inside the library, about 6 MB, held on every GPU that loads the library until the
+ * array inside the library, about 8 MB, held on every GPU that loads the library until the
  * process exits; its address is looked up on the first call on each device, so make that
  * first call before any stream capture.  Limits: at most 640 CTAs (the grid the kernel picks
  * for the device) and N <= 524288; beyond them the call returns QLIN_ERR_WORKSPACE.  Each call

@@ -179,11 +179,13 @@ __device__ __forceinline__ uint64_t ld_relaxed_b64(const uint64_t* p) {
   return v;
 }
 
-template <int NV>
+template <int NV, int MAXM = 1>  // MAXM: 1 (M == 1) or 4 (M <= 4) tokens
 struct OwnerFinisher {
-  uint64_t* tagged;  // [grid][2][64] words (copied from the workspace, see RowGroupFinisher)
+  static constexpr int kSlotWords = kRowGroup * 4;  // words per slot (room for four tokens)
+  static constexpr int PW = MAXM == 1 ? 1 : 2;      // words per work item
+  uint64_t* tagged;  // [grid][2][kSlotWords] words (copied from the workspace, see RowGroupFinisher)
   int32_t* status;
-  float* own;        // shared memory [64]: the owner's own partial sums
+  float* own;        // shared memory [64 * MAXM]: the owner's own partial sums
   uint32_t tag;
   int cta;
   int rg[2];         // shared row groups: [0] the first of the range, [1] the last (-1: none)
@@ -211,6 +213,12 @@ struct OwnerFinisher {
     }
   }
 
+  // word of entry idx = row * 16 + token
+  static __device__ __forceinline__ int word(int idx) { return (idx >> 4) * MAXM + (idx & 15); }
+  __device__ __forceinline__ uint64_t* slot(int c, int side) const {
+    return tagged + (int64_t)(c * 2 + side) * kSlotWords;
+  }
+
   template <typename Done>
   __device__ __forceinline__ void stage(int64_t r, const float (&vals)[NV], const int (&idx)[NV], Done done) {
     const int s = (r == rg[0]) ? 0 : (r == rg[1]) ? 1 : -1;
@@ -221,40 +229,53 @@ struct OwnerFinisher {
     if (s == owned) {
 #pragma unroll
       for (int i = 0; i < NV; ++i)
-        if (idx[i] >= 0) own[idx[i] >> 4] = vals[i];
+        if (idx[i] >= 0) own[word(idx[i])] = vals[i];
       pend = 1;
       return;
     }
-    uint64_t* slot = tagged + (int64_t)(cta * 2 + s) * kRowGroup;
+    uint64_t* sl = slot(cta, s);
     const uint64_t hi = (uint64_t)tag << 32;
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (idx[i] >= 0) st_relaxed_b64(slot + (idx[i] >> 4), hi | __float_as_uint(vals[i]));
+      if (idx[i] >= 0) st_relaxed_b64(sl + word(idx[i]), hi | __float_as_uint(vals[i]));
   }
 
-  // Only the owner works here; thread j < 64 finishes row j.  `put(rg, entry, value)`.
+  // Only the owner works here: work item j (thread j) is row j / (MAXM / PW), tokens
+  // PW * (j % (MAXM / PW)) onward.  `put(rg, entry, value)` stores one output.
   template <typename Put>
   __device__ __forceinline__ bool finish(int M, ConsumerSync& cs, int* flags, Put put) {
-    (void)M;
     (void)flags;
     if (!pend) return true;  // uniform over the consumer threads
     if (!cs.sync()) return false;
-    const int row = threadIdx.x;
-    if (row >= kRowGroup) return true;
-    float acc = own[row];
+    constexpr int IPR = MAXM / PW;  // items per row
+    const int item = threadIdx.x;
+    if (item >= kRowGroup * IPR) return true;
+    const int row = item / IPR, m0 = (item % IPR) * PW;
+    const int w0 = row * MAXM + m0;
+    float acc[PW];
+    bool need[PW];
+#pragma unroll
+    for (int j = 0; j < PW; ++j) {
+      need[j] = m0 + j < M;
+      acc[j] = own[w0 + j];
+    }
     constexpr int B = 8;  // contributors loaded per L2 round trip
     for (int c0 = 0; c0 < others; c0 += B) {
-      uint64_t v[B];
+      uint64_t v[B][PW];
 #pragma unroll
       for (int u = 0; u < B; ++u)
-        if (c0 + u < others) v[u] = ld_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row);
+        if (c0 + u < others)
+#pragma unroll
+          for (int j = 0; j < PW; ++j) v[u][j] = ld_relaxed_b64(slot(cta + 1 + c0 + u, 0) + w0 + j);
       // poll the whole batch: reload every word not yet tagged, one round trip per pass
       uint64_t t0 = 0;
       for (;;) {
         unsigned missing = 0;
 #pragma unroll
         for (int u = 0; u < B; ++u)
-          if (c0 + u < others && (uint32_t)(v[u] >> 32) != tag) missing |= 1u << u;
+#pragma unroll
+          for (int j = 0; j < PW; ++j)
+            if (c0 + u < others && need[j] && (uint32_t)(v[u][j] >> 32) != tag) missing |= 1u << u;
         if (!missing) break;
         if (t0 == 0) {
           t0 = global_ns();
@@ -264,16 +285,24 @@ struct OwnerFinisher {
         }
 #pragma unroll
         for (int u = 0; u < B; ++u)
-          if (missing & (1u << u)) v[u] = ld_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row);
+          if (missing & (1u << u))
+#pragma unroll
+            for (int j = 0; j < PW; ++j) v[u][j] = ld_relaxed_b64(slot(cta + 1 + c0 + u, 0) + w0 + j);
       }
 #pragma unroll
       for (int u = 0; u < B; ++u) {
         if (c0 + u >= others) continue;
-        acc += __uint_as_float((uint32_t)v[u]);
-        st_relaxed_b64(tagged + (int64_t)((cta + 1 + c0 + u) * 2) * kRowGroup + row, 0ull);
+#pragma unroll
+        for (int j = 0; j < PW; ++j) {
+          if (!need[j]) continue;
+          acc[j] += __uint_as_float((uint32_t)v[u][j]);
+          st_relaxed_b64(slot(cta + 1 + c0 + u, 0) + w0 + j, 0ull);
+        }
       }
     }
-    put((int64_t)rg[owned], row * 16, acc);
+#pragma unroll
+    for (int j = 0; j < PW; ++j)
+      if (need[j]) put((int64_t)rg[owned], row * 16 + m0 + j, acc[j]);
     return true;
   }
 };

@@ -43,7 +43,7 @@ struct SpSmem {
   __align__(16) uint32_t zeros[8];
   float rowacc[4][16][XR];
   float orow[4][16];  // M == 1: outlier sums per row of each tile
-  float own[kRowGroup];  // M == 1: this CTA's partial sums of the row group it owns
+  float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
   return __funnelshift_r(lo, hi, bit & 31) & 63u;
 }
 
-template <int MODE, int MT>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT
+template <int MODE, int MT, int OWN>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT; OWN: see below
 __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     spqr_decode_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
@@ -229,10 +229,10 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       if (n < vN) Y[(int64_t)m * vN + n] = f2bf(out[j]);
     }
   };
-  // one token: the owner-reduces completion (no atomics); more tokens: counted arrivals
+  // up to OWN (1 or 4) tokens: the owner-reduces completion (no atomics); otherwise counted
   auto fin = [&] {
-    if constexpr (MODE == 1)
-      return OwnerFinisher<NV>(S, U, grid, cta, ws.tagged, ws.tag, ws.status, sm.own);
+    if constexpr (OWN > 0)
+      return OwnerFinisher<NV, OWN>(S, U, grid, cta, ws.tagged, ws.tag, ws.status, sm.own);
     else
       return RowGroupFinisher<float, NV>(S, U, grid, cta, ws.partials, ws.counters);
   }();
@@ -503,14 +503,14 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   }
 }
 
-template <int MODE, int MT>
+template <int MODE, int MT, int OWN>
 int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                   void* stream) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
   const size_t smem = sizeof(SpSmem<XR>);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(spqr_decode_kernel<MODE, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(spqr_decode_kernel<MODE, MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
@@ -525,7 +525,7 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT>, v, X, Y, M, ws);
+  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT, OWN>, v, X, Y, M, ws);
 }
 
 }  // namespace
@@ -545,9 +545,10 @@ int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M,
                        void* stream) {
   grid = spqr_decode_grid(v, M, ws.sms);
   if (grid > ws.grid) return (int)cudaErrorInvalidValue;
-  if (M == 1) return launch_spqr_t<1, 1>(v, X, Y, M, ws, grid, stream);
-  if (M <= 8) return launch_spqr_t<2, 1>(v, X, Y, M, ws, grid, stream);
-  return launch_spqr_t<2, 2>(v, X, Y, M, ws, grid, stream);
+  if (M == 1) return launch_spqr_t<1, 1, 1>(v, X, Y, M, ws, grid, stream);
+  if (M <= 4) return launch_spqr_t<2, 1, 4>(v, X, Y, M, ws, grid, stream);
+  if (M <= 8) return launch_spqr_t<2, 1, 0>(v, X, Y, M, ws, grid, stream);
+  return launch_spqr_t<2, 2, 0>(v, X, Y, M, ws, grid, stream);
 }
 
 }  // namespace qlin

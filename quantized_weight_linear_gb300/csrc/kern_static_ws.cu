@@ -11,7 +11,7 @@
 //
 // Limits of the fixed array: at most kStaticMaxGrid CTAs (4 per SM on up to 160 SMs) and
 // kStaticMaxRowGroups row groups of 64 output rows (N <= 524288); larger requests return
-// QLIN_ERR_WORKSPACE.  Every GPU that loads the library holds the array (about 6 MB) until
+// QLIN_ERR_WORKSPACE.  Every GPU that loads the library holds the array (about 8 MB) until
 // the process exits.
 #include <mutex>
 
@@ -26,7 +26,7 @@ constexpr int kStaticMaxRowGroups = 8192;
 constexpr size_t kStaticPartialsOff = 256;
 constexpr size_t kStaticCountersOff = kStaticPartialsOff + (size_t)kStaticMaxGrid * 2 * kRowGroup * 16 * 4;
 constexpr size_t kStaticTaggedOff = kStaticCountersOff + (size_t)kStaticMaxRowGroups * 4;
-constexpr size_t kStaticScratchBytes = kStaticTaggedOff + (size_t)kStaticMaxGrid * 2 * kRowGroup * 8;
+constexpr size_t kStaticScratchBytes = kStaticTaggedOff + (size_t)kStaticMaxGrid * 2 * kRowGroup * 4 * 8;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_spqr_static_scratch[kStaticScratchBytes];

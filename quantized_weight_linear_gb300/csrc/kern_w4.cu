@@ -12,9 +12,9 @@
 //   with one AND/OR per register pair (bf16 128 + q) and one bf16 subtract of 128 + z,
 //   which leaves the exact integers q - z; mma.sync m16n8k16 accumulates sum (q - z) x in
 //   fp32 per group, and the group's fp16 scale is applied once per group;
-// * a row group split between CTAs is finished deterministically: with one token by the
-//   CTA that owns it (tagged partial words, no atomics), otherwise by the last CTA to arrive
-//   (partials in the workspace, arrival counter).
+// * a row group split between CTAs is finished deterministically: with up to four tokens by
+//   the CTA that owns it (tagged partial words, no atomics), otherwise by the last CTA to
+//   arrive (partials in the workspace, arrival counter).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
@@ -31,10 +31,10 @@ struct W4Smem {
   uint64_t empty[kStagesW4];
   uint64_t cons_bar;
   int flags[2];
-  float own[kRowGroup];  // one token: this CTA's partial sums of the row group it owns
+  float own[kRowGroup * 4];  // up to 4 tokens: this CTA's partial sums of the row group it owns
 };
 
-template <int MT, bool ONE>  // ONE: M == 1 (owner-reduces split completion)
+template <int MT, int OWN>  // OWN: 1 or 4 (M <= OWN, owner-reduces split completion), 0 counted
 __global__ void __launch_bounds__(160, 4)
     w4_decode_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(160, 4)
     }
   };
   auto fin = [&] {
-    if constexpr (ONE)
-      return OwnerFinisher<MT * 4>(G, U, grid, cta, ws.tagged, ws.tag, ws.status, sm.own);
+    if constexpr (OWN > 0)
+      return OwnerFinisher<MT * 4, OWN>(G, U, grid, cta, ws.tagged, ws.tag, ws.status, sm.own);
     else
       return RowGroupFinisher<float, MT * 4, MT == 1 ? 16 : 8>(G, U, grid, cta, ws.partials, ws.counters);
   }();
@@ -206,13 +206,13 @@ __global__ void __launch_bounds__(160, 4)
   }
 }
 
-template <int MT, bool ONE>
+template <int MT, int OWN>
 int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                  void* stream) {
   const size_t smem = sizeof(W4Smem<MT>);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4_decode_kernel<MT, ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(w4_decode_kernel<MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
@@ -226,7 +226,7 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT, ONE>, v, X, Y, M, ws);
+  return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT, OWN>, v, X, Y, M, ws);
 }
 
 }  // namespace
@@ -234,9 +234,10 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
   grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms);
-  if (M == 1) return launch_w4_mt<1, true>(v, X, Y, M, ws, grid, stream);
-  if (M <= 8) return launch_w4_mt<1, false>(v, X, Y, M, ws, grid, stream);
-  return launch_w4_mt<2, false>(v, X, Y, M, ws, grid, stream);
+  if (M == 1) return launch_w4_mt<1, 1>(v, X, Y, M, ws, grid, stream);
+  if (M <= 4) return launch_w4_mt<1, 4>(v, X, Y, M, ws, grid, stream);
+  if (M <= 8) return launch_w4_mt<1, 0>(v, X, Y, M, ws, grid, stream);
+  return launch_w4_mt<2, 0>(v, X, Y, M, ws, grid, stream);
 }
 
 }  // namespace qlin

@@ -747,7 +747,7 @@ static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   w.partials = 256;
   w.counters = w.partials + align256((size_t)grid * 2 * kRowGroup * 16 * 4);
   w.tagged = w.counters + align256((size_t)L->RG * 4);
-  w.qx = w.tagged + align256((size_t)grid * 2 * kRowGroup * 8);
+  w.qx = w.tagged + align256((size_t)grid * 2 * kRowGroup * 4 * 8);
   size_t qx_bytes = 0, sx_bytes = 0;
   if (L->format == QLIN_FMT_W8A8) {
     qx_bytes = align256((size_t)std::max(maxM, 1) * L->K * 2);

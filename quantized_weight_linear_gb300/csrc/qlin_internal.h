@@ -88,7 +88,7 @@ struct Workspace {
   int32_t* status;     // device status word
   float* partials;     // [grid][2][64 * 16] split-row partial sums
   uint32_t* counters;  // [RG] arrival counters of split row groups
-  uint64_t* tagged;    // [grid][2][64] one-token partial sums as 8-byte words (value, tag)
+  uint64_t* tagged;    // [grid][2][64 * 4] partial sums of up to 4 tokens as 8-byte words (value, tag)
   uint32_t tag;        // nonzero tag of this workspace's valid words in `tagged`
   void* qx;            // W8A8: fp16 activation codes [maxM][K]
   float* sx;           // W8A8: [maxM]
