@@ -23,11 +23,19 @@ namespace {
 constexpr int kStagesW8 = 4;
 constexpr int kXStrideW8 = 72;  // staged qx row: 64 fp16 + 8 pad
 
+// Where the fp16 code of (token m, channel k) goes.  blk == 0: row-major [M][K] (the prefill
+// GEMM's TMA map).  blk == M: blocked for the decode GEMV, [K/64][M][kXStrideW8], so that one
+// bulk copy moves a 64-wide K block of every token into the staged layout (pad not written).
+__device__ __forceinline__ int64_t q16_offset(int m, int k, int K, int blk) {
+  if (blk == 0) return (int64_t)m * K + k;
+  return ((int64_t)(k >> 6) * blk + m) * kXStrideW8 + (k & 63);
+}
+
 template <bool F16OUT>
 __global__ void __launch_bounds__(256)
     w8_act_quant_kernel(const uint16_t* __restrict__ X, const float* __restrict__ s_inv, int K,
                         int8_t* __restrict__ q8, uint16_t* __restrict__ q16, float* __restrict__ sx,
-                        int32_t* __restrict__ kbound) {
+                        int32_t* __restrict__ kbound, int blk) {
   __shared__ float red[8];
   __shared__ float scale_sh;
   pdl_wait();
@@ -87,7 +95,7 @@ __global__ void __launch_bounds__(256)
         const __half2 h = __halves2half2(__int2half_rn(qv[2 * e]), __int2half_rn(qv[2 * e + 1]));
         o[e] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      *reinterpret_cast<uint4*>(q16 + (int64_t)m * K + k) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(q16 + q16_offset(m, k, K, blk)) = make_uint4(o[0], o[1], o[2], o[3]);
     } else {
       uint32_t lo = 0, hi = 0;
 #pragma unroll
@@ -96,6 +104,96 @@ __global__ void __launch_bounds__(256)
         hi |= (uint32_t)(uint8_t)(int8_t)qv[4 + e] << (8 * e);
       }
       *reinterpret_cast<uint2*>(q8 + (int64_t)m * K + k) = make_uint2(lo, hi);
+    }
+  }
+}
+
+// The same quantization in a single read: one CTA of kAqThreads threads per token, each
+// thread holding R chunks of 8 scaled activations x' in registers between the row maximum and
+// the rounding (rows up to kAqThreads * 8 * R wide).  The arithmetic is the two-pass kernel's,
+// operation for operation, so the codes and scales are the same bits.
+constexpr int kAqThreads = 512;
+
+template <bool F16OUT, int R>
+__global__ void __launch_bounds__(kAqThreads)
+    w8_act_quant_reg_kernel(const uint16_t* __restrict__ X, const float* __restrict__ s_inv, int K,
+                            int8_t* __restrict__ q8, uint16_t* __restrict__ q16, float* __restrict__ sx,
+                            int32_t* __restrict__ kbound, int blk) {
+  __shared__ float red[kAqThreads / 32];
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int m = blockIdx.x, lane = threadIdx.x & 31;
+  const uint16_t* xr = X + (int64_t)m * K;
+  const int nc = K >> 3;  // chunks of 8
+  float xs[R][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int c = threadIdx.x + i * kAqThreads;
+    if (c < nc) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xr + 8 * c);
+      const float4 s0 = *reinterpret_cast<const float4*>(s_inv + 8 * c);
+      const float4 s1 = *reinterpret_cast<const float4*>(s_inv + 8 * c + 4);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
+        xs[i][e] = __fmul_rn(x, sv[e]);
+        amax = fmaxf(amax, fabsf(xs[i][e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xs[i][e] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  float a = red[0];
+#pragma unroll
+  for (int i = 1; i < kAqThreads / 32; ++i) a = fmaxf(a, red[i]);
+  const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 127.f);
+  if (threadIdx.x == 0) sx[m] = sc;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int c = threadIdx.x + i * kAqThreads;
+    const bool valid = c < nc;
+    int qv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int q = valid ? __float2int_rn(__fdiv_rn(xs[i][e], sc)) : 0;
+      qv[e] = q < -127 ? -127 : (q > 127 ? 127 : q);
+    }
+    if (kbound) {
+      // sum |q| over a 64-wide k-block: 8 consecutive chunks are 8 consecutive lanes, all valid
+      // or all past the row (K is a multiple of 64)
+      int l1 = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) l1 += qv[e] < 0 ? -qv[e] : qv[e];
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+      if (valid && (lane & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + c / 8, l1);
+    }
+    if (!valid) continue;
+    if constexpr (F16OUT) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 h = __halves2half2(__int2half_rn(qv[2 * e]), __int2half_rn(qv[2 * e + 1]));
+        o[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(q16 + q16_offset(m, 8 * c, K, blk)) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo |= (uint32_t)(uint8_t)(int8_t)qv[e] << (8 * e);
+        hi |= (uint32_t)(uint8_t)(int8_t)qv[4 + e] << (8 * e);
+      }
+      *reinterpret_cast<uint2*>(q8 + (int64_t)m * K + 8 * c) = make_uint2(lo, hi);
     }
   }
 }
@@ -146,12 +244,12 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
 
   if (warp == 4) {
     if (lane != 0) return;
-    const uint32_t xbytes = kW8Block * 2;
-    const uint32_t tx = kW8UnitBytes + (uint32_t)M * xbytes;
+    // the codes are blocked [K/64][M][kXStrideW8]: a unit's X slice is one contiguous copy
+    const uint32_t xbytes = (uint32_t)M * kXStrideW8 * 2;
+    const uint32_t tx = kW8UnitBytes + xbytes;
     int kx = (int)(u0 % KB);  // K block of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
-      const int64_t k0 = (int64_t)kx * kW8Block;
-      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], q16 + (int64_t)m * v.K + k0, xbytes, &sm.full[s]);
+      bulk_g2s(&sm.x[s][0][0], q16 + (int64_t)kx * M * kXStrideW8, xbytes, &sm.full[s]);
       if (++kx == (int)KB) kx = 0;
     };
     const int pro = n_units < kStagesW8 ? n_units : kStagesW8;
@@ -314,10 +412,10 @@ int launch_w8_mt(const W8View& v, const uint16_t* q16, const float* sx, uint16_t
 
 template <bool F16>
 int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, float* sx, int32_t* kbound, int M,
-              void* stream) {
+              int blk, void* stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kAqThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
@@ -325,18 +423,28 @@ int launch_aq(const W8View& v, const uint16_t* X, int8_t* q8, uint16_t* q16, flo
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx, kbound);
+  const int chunks = v.K / 8;
+  if (chunks <= kAqThreads)
+    return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_reg_kernel<F16, 1>, X, v.s_inv, v.K, q8, q16, sx, kbound, blk);
+  if (chunks <= 2 * kAqThreads)
+    return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_reg_kernel<F16, 2>, X, v.s_inv, v.K, q8, q16, sx, kbound, blk);
+  if (chunks <= 4 * kAqThreads)
+    return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_reg_kernel<F16, 4>, X, v.s_inv, v.K, q8, q16, sx, kbound, blk);
+  if (chunks <= 8 * kAqThreads)
+    return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_reg_kernel<F16, 8>, X, v.s_inv, v.K, q8, q16, sx, kbound, blk);
+  cfg.blockDim = dim3(256);  // wider rows: the two-pass kernel
+  return (int)cudaLaunchKernelEx(&cfg, w8_act_quant_kernel<F16>, X, v.s_inv, v.K, q8, q16, sx, kbound, blk);
 }
 
 }  // namespace
 
 int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M, void* stream) {
-  return launch_aq<false>(v, X, qx, nullptr, sx, nullptr, M, stream);
+  return launch_aq<false>(v, X, qx, nullptr, sx, nullptr, M, 0, stream);
 }
 
 int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int32_t* kbound, int M,
-                            void* stream) {
-  return launch_aq<true>(v, X, nullptr, q16, sx, kbound, M, stream);
+                            bool blocked, void* stream) {
+  return launch_aq<true>(v, X, nullptr, q16, sx, kbound, M, blocked ? M : 0, stream);
 }
 
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc_out, int M,

@@ -750,7 +750,9 @@ static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   w.qx = w.tagged + align256((size_t)grid * 2 * kRowGroup * 4 * 8);
   size_t qx_bytes = 0, sx_bytes = 0;
   if (L->format == QLIN_FMT_W8A8) {
-    qx_bytes = align256((size_t)std::max(maxM, 1) * L->K * 2);
+    // row-major codes for the prefill GEMM, or the decode GEMV's blocked [K/64][M][72] (M <= 16)
+    qx_bytes = align256(std::max((size_t)std::max(maxM, 1) * L->K * 2,
+                                 (size_t)(L->K / 64) * std::min(std::max(maxM, 1), 16) * 72 * 2));
     sx_bytes = align256((size_t)std::max(maxM, 1) * 4);
   }
   w.sx = w.qx + qx_bytes;
@@ -942,7 +944,7 @@ static qlin_status run_decode(qlin_handle h, const uint16_t* X, uint16_t* Y, int
       break;
     case QLIN_FMT_W8A8: {
       uint16_t* q16 = reinterpret_cast<uint16_t*>(h->wsv.qx);
-      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, nullptr, M, s);
+      e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, nullptr, M, true, s);
       if (!e) e = launch_w8_decode(w8view(h), q16, h->wsv.sx, Y, acc, M, h->wsv, h->grid, s);
       break;
     }
@@ -967,7 +969,7 @@ static qlin_status run_prefill(qlin_handle h, const uint16_t* X, uint16_t* Y, in
       // per-tile bounds of sum |qx| per k-block, gathered by the act-quant kernel with atomicMax
       const size_t kb_bytes = (size_t)((M + 255) / 256) * (h->K / 64) * 4;
       e = (int)cudaMemsetAsync(h->wsv.kbound, 0, kb_bytes, s);
-      if (!e) e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, h->wsv.kbound, M, s);
+      if (!e) e = launch_w8_act_quant_f16(w8view(h), X, q16, h->wsv.sx, h->wsv.kbound, M, false, s);
       if (!e) e = launch_w8_prefill(w8view(h), q16, h->wsv.sx, h->wsv.kbound, Y, acc, M, h->wsv.status, s);
       break;
     }

@@ -107,8 +107,9 @@ int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M,
                        const Workspace& ws, int grid, void* stream);
 int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M,
                         void* stream);
+// blocked: codes laid out [K/64][M][72] for the decode GEMV (M <= 16) instead of [M][K]
 int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, float* sx, int32_t* kbound, int M,
-                            void* stream);
+                            bool blocked, void* stream);
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y,
                      int32_t* acc_out, int M, const Workspace& ws, int grid, void* stream);
 int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream);
