@@ -9,6 +9,8 @@
 //   the previous kernel on the stream drains, and waits (griddepcontrol.wait) before it
 //   touches activations, outputs or workspace.
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -23,6 +25,49 @@ namespace qlin {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 2D tiled TMA load of box (x, y) of `map` into shared memory (128-byte aligned destination),
+// completing on `bar`'s transaction count
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The driver's tensor-map encoder (looked up once through the runtime)
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Map of the decode kernels' activations X [M][K] bf16 (row-major): boxes of box_k channels of
+// all M tokens, unswizzled, so one copy lands as M rows of box_k elements.  Channels past K
+// read as zero.  Returns false if the encoder is missing or refuses the shape.
+inline bool encode_decode_x_map(CUtensorMap* map, const void* X, int64_t K, int M, int box_k) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)M};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Dynamic shared memory rounded up to a 128-byte boundary (the launch adds 128 bytes)
+__device__ __forceinline__ uint8_t* smem_align128(uint8_t* raw) {
+  return raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

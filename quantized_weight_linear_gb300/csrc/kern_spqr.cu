@@ -8,7 +8,8 @@
 // * same persistent weight stream as the W4 kernel: up to four CTAs per SM, equal contiguous
 //   ranges of (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group
 //   statistics and fp16 supergroup statistics), a producer warp with cp.async.bulk into a
-//   3-deep ring per CTA, the unit's outlier bucket and X slice staged alongside;
+//   3-deep ring per CTA, the unit's outlier bucket and X slice staged alongside (with two or
+//   more tokens the slice is two 2D tensor copies of all M rows, not one copy per token);
 // * code words hold five 3-bit fields per 16-bit half; one AND/OR turns a field pair into
 //   bf16 (base + q) with base 128 or 16 depending on the field, no shifts for 2 of 5;
 // * M == 1: the eight MMA columns carry eight different 16-groups (block-diagonal B), so
@@ -30,14 +31,16 @@ namespace qlin {
 namespace {
 
 constexpr int kStagesSp = 3;
-constexpr int kXStrideSp = 264;    // 256 bf16 + 8 pad
+constexpr int kXStrideSp = 264;    // M == 1: staged X row, 256 bf16 + 8 pad
+constexpr int kXHalfSp = 136;      // M >= 2: each 128-wide half of the slice as [XR][128 + 8 pad]
 constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
 constexpr int kOffsCap = 1024 + 16;  // offsets staged per CTA
 
 template <int XR>  // staged X rows (1 for the M == 1 kernel, 8 or 16 otherwise)
 struct SpSmem {
-  __align__(16) uint8_t unit[kStagesSp][kSpqrUnitBytes];
-  __align__(16) uint16_t x[kStagesSp][XR][kXStrideSp];
+  static constexpr int kXE = XR == 1 ? kXStrideSp : 2 * XR * kXHalfSp;  // X elements per stage
+  __align__(128) uint8_t unit[kStagesSp][kSpqrUnitBytes];
+  __align__(128) uint16_t x[kStagesSp][kXE];
   __align__(16) uint32_t out[kStagesSp][kOutCap + 8];
   __align__(16) uint32_t offs[kOffsCap];
   __align__(16) uint32_t zeros[8];
@@ -98,15 +101,16 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
 
 template <int MODE, int MT, int OWN>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT; OWN: see below
 __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
-    spqr_decode_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
+    spqr_decode_kernel(const __grid_constant__ CUtensorMap xmap, SpqrView v, const uint16_t* __restrict__ X,
+                       uint16_t* __restrict__ Y, int M, Workspace ws) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  SpSmem<XR>& sm = *reinterpret_cast<SpSmem<XR>*>(smem_raw);
+  SpSmem<XR>& sm = *reinterpret_cast<SpSmem<XR>*>(smem_align128(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t grid = gridDim.x, cta = blockIdx.x;
   // scalars of the view as locals: lambdas capture them, and capturing the kernel parameter
   // itself would move it to local memory
-  const int64_t vN = v.N, vK = v.K;
+  const int64_t vN = v.N;
   const int64_t S = v.S, U = (int64_t)v.RG * S;
   const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
   const int n_units = (int)(u1 - u0);
@@ -126,8 +130,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     pdl_launch_dependents();
   }
   {
-    uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0][0]);
-    for (int i = threadIdx.x; i < kStagesSp * XR * kXStrideSp / 2; i += blockDim.x) xz[i] = 0u;
+    uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0]);
+    for (int i = threadIdx.x; i < kStagesSp * SpSmem<XR>::kXE / 2; i += blockDim.x) xz[i] = 0u;
     if (threadIdx.x < 8) sm.zeros[threadIdx.x] = 0u;
   }
   fence_proxy_async_smem();
@@ -155,16 +159,23 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       if (e1 - e0 <= (uint32_t)kOutCap && e1 > e0) return (((e1 + 3u) & ~3u) - (e0 & ~3u)) * 4;
       return 0u;
     };
-    const int xm = MODE == 1 ? 1 : M;
+    // M == 1: one plain copy of the 256-wide slice; otherwise two boxes of xmap ([M][136] at
+    // k0 and k0 + 128), one per half of the staged layout
+    const uint32_t xtx = MODE == 1 ? xbytes : 2u * (uint32_t)M * kXHalfSp * 2;
     int kx = (int)(u0 % S);  // supergroup of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
-      const int64_t k0 = (int64_t)kx * kSpqrSuper;
+      const int k0 = kx * kSpqrSuper;
       if (++kx == (int)S) kx = 0;
-      for (int m = 0; m < xm; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * vK + k0, xbytes, &sm.full[s]);
+      if constexpr (MODE == 1) {
+        bulk_g2s(&sm.x[s][0], X + k0, xbytes, &sm.full[s]);
+      } else {
+        tma_load_2d(&sm.x[s][0], &xmap, k0, 0, &sm.full[s]);
+        tma_load_2d(&sm.x[s][XR * kXHalfSp], &xmap, k0 + 128, 0, &sm.full[s]);
+      }
     };
     const int pro = n_units < kStagesSp ? n_units : kStagesSp;
     for (int i = 0; i < pro; ++i) {
-      mbar_arrive_expect_tx(&sm.full[i], kSpqrUnitBytes + out_bytes(u0 + i) + (uint32_t)xm * xbytes);
+      mbar_arrive_expect_tx(&sm.full[i], kSpqrUnitBytes + out_bytes(u0 + i) + xtx);
       weights(i, u0 + i);
     }
     pdl_wait();
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       const int s = i % kStagesSp;
       const uint32_t ph = (uint32_t)(i / kStagesSp) & 1u;
       if (!mbar_wait(&sm.empty[s], ph ^ 1u, ws.status)) return;
-      mbar_arrive_expect_tx(&sm.full[s], kSpqrUnitBytes + out_bytes(u0 + i) + (uint32_t)xm * xbytes);
+      mbar_arrive_expect_tx(&sm.full[s], kSpqrUnitBytes + out_bytes(u0 + i) + xtx);
       weights(s, u0 + i);
       load_x(s);
     }
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
 
     if constexpr (MODE == 1) {
       // per-group X sums of the unit: lane l covers group l/2, half l%2
-      const uint16_t* x0 = &sm.x[s][0][0];
+      const uint16_t* x0 = &sm.x[s][0];
       float sa = 0.f, sb = 0.f;
       {
         const int gl = lane >> 1, h = lane & 1;
@@ -406,7 +417,6 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
           const float cz = -sh * zh;
           ch2[r] = pack_bf16x2(cz, cz);
         }
-        const int kb = blk * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t a[4];
@@ -425,9 +435,9 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
           for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            const uint16_t* xr = &sm.x[s][g + 8 * mt][0];
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + kb + 16 * t + 2 * j);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + kb + 16 * (t + 4) + 2 * j);
+            const uint16_t* xr = &sm.x[s][(blk * XR + g + 8 * mt) * kXHalfSp];
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + 16 * t + 2 * j);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 16 * (t + 4) + 2 * j);
             mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
           }
         }
@@ -457,7 +467,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
           const bool valid = i < n;
           const uint32_t e = valid ? ent(i) : 0u;
           const int r = valid ? (int)(e & 15u) : 16;
-          float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][0][(e >> 4) & 255u]) : 0.f;
+          float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]) : 0.f;
           // runs from head flags: lane l's run starts at the last head at or below l
           const int rprev = __shfl_up_sync(0xffffffffu, r, 1);
           const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || rprev != r);
@@ -487,7 +497,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
         const float val = h2f_dev((uint16_t)(e >> 16));
 #pragma unroll
         for (int j = 0; j < OT; ++j)
-          if (otok0 + j < (MODE == 1 ? 1 : M)) oacc[j] += val * bf2f(sm.x[s][otok0 + j][k]);
+          if (otok0 + j < (MODE == 1 ? 1 : M))
+            oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
       }
       }
     }
@@ -503,11 +514,17 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   }
 }
 
+static_assert(offsetof(SpSmem<8>, x) % 128 == 0 && offsetof(SpSmem<16>, x) % 128 == 0 &&
+                  (SpSmem<8>::kXE * 2) % 128 == 0 && (SpSmem<16>::kXE * 2) % 128 == 0 && (8 * kXHalfSp * 2) % 128 == 0,
+              "TMA destinations");
+
 template <int MODE, int MT, int OWN>
 int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                   void* stream) {
   constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
-  const size_t smem = sizeof(SpSmem<XR>);
+  CUtensorMap xmap{};
+  if (MODE == 2 && !encode_decode_x_map(&xmap, X, v.K, M, kXHalfSp)) return (int)cudaErrorInvalidValue;
+  const size_t smem = sizeof(SpSmem<XR>) + 128;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(spqr_decode_kernel<MODE, MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -525,7 +542,7 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT, OWN>, v, X, Y, M, ws);
+  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT, OWN>, xmap, v, X, Y, M, ws);
 }
 
 }  // namespace

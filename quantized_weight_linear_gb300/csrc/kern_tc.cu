@@ -23,9 +23,6 @@
 //   partial sums kept in the other half of TMEM (columns 256..511), release the accumulator
 //   to the next chunk, and after the last one write y = bf16((acc * sx) * sw) (or acc).
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "kern_common.cuh"
 
 namespace qlin {
@@ -157,14 +154,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
 }
 
 // byte offset of element (row, k) in a 128 x 64 K-major tile with 128-byte swizzle
@@ -705,18 +694,6 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 template <int F>
 int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
   using C = TcCfg<F>;
@@ -724,7 +701,7 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
   if constexpr (F == kSpqr) {
     if (4 * (int64_t)args.KU + 8 > kOffsCapTc) return (int)cudaErrorInvalidValue;  // K > 65536: not staged
   }
-  auto enc = get_encode();
+  auto enc = tensor_map_encoder();
   if (!enc) return (int)cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.M};

@@ -7,7 +7,8 @@
 // * persistent grid of up to four CTAs per SM, each owning an equal, contiguous range of
 //   (64-row group, 128-wide K group) units (4352 bytes of codes + statistics each);
 // * one producer warp streams units with cp.async.bulk into a 4-deep shared-memory
-//   ring (mbarrier full/empty pairs) together with the matching 128-wide slice of X;
+//   ring (mbarrier full/empty pairs) together with the matching 128-wide slice of X (with
+//   two or more tokens one 2D tensor copy of all M rows, not one copy per token);
 // * four consumer warps (one 16-row tile each) turn code words into bf16 A fragments
 //   with one AND/OR per register pair (bf16 128 + q) and one bf16 subtract of 128 + z,
 //   which leaves the exact integers q - z; mma.sync m16n8k16 accumulates sum (q - z) x in
@@ -25,8 +26,8 @@ constexpr int kXStrideW4 = 136;  // staged X row: 128 bf16 + 8 pad (bank-conflic
 
 template <int MT>
 struct W4Smem {
-  __align__(16) uint8_t unit[kStagesW4][kW4UnitBytes];
-  __align__(16) uint16_t x[kStagesW4][8 * MT][kXStrideW4];
+  __align__(128) uint8_t unit[kStagesW4][kW4UnitBytes];
+  __align__(128) uint16_t x[kStagesW4][8 * MT][kXStrideW4];  // stage stride 2176 * MT bytes
   uint64_t full[kStagesW4];
   uint64_t empty[kStagesW4];
   uint64_t cons_bar;
@@ -36,14 +37,17 @@ struct W4Smem {
 
 template <int MT, int OWN>  // OWN: 1 or 4 (M <= OWN, owner-reduces split completion), 0 counted
 __global__ void __launch_bounds__(160, 4)
-    w4_decode_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, int M, Workspace ws) {
+    w4_decode_kernel(const __grid_constant__ CUtensorMap xmap, W4View v, const uint16_t* __restrict__ X,
+                     uint16_t* __restrict__ Y, int M, Workspace ws) {
+  // M == 1: the X slice is one plain bulk copy; otherwise one box of xmap ([M][136] at k0)
+  constexpr bool kTmaX = !(MT == 1 && OWN == 1);
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_raw);
+  W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_align128(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t grid = gridDim.x, cta = blockIdx.x;
   // scalars of the view as locals: lambdas capture them, and capturing the kernel parameter
   // itself would move it to local memory
-  const int64_t vN = v.N, vK = v.K;
+  const int64_t vN = v.N;
   const int64_t G = v.G, U = (int64_t)v.RG * G;
   const int64_t u0 = split_start(cta, U, grid), u1 = split_start(cta + 1, U, grid);
   const int n_units = (int)(u1 - u0);
@@ -66,12 +70,15 @@ __global__ void __launch_bounds__(160, 4)
 
   if (warp == 4) {
     if (lane != 0) return;
-    const uint32_t xbytes = kW4Group * 2;
-    const uint32_t tx = kW4UnitBytes + (uint32_t)M * xbytes;
+    const uint32_t xbytes = kTmaX ? (uint32_t)M * kXStrideW4 * 2 : kW4Group * 2;
+    const uint32_t tx = kW4UnitBytes + xbytes;
     int kx = (int)(u0 % G);  // K group of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
-      const int64_t k0 = (int64_t)kx * kW4Group;
-      for (int m = 0; m < M; ++m) bulk_g2s(&sm.x[s][m][0], X + (int64_t)m * vK + k0, xbytes, &sm.full[s]);
+      const int k0 = kx * kW4Group;
+      if constexpr (kTmaX)
+        tma_load_2d(&sm.x[s][0][0], &xmap, k0, 0, &sm.full[s]);
+      else
+        bulk_g2s(&sm.x[s][0][0], X + k0, xbytes, &sm.full[s]);
       if (++kx == (int)G) kx = 0;
     };
     const int pro = n_units < kStagesW4 ? n_units : kStagesW4;
@@ -206,10 +213,14 @@ __global__ void __launch_bounds__(160, 4)
   }
 }
 
+static_assert(offsetof(W4Smem<1>, x) % 128 == 0 && offsetof(W4Smem<2>, x) % 128 == 0, "TMA destination");
+
 template <int MT, int OWN>
 int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                  void* stream) {
-  const size_t smem = sizeof(W4Smem<MT>);
+  CUtensorMap xmap{};
+  if (!(MT == 1 && OWN == 1) && !encode_decode_x_map(&xmap, X, v.K, M, kXStrideW4)) return (int)cudaErrorInvalidValue;
+  const size_t smem = sizeof(W4Smem<MT>) + 128;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(w4_decode_kernel<MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -226,7 +237,7 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT, OWN>, v, X, Y, M, ws);
+  return (int)cudaLaunchKernelEx(&cfg, w4_decode_kernel<MT, OWN>, xmap, v, X, Y, M, ws);
 }
 
 }  // namespace
