@@ -20,11 +20,15 @@
 // * M >= 2: the same A pairs are dequantized to bf16 s^ (q - z^) in registers and the
 //   MMA columns carry the tokens;
 // * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
-//   fp16 value; sorted by row, then k, so every row's outliers form one run).  M == 1: a
-//   segmented warp sum over the runs of 32 entries at a time; M >= 2: lane L owns row L % 16,
-//   finds its run by bisection and accumulates value * x[k] in registers.  Either way no two
-//   lanes ever add into the same sum (no atomics; the page's warning about the sparse part
-//   is about exactly this scattered accumulation).
+//   fp16 value; sorted by quad (row & 7), then row, then k).  M == 1: lane (g, t) of the
+//   MMA layout already owns the sums of rows g and g + 8, which are exactly quad g's run;
+//   the run's bounds come from the quad counts in the bucket's first entries, the quad's
+//   four lanes take every fourth entry into two registers, and the accumulator reduction
+//   over the quad adds them in (buckets too small or too crowded for the counts: a
+//   segmented warp sum over the row runs).  M >= 2: lane L owns row L % 16, finds its run by
+//   bisection and accumulates value * x[k] in registers.  Either way no two lanes ever add
+//   into the same sum (no atomics; the page's warning about the sparse part is about exactly
+//   this scattered accumulation).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   float oacc[OT];
 #pragma unroll
   for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
+  float oa = 0.f, ob = 0.f;  // M == 1: outlier sums of rows g and g + 8 (this lane's share)
   if (lane < 16) sm.orow[rt][lane] = 0.f;
   __syncwarp();
   int64_t cur_rg = u0 / S;
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     __syncwarp();
     float vals[NV];
     if constexpr (MODE == 1) {
-      float r0 = acc[0] + acc[1], r1 = acc[2] + acc[3];
+      float r0 = (acc[0] + acc[1]) + oa, r1 = (acc[2] + acc[3]) + ob;
       r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
       r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
       r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
@@ -295,6 +300,8 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
+      oa = 0.f;
+      ob = 0.f;
       __syncwarp();
       if (lane < 16) sm.orow[rt][lane] = 0.f;
       __syncwarp();
@@ -457,49 +464,98 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
       const uint32_t* bs = sm.out[s] + (b0 - (e0 & ~3u));  // staged bucket
       const uint32_t* bg = v.ents + b0;                     // the same bucket in global memory
-      auto ent = [&](int i) -> uint32_t { return staged ? bs[i] : __ldg(bg + i); };
       const int n = (int)(b1 - b0);
+      // Every walk below is instantiated once per source (staged copy, global memory) behind
+      // a warp-uniform branch: a select between the two would issue the global load as well.
+      auto from_smem = [bs](int i) -> uint32_t { return bs[i]; };
+      auto from_gmem = [bg](int i) -> uint32_t { return __ldg(bg + i); };
       if constexpr (MODE == 1) {
-        // chunks of 32 entries: segmented sum over each row's run (runs are contiguous), and
-        // the last lane of a run adds it to the row's sum
-        for (int c0 = 0; c0 < n; c0 += 32) {
-          const int i = c0 + lane;
-          const bool valid = i < n;
-          const uint32_t e = valid ? ent(i) : 0u;
-          const int r = valid ? (int)(e & 15u) : 16;
-          float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]) : 0.f;
-          // runs from head flags: lane l's run starts at the last head at or below l
-          const int rprev = __shfl_up_sync(0xffffffffu, r, 1);
-          const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || rprev != r);
-          const int start = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const float vu = __shfl_up_sync(0xffffffffu, vsum, d);
-            if (lane - d >= start) vsum += vu;
+        // quad counts: bits 12..15 of the bucket's first eight entries (n >= 8, no escape)
+        uint32_t qc = 0u;
+        if (n >= 8) {
+          if (staged) {
+            if (lane < 8) qc = (bs[lane] >> 12) & 15u;
+          } else {
+            if (lane < 8) qc = (__ldg(bg + lane) >> 12) & 15u;
           }
-          const bool run_end = lane == 31 || ((heads >> (lane + 1)) & 1u);
-          if (run_end && r < 16) sm.orow[rt][r] += vsum;
-          __syncwarp();
+        }
+        const bool by_quad = n >= 8 && __shfl_sync(0xffffffffu, qc, 0) != 15u;  // warp-uniform
+        auto add = [&](uint32_t e) {  // entry of row g (bit 3 clear) or g + 8
+          const float pv = h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]);
+          if (e & 8u) ob += pv; else oa += pv;
+        };
+        if (by_quad) {
+          uint32_t qe = qc;  // inclusive prefix sum over lanes 0..7: end of quad `lane`
+#pragma unroll
+          for (int d = 1; d < 8; d <<= 1) {
+            const uint32_t w = __shfl_up_sync(0xffffffffu, qe, d);
+            if (lane >= d) qe += w;
+          }
+          const int qend = (int)__shfl_sync(0xffffffffu, qe, g);
+          const int beg = qend - (int)__shfl_sync(0xffffffffu, qc, g) + t;
+          const int end = qend < n ? qend : n;  // the counts never point past the bucket
+          if (staged) {
+            // the first three entries of each lane loaded together (a quad rarely has more
+            // than twelve), then the rest
+            uint32_t e[3];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) e[i] = (beg + 4 * i < end) ? bs[beg + 4 * i] : 0u;
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+              if (beg + 4 * i < end) add(e[i]);
+            for (int p = beg + 12; p < end; p += 4) add(bs[p]);
+          } else {
+            for (int p = beg; p < end; p += 4) add(__ldg(bg + p));
+          }
+        } else {
+          // chunks of 32 entries: segmented sum over each row's run (runs are contiguous),
+          // and the last lane of a run adds it to the row's sum
+          auto chunks = [&](auto ld) {
+            for (int c0 = 0; c0 < n; c0 += 32) {
+              const int i = c0 + lane;
+              const bool valid = i < n;
+              uint32_t e = 0u;
+              if (valid) e = ld(i);
+              const int r = valid ? (int)(e & 15u) : 16;
+              float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]) : 0.f;
+              // runs from head flags: lane l's run starts at the last head at or below l
+              const int rprev = __shfl_up_sync(0xffffffffu, r, 1);
+              const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || rprev != r);
+              const int start = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
+#pragma unroll
+              for (int d = 1; d < 32; d <<= 1) {
+                const float vu = __shfl_up_sync(0xffffffffu, vsum, d);
+                if (lane - d >= start) vsum += vu;
+              }
+              const bool run_end = lane == 31 || ((heads >> (lane + 1)) & 1u);
+              if (run_end && r < 16) sm.orow[rt][r] += vsum;
+              __syncwarp();
+            }
+          };
+          if (staged) chunks(from_smem); else chunks(from_gmem);
         }
       } else {
-      int lo = 0;
-      if (n > 0) {
-        int hi = n;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if ((int)(ent(mid) & 15u) < lane) lo = mid + 1; else hi = mid;
-        }
-      }
-      const int beg = __shfl_sync(0xffffffffu, lo, orow), end = __shfl_sync(0xffffffffu, lo, orow + 1);
-      for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
-        const uint32_t e = ent(p);
-        const int k = (int)((e >> 4) & 255u);
-        const float val = h2f_dev((uint16_t)(e >> 16));
+        // lane q <= 16 finds the first entry whose row position (2 (row & 7) + row / 8, the
+        // bucket's order) is >= q; row r's run starts at its position's answer
+        auto pos = [](uint32_t e) { return (int)(((e & 7u) << 1) | ((e >> 3) & 1u)); };
+        const int rpos = ((orow & 7) << 1) | (orow >> 3);
+        auto rows = [&](auto ld) {
+          int lo = 0, hi = n;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (pos(ld(mid)) < lane) lo = mid + 1; else hi = mid;
+          }
+          const int beg = __shfl_sync(0xffffffffu, lo, rpos), end = __shfl_sync(0xffffffffu, lo, rpos + 1);
+          for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
+            const uint32_t e = ld(p);
+            const int k = (int)((e >> 4) & 255u);
+            const float val = h2f_dev((uint16_t)(e >> 16));
 #pragma unroll
-        for (int j = 0; j < OT; ++j)
-          if (otok0 + j < (MODE == 1 ? 1 : M))
-            oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
-      }
+            for (int j = 0; j < OT; ++j)
+              if (otok0 + j < M) oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
+          }
+        };
+        if (staged) rows(from_smem); else rows(from_gmem);
       }
     }
     __syncwarp();

@@ -330,14 +330,21 @@ __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, i
 __device__ __forceinline__ void spqr_outliers_tile(uint8_t* bt, const uint32_t* staged, uint32_t stage_base,
                                                    const uint32_t* ents, uint32_t b0, uint32_t b1, int kb, int row0,
                                                    int lane) {
-  for (uint32_t p = b0 + lane; p < b1; p += 32) {
-    const uint32_t e = staged ? staged[p - stage_base] : __ldg(ents + p);
-    const int kin = (int)((e >> 4) & 255u);
-    if ((kin >> 6) != kb) continue;
-    const int row = row0 + (int)(e & 15u);
-    uint16_t* dst = reinterpret_cast<uint16_t*>(bt + sw128(row, kin & 63));
-    *dst = f2bf(__fadd_rn(bf2f(*dst), h2f_dev((uint16_t)(e >> 16))));
-  }
+  // one loop per source behind a uniform branch (a select would issue the global load too)
+  auto walk = [&](auto ld) {
+    for (uint32_t p = b0 + lane; p < b1; p += 32) {
+      const uint32_t e = ld(p);
+      const int kin = (int)((e >> 4) & 255u);
+      if ((kin >> 6) != kb) continue;
+      const int row = row0 + (int)(e & 15u);
+      uint16_t* dst = reinterpret_cast<uint16_t*>(bt + sw128(row, kin & 63));
+      *dst = f2bf(__fadd_rn(bf2f(*dst), h2f_dev((uint16_t)(e >> 16))));
+    }
+  };
+  if (staged)
+    walk([&](uint32_t p) { return staged[p - stage_base]; });
+  else
+    walk([&](uint32_t p) { return __ldg(ents + p); });
 }
 
 template <int F>

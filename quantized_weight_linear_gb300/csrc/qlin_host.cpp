@@ -612,6 +612,25 @@ static qlin_status build_spqr(qlin_layer* L, const float* W) {
         ents[fill[bkt]++] = ((uint32_t)L->val[p] << 16) | ((uint32_t)(k % kSpqrSuper) << 4) | (uint32_t)rr;
       }
     }
+    // Order inside a bucket: by quad (row & 7), then row, then k -- an MMA lane quad g owns
+    // the accumulators of rows g and g + 8, so each quad's outliers are one run, and so is
+    // each row's.  With at least 8 entries, bits 12..15 of entries 0..7 hold the entry counts
+    // of quads 0..7 (15 in all eight when some quad has 15 or more).
+    auto key = [](uint32_t e) {
+      const uint32_t r = e & 15u;
+      return (((r & 7u) << 1 | (r >> 3)) << 8) | ((e >> 4) & 255u);
+    };
+    for (size_t b = 0; b < units * 4; ++b) {
+      uint32_t* e0 = ents + offs[b];
+      const uint32_t n = offs[b + 1] - offs[b];
+      std::sort(e0, e0 + n, [&](uint32_t a, uint32_t c) { return key(a) < key(c); });
+      if (n < 8) continue;
+      uint32_t cnt[8] = {};
+      for (uint32_t i = 0; i < n; ++i) cnt[e0[i] & 7u]++;
+      bool esc = false;
+      for (int q = 0; q < 8; ++q) esc = esc || cnt[q] >= 15;
+      for (int q = 0; q < 8; ++q) e0[q] |= (esc ? 15u : cnt[q]) << 12;
+    }
   }
   return QLIN_OK;
 }

@@ -35,8 +35,11 @@
 //     (row g+8, group 2t), (row g+8, group 2t+1)  -- the accumulator (C) side of the MMA.
 //   Outliers: a separate entry array of uint32 (fp16 value << 16 | k in unit << 4 | row
 //   in tile), bucketed by (unit, row tile); offs[(unit * 4 + rt)] is the first entry of a
-//   bucket and offs[units * 4] the total.  Within a bucket entries are sorted by row, then
-//   k (the decode kernel finds each row's run by bisection).
+//   bucket and offs[units * 4] the total.  Within a bucket entries are sorted by quad
+//   (row & 7), then row, then k: the rows g and g + 8 of MMA lane quad g form one run, each
+//   row a run inside it.  Bits 12..15 of entries 0..7 of a bucket with at least 8 entries
+//   hold the entry counts of quads 0..7, or 15 in all eight when a quad has 15 or more
+//   (bits 12..15 of every other entry are zero).
 //
 // W8A8 unit = (row group, one 64-wide K block), 4096 bytes of codes:
 //   codes [4 row tiles][32 lanes][8 words] bytes u = q + 128 in A-fragment order; for

@@ -80,9 +80,11 @@ def test_spqr_device_dequant_bit_exact(qlin, N, K, frac):
     assert np.array_equal(wd.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (1000, 2048, 0.01)])
+@pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (1000, 2048, 0.01), (192, 1024, 0.001)])
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
 def test_spqr_forward_tolerance(qlin, N, K, frac, M):
+    """frac = 0.001 leaves most (unit, row tile) buckets with fewer than eight outliers, the
+    size below which the M == 1 kernel does not use the quad counts."""
     W, X = synth.spqr_layer(N, K, M, seed=M)
     layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
