@@ -66,6 +66,7 @@ struct TcCfg<kW4> {
   static constexpr int kConvGroups = 1;
   static constexpr int kNPK = QLIN_W4_NPK;  // packed-unit stages (each covers kBlocksPerUnit k-blocks)
   static constexpr uint32_t kAType = 1;  // bf16
+  static constexpr bool kRowsInLanes = true;  // D = weight rows (TMEM lanes) x tokens (columns)
 };
 template <>
 struct TcCfg<kSpqr> {
@@ -73,6 +74,7 @@ struct TcCfg<kSpqr> {
   static constexpr int kConvGroups = 2;  // two groups of 8 converter warps take alternate k-blocks
   static constexpr int kNPK = QLIN_SP_NPK;
   static constexpr uint32_t kAType = 1;
+  static constexpr bool kRowsInLanes = false;  // D = tokens (lanes) x weight rows (columns)
 };
 template <>
 struct TcCfg<kW8> {
@@ -80,6 +82,7 @@ struct TcCfg<kW8> {
   static constexpr int kConvGroups = 1;
   static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
+  static constexpr bool kRowsInLanes = true;  // (the drain epilogue assumes this)
 };
 
 template <int F>
@@ -380,7 +383,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   const int bpu = C::kBlocksPerUnit;
   const int nunits = nkb / bpu;
   const int32_t* kb = F == kW8 ? a.kbound + (int64_t)m_tile * nkb : nullptr;  // this tile's block bounds
-  constexpr uint32_t idesc = idesc_f16(C::kAType, kBN, 128);
+  // W4, W8A8: one MMA per k-step, A = the converted weight tile (M = 128 rows), B = the X tile
+  // (N = 256 tokens); D in TMEM has the weight rows in its lanes and the tokens in its columns.
+  // SpQR: two MMAs per k-step, A = one 128-token half of X, B = the weight tile (N = 128); D
+  // has the tokens in its lanes (measured faster for SpQR only).
+  constexpr bool kRowsInLanes = C::kRowsInLanes;
+  static_assert(F != kW8 || kRowsInLanes, "the W8A8 drain reads weight rows from TMEM lanes");
+  constexpr uint32_t idesc = kRowsInLanes ? idesc_f16(C::kAType, BM, kBN) : idesc_f16(C::kAType, kBN, 128);
   constexpr uint32_t tmem_cols = F == kW8 ? 512u : 128u * MH;  // W8A8: fp32 chunk sums + int32 partials
   // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
   int64_t off_base[2] = {0, 0};
@@ -519,14 +528,21 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
           break;
         }
         tc_fence_after();
-        const uint64_t db = umma_desc_sw128(sm.b[s]);
-#pragma unroll
-        for (int mh = 0; mh < MH; ++mh) {
-          const uint64_t da = umma_desc_sw128(sm.a[s] + mh * kTileBytes);
+        const uint64_t dw = umma_desc_sw128(sm.b[s]);  // weights, 128 rows
+        if constexpr (kRowsInLanes) {
+          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16(tmem + dcol + 128u * mh, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc,
-                     (first && kk == 0) ? 0u : 1u);
+            umma_f16(tmem + dcol, dw + (uint64_t)(2 * kk), dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        } else {
+#pragma unroll
+          for (int mh = 0; mh < MH; ++mh) {
+            const uint64_t dx = umma_desc_sw128(sm.a[s] + mh * kTileBytes);  // X, 128 tokens
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_f16(tmem + dcol + 128u * mh, dx + (uint64_t)(2 * kk), dw + (uint64_t)(2 * kk), idesc,
+                       (first && kk == 0) ? 0u : 1u);
+          }
         }
         umma_commit(&sm.ab_empty[s]);
         if constexpr (F == kW8) {
@@ -588,44 +604,61 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       if (lane == 0) mbar_arrive(&sm.pk_empty[p]);
     }
     if constexpr (F != kW8) {
-      // epilogue (first converter group): TMEM lane quadrant q = warp % 4; the two warps of a
-      // quadrant take one 128-token half each
+      // epilogue (first converter group): TMEM lane quadrant q = warp % 4 holds weight rows
+      // 32q.., the two warps of a quadrant take one 128-token half each; a warp's store of one
+      // token writes 32 consecutive outputs of Y's row
       const int q = warp & 3;
       const int mh = cw / 4;
       if (grp == 0 && ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
         tc_fence_after();
-        const int m = m_tile * BM + 128 * mh + 32 * q + lane;
-        const int n0 = n_tile * kBN;
+        if constexpr (kRowsInLanes) {
+          const int n = n_tile * kBN + 32 * q + lane;
+#pragma unroll 1
+          for (int cb = 0; cb < 128 / 32; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128u * mh + 32u * cb, r);
+            const int m0 = m_tile * BM + 128 * mh + 32 * cb;
+            if (n < a.N) {
+              uint16_t* dst = a.Y + (int64_t)m0 * a.N + n;
 #pragma unroll
-        for (int cb = 0; cb < kBN / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128u * mh + 32u * cb, r);
-          // N is a multiple of 64 rows (the device image pads row groups), so a 32-column
-          // slice is either fully inside or fully outside the output
-          const int n = n0 + 32 * cb;
-          if (m < a.M && n + 32 <= a.N) {
-            uint32_t pk16[16];
+              for (int i = 0; i < 32; ++i)
+                if (m0 + i < a.M) dst[(int64_t)i * a.N] = f2bf(__uint_as_float(r[i]));
+            }
+          }
+        } else {
+          // lanes are tokens: each lane writes 32 consecutive outputs of its token's row
+          const int m = m_tile * BM + 128 * mh + 32 * q + lane;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            uint16_t* dst = a.Y + (int64_t)m * a.N + n;
+          for (int cb = 0; cb < kBN / 32; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128u * mh + 32u * cb, r);
+            // N is a multiple of 64 rows (the device image pads row groups), so a 32-column
+            // slice is either fully inside or fully outside the output
+            const int n = n_tile * kBN + 32 * cb;
+            if (m < a.M && n + 32 <= a.N) {
+              uint32_t pk16[16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+              for (int i = 0; i < 16; ++i) pk16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+              uint16_t* dst = a.Y + (int64_t)m * a.N + n;
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+            }
           }
         }
       }
     }
   } else if constexpr (F == kW8) {
     // ------------------------------------------------------------------ exact int32 drain + epilogue
-    // warps 6..13: TMEM lane quadrant q = warp % 4 (tokens 32q..32q+31 of an M half), M half
+    // warps 6..13: TMEM lane quadrant q = warp % 4 (weight rows 32q..32q+31), token half
     // mh = (warp - 6) / 4 (accumulator columns 128 mh.., int32 partials 256 + 128 mh..)
     pdl_wait();
     const int q = warp & 3;
     const int mh = (warp - 2 - NCONV) / 4;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const uint32_t fcol = 128u * mh, icol = 256u + 128u * mh;
-    const int m = m_tile * BM + 128 * mh + 32 * q + lane;
-    const int n0 = n_tile * kBN;
+    const int n = n_tile * kBN + 32 * q + lane;  // this lane's weight row
+    const float swn = n < a.N ? a.sw[n] : 0.f;
     int nchunks = 1;  // the MMA issuer's chunking, replayed
     for (int i = 0, bound = 0; i < nkb; ++i) {
       const int bi = kb[i];
@@ -660,29 +693,20 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
           tmem_st32(tmem + lane_base + icol + 32u * cb, r);
           continue;
         }
-        // N is a multiple of 64 rows (the device image pads row groups), so a 32-column slice
-        // is either fully inside or fully outside the output
-        const int n = n0 + 32 * cb;
-        if (m >= a.M || n + 32 > a.N) continue;
+        // columns are tokens m0 + i; a warp's store of one token writes 32 consecutive outputs
+        const int m0 = m_tile * BM + 128 * mh + 32 * cb;
+        if (n >= a.N) continue;
         if (a.acc_out) {
-          int32_t* dst = a.acc_out + (int64_t)m * a.N + n;
+          int32_t* dst = a.acc_out + (int64_t)m0 * a.N + n;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            reinterpret_cast<int4*>(dst)[v] =
-                make_int4((int)r[4 * v], (int)r[4 * v + 1], (int)r[4 * v + 2], (int)r[4 * v + 3]);
+          for (int i = 0; i < 32; ++i)
+            if (m0 + i < a.M) dst[(int64_t)i * a.N] = (int32_t)r[i];
         } else {
-          const float sxm = a.sx[m];
-          uint32_t pk16[16];
+          uint16_t* dst = a.Y + (int64_t)m0 * a.N + n;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[2 * i]), sxm), a.sw[n + 2 * i]);
-            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[2 * i + 1]), sxm), a.sw[n + 2 * i + 1]);
-            pk16[i] = (uint32_t)f2bf(y0) | ((uint32_t)f2bf(y1) << 16);
-          }
-          uint16_t* dst = a.Y + (int64_t)m * a.N + n;
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2], pk16[4 * v + 3]);
+          for (int i = 0; i < 32; ++i)
+            if (m0 + i < a.M)
+              dst[(int64_t)i * a.N] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[i]), a.sx[m0 + i]), swn));
         }
       }
       if (!last) {
