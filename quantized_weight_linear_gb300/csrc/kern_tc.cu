@@ -37,6 +37,10 @@ constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
 constexpr int kExactL1 = 132104;  // floor(2^24 / 127)
 constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
 constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
+#ifndef QLIN_TC_RASTER_G
+#define QLIN_TC_RASTER_G 4
+#endif
+constexpr int kRasterG = QLIN_TC_RASTER_G;  // token tiles per raster group
 
 enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 
@@ -377,7 +381,14 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   constexpr int NGRP = C::kConvGroups, GCONV = NCONV / NGRP;  // converter warps per k-block
   constexpr int BM = 128 * MH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+  // grouped raster: consecutive CTAs walk kRasterG token tiles of one weight tile before the
+  // next weight tile, so a wave reads each weight tile from HBM once and shares it through L2
+  const int mt_count = (a.M + BM - 1) / BM, nt_count = (a.N + kBN - 1) / kBN;
+  const int group = (int)(blockIdx.x / (unsigned)(kRasterG * nt_count));
+  const int m_first = group * kRasterG;
+  const int gm = mt_count - m_first < kRasterG ? mt_count - m_first : kRasterG;
+  const int r_in = (int)blockIdx.x - group * kRasterG * nt_count;
+  const int m_tile = m_first + r_in % gm, n_tile = r_in / gm;
   const int64_t rg0 = (int64_t)n_tile * 2;  // two 64-row groups per 128-row tile
   const int nkb = a.K / kBK;
   const int bpu = C::kBlocksPerUnit;
@@ -751,7 +762,7 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((args.N + kBN - 1) / kBN), (unsigned)((args.M + BM - 1) / BM));
+  cfg.gridDim = dim3((unsigned)(((args.N + kBN - 1) / kBN) * ((args.M + BM - 1) / BM)));
   cfg.blockDim = dim3(tc_threads<F>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
