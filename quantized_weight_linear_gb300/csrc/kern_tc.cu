@@ -5,17 +5,22 @@
 // batch grows the layer becomes compute-bound and the dequantization overhead is what
 // erodes weight-only speedups; W8A8 keeps both operands on the tensor cores.  Design:
 //
-// * CTA tile: 128 output rows (MMA N) x 256 tokens (two 128-row MMAs that share each
-//   dequantized B tile, halving the dequantization per FLOP); K in blocks of 64;
+// * CTA tile: 128 output rows x 256 tokens (each dequantized weight tile serves 256 tokens,
+//   halving the dequantization per FLOP); K in blocks of 64.  W4 / W8A8: one MMA per k-step
+//   with the weight tile as A (M = 128) and the X tile as B (N = 256), so D has the weight
+//   rows in its TMEM lanes; SpQR: two MMAs per k-step (X halves as A, M = 128; the weight
+//   tile as B, N = 128), tokens in the lanes (each orientation measured faster for its formats);
+// * grouped raster: consecutive CTAs take 4 token tiles of one weight tile before the next,
+//   so the CTAs of a wave share weight tiles through L2;
 // * warp 0: TMA producer -- X tiles through a 2-D tensor map (128B swizzle) and the packed
 //   weight units of the tile (the device image the decode kernels stream; SpQR: plus the
 //   unit's outlier buckets) through cp.async.bulk into a packed ring;
 // * warp 1: allocates TMEM and issues tcgen05.mma (kind::f16, bf16 or fp16 operands, fp32
 //   accumulators in TMEM) from one elected thread, committing each k-block back to its
 //   shared-memory stage;
-// * converter warps (8 for W4 / SpQR, 4 for W8A8): turn packed codes into the bf16 / fp16
-//   K-major 128B-swizzled B operand; for W4 / SpQR they then run the epilogue
-//   (tcgen05.ld -> bf16 -> Y);
+// * converter warps (8 for W4 and W8A8, 16 in two groups for SpQR): turn packed codes into
+//   the bf16 / fp16 K-major 128B-swizzled weight operand; for W4 / SpQR they then run the
+//   epilogue (tcgen05.ld -> bf16 -> Y);
 // * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
 //   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds of
 //   sum |qx| that the act-quant kernel gathers), so the fp32 chunk accumulators (TMEM
@@ -55,6 +60,9 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #ifndef QLIN_W8_ST
 #define QLIN_W8_ST 3
 #endif
+#ifndef QLIN_W8_CONV
+#define QLIN_W8_CONV 8
+#endif
 #ifndef QLIN_W4_NPK
 #define QLIN_W4_NPK 2
 #endif
@@ -82,7 +90,7 @@ struct TcCfg<kSpqr> {
 };
 template <>
 struct TcCfg<kW8> {
-  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = 4, kStages = QLIN_W8_ST;
+  static constexpr int kUnitBytes = kW8UnitBytes, kBlocksPerUnit = 1, kMH = 2, kConv = QLIN_W8_CONV, kStages = QLIN_W8_ST;
   static constexpr int kConvGroups = 1;
   static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
