@@ -103,6 +103,23 @@ typedef struct {
  * Returns INVALID_ARG on bad shapes/values (a group whose scale overflows fp16 included). */
 qlin_status qlin_pack_w4g128(const float* W, int N, int K, qlin_handle* out);
 
+/* W4 g128 with GPTQ error compensation (GPTQ page, "Makale Bülteni — GPTQ" intro and
+ * "İddia ve Gerçeklik: GPTQ": inverse Hessian from the covariance of the layer inputs,
+ * stabilised by a Cholesky decomposition; columns quantized in order, each column's rounding
+ * error spread at once over the columns not yet quantized).  Same handle, layout and kernels
+ * as qlin_pack_w4g128.  Steps: H = Xcal^T Xcal (fp64); an always-zero input column gets
+ * H_kk = 1 and zero weights; H += damp * mean(diag H) * I; U = upper Cholesky factor of H^-1;
+ * at the first column of each 128-group the group's scale/zero are round-to-nearest over the
+ * group's current weights (fp32); column k gets the round-to-nearest code with them, and
+ * every later weight of the row moves by -e * U_kj, e = (w_k - w_hat_k) / U_kk (fp64).
+ * With H = I the result equals qlin_pack_w4g128's bit for bit.
+ * W: host fp32 [N][K]; Xcal: host fp32 [S][K] calibration inputs (row-major); both read only,
+ * not retained.  K % 128 == 0, K <= 8192 (H and its factors are K x K fp64 on the host),
+ * S >= 1, damp > 0 (0.01 is the usual value), W and Xcal finite.  Returns INVALID_ARG on bad
+ * shapes/values or if H + damping is not positive definite; the work is O(K^3 + N K^2). */
+qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xcal, int S, double damp,
+                                  qlin_handle* out);
+
 /* SpQR 3-bit g16 bi-level + fp16 CSR outliers (SpQR page, see above).  The outliers are
  * the floor(f*N*K) largest |w| (ties: smaller linear index), standing in for the page's
  * Hessian-sensitivity choice.  K % 256 == 0, K <= 32768 (int16 columns), 0 <= f < 1. */

@@ -12,7 +12,8 @@ SmoothQuant pages talk about:
   reality" section);
 * the per-channel activation maxima a calibration pass would collect.
 
-Stream keys: X = 1, W = 2, outlier channels = 3, chi-square draws = 4.
+Stream keys: X = 1, W = 2, outlier channels = 3, chi-square draws = 4, calibration
+block factors = 5.
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ KEY_X = 1
 KEY_W = 2
 KEY_CHANNELS = 3
 KEY_CHI = 4
+KEY_CALIB = 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
@@ -146,6 +148,21 @@ def spqr_layer(N: int, K: int, M: int, seed: int = 0):
     W = student_t3(seed, 0.02, (N, K))
     X = activations_bf16(seed, M, K)
     return W, X
+
+
+def gptq_calibration(S: int, K: int, seed: int = 0, block: int = 16) -> np.ndarray:
+    """Calibration rows for the GPTQ packer: fp32 [S, K] of bf16 values.
+
+    x[s, k] = z[s, k] + c[s, k // block] with z, c ~ N(0, 1) on their own streams, so the
+    channels of a block are correlated as real layer inputs are (an identity covariance would
+    leave nothing to compensate); rounded to bf16, and |x| < 2^-8 set to 0, so that every
+    product of two inputs is a multiple of 2^-30 and X^T X is exact in fp64 whatever the
+    summation order (for S * max|x|^2 < 2^23).
+    """
+    z = normal(seed, KEY_X, 1.0, (S, K))
+    c = normal(seed, KEY_CALIB, 1.0, (S, (K + block - 1) // block))
+    x = bf16_to_f32(f32_to_bf16(z + np.repeat(c, block, axis=1)[:, :K]))
+    return np.where(np.abs(x) < np.float32(2.0 ** -8), np.float32(0), x).astype(np.float32)
 
 
 def smoothquant_layer(N: int, K: int, M: int, seed: int = 0):

@@ -35,7 +35,8 @@ FMT_W8A8 = 3
 
 #: every entry point include/qlin.h declares
 EXPORTED_SYMBOLS = (
-    "qlin_pack_w4g128", "qlin_pack_spqr", "qlin_pack_w8", "qlin_device_bytes", "qlin_workspace_bytes",
+    "qlin_pack_w4g128", "qlin_pack_w4g128_gptq", "qlin_pack_spqr", "qlin_pack_w8", "qlin_device_bytes",
+    "qlin_workspace_bytes",
     "qlin_bind", "qlin_attach", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
     "qlin_forward_acc", "qlin_dequant_device", "qlin_poll_status", "qlin_export", "qlin_info",
     "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout", "qlin_forward_spqr_static",
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
         H = ctypes.c_void_p
         sig = {
             "qlin_pack_w4g128": ([vp, i32, i32, ctypes.POINTER(H)], i32),
+            "qlin_pack_w4g128_gptq": ([vp, i32, i32, vp, i32, ctypes.c_double, ctypes.POINTER(H)], i32),
             "qlin_pack_spqr": ([vp, i32, i32, f32, ctypes.POINTER(H)], i32),
             "qlin_pack_w8": ([vp, i32, i32, vp, f32, ctypes.POINTER(H)], i32),
             "qlin_device_bytes": ([H, ctypes.POINTER(sz)], i32),
@@ -174,6 +176,17 @@ def qlin_pack_w4g128(W) -> Handle:
     W = _f32(W)
     h = ctypes.c_void_p()
     _check(lib().qlin_pack_w4g128(_vp(W), W.shape[0], W.shape[1], ctypes.byref(h)), "qlin_pack_w4g128")
+    return Handle(h)
+
+
+def qlin_pack_w4g128_gptq(W, Xcal, damp: float = 0.01) -> Handle:
+    W = _f32(W)
+    X = _f32(Xcal)
+    if X.ndim != 2 or X.shape[1] != W.shape[1]:
+        raise ValueError("Xcal must be [S, K] with the layer's K")
+    h = ctypes.c_void_p()
+    _check(lib().qlin_pack_w4g128_gptq(_vp(W), W.shape[0], W.shape[1], _vp(X), X.shape[0], float(damp),
+                                       ctypes.byref(h)), "qlin_pack_w4g128_gptq")
     return Handle(h)
 
 
@@ -302,6 +315,10 @@ class QLinear:
     @classmethod
     def from_w4g128(cls, W):
         return cls(qlin_pack_w4g128(W))
+
+    @classmethod
+    def from_w4g128_gptq(cls, W, Xcal, damp: float = 0.01):
+        return cls(qlin_pack_w4g128_gptq(W, Xcal, damp))
 
     @classmethod
     def from_spqr(cls, W, outlier_frac: float = 0.01):

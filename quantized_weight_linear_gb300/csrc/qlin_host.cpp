@@ -212,9 +212,10 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // ------------------------------------------------------------------------------------
 // W4 g128
 
+static void build_w4_image(qlin_layer* L, const std::vector<uint8_t>& q);
+
 static qlin_status build_w4(qlin_layer* L, const float* W) {
   const int N = L->N, K = L->K, G = K / kW4Group;
-  L->codes.assign((size_t)N * (K / 8), 0u);
   L->scale.assign((size_t)N * G, 0);
   L->zero.assign((size_t)N * G, 0);
   std::vector<uint8_t> q((size_t)N * K);
@@ -233,14 +234,25 @@ static qlin_status build_w4(qlin_layer* L, const float* W) {
         for (int i = 0; i < kW4Group; ++i)
           q[(size_t)n * K + g * kW4Group + i] = (uint8_t)rtn_code(row[g * kW4Group + i], st, 4);
       }
+    }
+  });
+  if (bad) return QLIN_ERR_INVALID_ARG;
+  build_w4_image(L, q);
+  return QLIN_OK;
+}
+
+// Canonical codes [N][K/8] and the device image from codes q [N][K] (scale and zero set).
+static void build_w4_image(qlin_layer* L, const std::vector<uint8_t>& q) {
+  const int N = L->N, K = L->K, G = K / kW4Group;
+  L->codes.assign((size_t)N * (K / 8), 0u);
+  parallel_for(N, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n)
       for (int j = 0; j < K / 8; ++j) {
         uint32_t w = 0;
         for (int i = 0; i < 8; ++i) w |= (uint32_t)q[(size_t)n * K + 8 * j + i] << (4 * i);
         L->codes[(size_t)n * (K / 8) + j] = w;
       }
-    }
   });
-  if (bad) return QLIN_ERR_INVALID_ARG;
 
   // device image: units [RG][G], codes in A-fragment order + (scale, zero) per row
   const int RG = (N + kRowGroup - 1) / kRowGroup;
@@ -287,6 +299,138 @@ static qlin_status build_w4(qlin_layer* L, const float* W) {
       }
     }
   });
+}
+
+// ------------------------------------------------------------------------------------
+// GPTQ W4 g128 (GPTQ page, "Makale Bülteni — GPTQ" intro and "İddia ve Gerçeklik: GPTQ"):
+// the inverse Hessian comes from the covariance of the layer inputs and is stabilised by a
+// Cholesky decomposition; columns are quantized in order and each column's rounding error is
+// spread at once over the columns not yet quantized.  The steps the page leaves open are read
+// as: H = Xcal^T Xcal (fp64); an always-zero input column gets H_kk = 1 and zero weights;
+// H += damp * mean(diag H) * I; U = the upper Cholesky factor of H^-1 (H^-1 = U^T U); at the
+// first column of each 128-group the group's scale and zero are the round-to-nearest ones of
+// the group's current weights (as fp32); a column's code is the round-to-nearest code with
+// them, and with e = (w_k - w_hat_k) / U_kk every later weight of the row becomes
+// w_j - e * U_kj (fp64).  The page batches the updates of a 128-block for speed on a GPU; on
+// the host each row is independent and is updated column by column (the same arithmetic).
+
+static constexpr int kGptqMaxK = 8192;  // H and its factors are K x K fp64 on the host
+
+// U with H^-1 = U^T U, U upper triangular with a positive diagonal: with J the order reversal,
+// J H J = L L^T (lower Cholesky factor L) gives H = V V^T for the upper V = J L J, and
+// H^-1 = (V^-1)^T V^-1, so U = V^-1.  H is overwritten.  Returns false if H is not positive
+// definite.
+static bool gptq_inverse_factor(std::vector<double>& H, int K, std::vector<double>& U) {
+  // L (lower, row-major) of A = J H J, computed in place over A
+  std::vector<double> A((size_t)K * K);
+  for (int i = 0; i < K; ++i)
+    for (int j = 0; j < K; ++j) A[(size_t)i * K + j] = H[(size_t)(K - 1 - i) * K + (K - 1 - j)];
+  std::vector<double>().swap(H);
+  for (int j = 0; j < K; ++j) {
+    const double* Lj = &A[(size_t)j * K];
+    double d = A[(size_t)j * K + j];
+    for (int p = 0; p < j; ++p) d -= Lj[p] * Lj[p];
+    if (!(d > 0.0)) return false;
+    const double ljj = std::sqrt(d);
+    A[(size_t)j * K + j] = ljj;
+    auto rows = [&](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i) {
+        double* Li = &A[(size_t)(j + 1 + i) * K];
+        double v = Li[j];
+        for (int p = 0; p < j; ++p) v -= Li[p] * Lj[p];
+        Li[j] = v / ljj;
+      }
+    };
+    const int64_t rest = K - 1 - j;
+    if ((int64_t)rest * j > (1 << 16)) parallel_for(rest, rows); else rows(0, rest);
+  }
+  // V = J L J (upper): V[i][j] = L[K-1-i][K-1-j]; U = V^-1 column by column (back substitution),
+  // column j of U kept as row j of UT so both operands are contiguous
+  auto V = [&](int i, int j) { return A[(size_t)(K - 1 - i) * K + (K - 1 - j)]; };
+  std::vector<double> Vr((size_t)K * K, 0.0);  // V row-major, upper part
+  for (int i = 0; i < K; ++i)
+    for (int j = i; j < K; ++j) Vr[(size_t)i * K + j] = V(i, j);
+  std::vector<double>().swap(A);
+  std::vector<double> UT((size_t)K * K, 0.0);
+  parallel_for(K, [&](int64_t b, int64_t e) {
+    for (int64_t j = b; j < e; ++j) {
+      double* u = &UT[(size_t)j * K];
+      for (int64_t i = j; i >= 0; --i) {
+        const double* Vi = &Vr[(size_t)i * K];
+        double v = (i == j) ? 1.0 : 0.0;
+        for (int64_t p = i + 1; p <= j; ++p) v -= Vi[p] * u[p];
+        u[i] = v / Vi[i];
+      }
+    }
+  });
+  U.assign((size_t)K * K, 0.0);
+  for (int j = 0; j < K; ++j)
+    for (int i = 0; i <= j; ++i) U[(size_t)i * K + j] = UT[(size_t)j * K + i];
+  return true;
+}
+
+static qlin_status build_w4_gptq(qlin_layer* L, const float* W, const float* Xcal, int S, double damp) {
+  const int N = L->N, K = L->K, G = K / kW4Group;
+  // H = Xcal^T Xcal over the calibration rows, in row order
+  std::vector<double> H((size_t)K * K, 0.0);
+  parallel_for(K, [&](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i)
+      for (int s = 0; s < S; ++s) {
+        const float* x = Xcal + (size_t)s * K;
+        const double xi = (double)x[i];
+        if (xi == 0.0) continue;
+        double* Hi = &H[(size_t)i * K];
+        for (int j = 0; j < K; ++j) Hi[j] += xi * (double)x[j];
+      }
+  });
+  std::vector<uint8_t> dead(K, 0);
+  double diag = 0.0;
+  for (int k = 0; k < K; ++k) {
+    if (H[(size_t)k * K + k] == 0.0) {
+      dead[k] = 1;
+      H[(size_t)k * K + k] = 1.0;
+    }
+    diag += H[(size_t)k * K + k];
+  }
+  const double add = damp * (diag / K);
+  for (int k = 0; k < K; ++k) H[(size_t)k * K + k] += add;
+  std::vector<double> U;
+  if (!gptq_inverse_factor(H, K, U)) return QLIN_ERR_INVALID_ARG;
+
+  L->scale.assign((size_t)N * G, 0);
+  L->zero.assign((size_t)N * G, 0);
+  std::vector<uint8_t> q((size_t)N * K);
+  std::atomic<bool> bad{false};
+  parallel_for(N, [&](int64_t b, int64_t e) {
+    std::vector<double> w(K);
+    std::vector<float> gv(kW4Group);
+    for (int64_t n = b; n < e; ++n) {
+      const float* row = W + (size_t)n * K;
+      for (int k = 0; k < K; ++k) w[k] = dead[k] ? 0.0 : (double)row[k];
+      RtnStats st{};
+      for (int k = 0; k < K; ++k) {
+        const int g = k / kW4Group;
+        if (k % kW4Group == 0) {
+          for (int i = 0; i < kW4Group; ++i) gv[i] = (float)w[k + i];
+          st = rtn_stats(gv.data(), nullptr, kW4Group, 4);
+          if (st.overflow) {
+            bad = true;
+            return;
+          }
+          L->scale[(size_t)n * G + g] = st.scale_h;
+          L->zero[(size_t)n * G + g] = f2h(st.zero);
+        }
+        const int code = rtn_code((float)w[k], st, 4);
+        q[(size_t)n * K + k] = (uint8_t)code;
+        const float w_hat = ((float)code - st.zero) * st.scale;
+        const double ek = (w[k] - (double)w_hat) / U[(size_t)k * K + k];
+        const double* Uk = &U[(size_t)k * K];
+        for (int j = k + 1; j < K; ++j) w[j] -= ek * Uk[j];
+      }
+    }
+  });
+  if (bad) return QLIN_ERR_INVALID_ARG;
+  build_w4_image(L, q);
   return QLIN_OK;
 }
 
@@ -821,6 +965,34 @@ qlin_status qlin_pack_w4g128(const float* W, int N, int K, qlin_handle* out) {
   L->K = K;
   try {
     st = build_w4(L, W);
+  } catch (const std::bad_alloc&) {
+    st = QLIN_ERR_INVALID_ARG;
+  }
+  if (st != QLIN_OK) {
+    delete L;
+    return st;
+  }
+  *out = L;
+  return QLIN_OK;
+}
+
+qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xcal, int S, double damp,
+                                  qlin_handle* out) {
+  if (!out) return QLIN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (K % kW4Group || K > kGptqMaxK || !Xcal || S <= 0 || !(damp > 0.0) || !std::isfinite(damp))
+    return QLIN_ERR_INVALID_ARG;
+  qlin_status st = check_w(W, N, K);
+  if (st != QLIN_OK) return st;
+  st = check_w(Xcal, S, K);
+  if (st != QLIN_OK) return st;
+  qlin_layer* L = nullptr;
+  QLIN_TRY_ALLOC(L = new qlin_layer());
+  L->format = QLIN_FMT_W4G128;
+  L->N = N;
+  L->K = K;
+  try {
+    st = build_w4_gptq(L, W, Xcal, S, damp);
   } catch (const std::bad_alloc&) {
     st = QLIN_ERR_INVALID_ARG;
   }

@@ -69,6 +69,22 @@ def test_w4_one_hot_rows_bit_exact(qlin):
         assert np.array_equal(y[i], bf16_round(w_hat[:, k]))
 
 
+@pytest.mark.parametrize("M", [1, 16, 40])
+def test_w4_gptq_layer(qlin, M):
+    """GPTQ-packed codes (error-compensated, same W4 g128 format): the same kernels read
+    them; dequantized weights bit-exact, outputs within tolerance (M = 40: prefill)."""
+    from oracle import gptq
+    N, K = 192, 1024
+    W = synth.normal(21, synth.KEY_W, 0.02, (N, K))
+    Xcal = synth.gptq_calibration(256, K, seed=21)
+    layer = qlin.QLinear.from_w4g128_gptq(W, Xcal).to("cuda")
+    ref = gptq.pack(W, Xcal)
+    wd = layer.dequant_device().cpu().numpy()
+    assert np.array_equal(wd.view(np.uint32), ref["w_hat"].view(np.uint32))
+    X = synth.activations_bf16(21, M, K)
+    _check(_y(layer, X, M), X, ref["w_hat"])
+
+
 # ----------------------------------------------------------------------------- SpQR
 
 @pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (64, 256, 0.0)])
