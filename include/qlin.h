@@ -96,6 +96,22 @@ typedef struct {
   const float* s_inv;
 } qlin_canonical;
 
+/* ---- checkpoint load (host) --------------------------------------------------------- */
+
+/* A handle from canonical arrays in the layout qlin_export describes (a saved checkpoint):
+ * the GPTQ page ("Makale Bülteni — GPTQ", open-source paragraphs) and the SmoothQuant page
+ * ("Ticari Etki") describe inference engines loading already-quantized checkpoints; this is
+ * that load, with no quantization -- the device image is built exactly as the packer of the
+ * same format builds it, so forwards match the exporting handle bit for bit.
+ * format: QLIN_FMT_*.  in: host pointers to the format's arrays (the others are ignored),
+ * read only, not retained, sized as qlin_export documents (SpQR: nnz = rowptr[N]; col and val
+ * may be NULL when nnz == 0).  Checked: shapes as for the packers; W4 scales positive finite,
+ * zeros integers 0..15; SpQR stats finite with integer zs, zz in 0..7, rowptr starting at 0 and
+ * non-decreasing with at most K entries per row, columns strictly ascending in [0, K), values
+ * finite; W8 qw >= -127, sw, s, s_inv positive finite.  Anything else: INVALID_ARG.  The
+ * info fields alpha (W8A8) and outlier_frac (SpQR: nnz / (N K)) are informational. */
+qlin_status qlin_import(int format, int N, int K, const qlin_canonical* in, qlin_handle* out);
+
 /* ---- packing (offline, host) ------------------------------------------------------ */
 
 /* W4 g128, round-to-nearest asymmetric per (row, 128-group) (GPTQ page, see above).

@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "qlin_bind", "qlin_attach", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
     "qlin_forward_acc", "qlin_dequant_device", "qlin_poll_status", "qlin_export", "qlin_info",
     "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout", "qlin_forward_spqr_static",
+    "qlin_import",
 )
 
 
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
             "qlin_sm_count": ([], i32),
             "qlin_debug_wait_timeout": ([vp, i32, vp], i32),
             "qlin_forward_spqr_static": ([H, vp, vp, i32, vp], i32),
+            "qlin_import": ([i32, i32, i32, ctypes.POINTER(Canonical), ctypes.POINTER(H)], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -299,6 +301,35 @@ def qlin_export(h: Handle) -> dict:
             "s": arr(c.s, np.float32, (K,)), "s_inv": arr(c.s_inv, np.float32, (K,))}
 
 
+# canonical array names per format, with their dtypes (the dict qlin_export returns)
+_CANONICAL = {
+    FMT_W4G128: {"codes": np.uint32, "scale": np.float16, "zero": np.float16},
+    FMT_SPQR: {"codes": np.uint8, "qs_bits": np.uint8, "qz_bits": np.uint8, "stats": np.float16,
+               "rowptr": np.int32, "col": np.int16, "val": np.float16},
+    FMT_W8A8: {"qw": np.int8, "sw": np.float32, "s": np.float32, "s_inv": np.float32},
+}
+_FIELD = {"codes3": "codes", "qs3": "qs_bits", "qz3": "qz_bits"}  # struct field -> dict key (SpQR)
+
+
+def qlin_import(fmt: int, N: int, K: int, arrays: dict) -> Handle:
+    """A handle from canonical arrays (a qlin_export dict or a loaded checkpoint); no quantization."""
+    if fmt not in _CANONICAL:
+        raise ValueError(f"unknown format {fmt}")
+    keep = {k: np.ascontiguousarray(arrays[k], dtype=dt) for k, dt in _CANONICAL[fmt].items()}
+    c = Canonical()
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p).value if a.size else None
+    if fmt == FMT_W4G128:
+        c.codes, c.scale, c.zero = ptr(keep["codes"]), ptr(keep["scale"]), ptr(keep["zero"])
+    elif fmt == FMT_SPQR:
+        c.codes3, c.qs3, c.qz3 = ptr(keep["codes"]), ptr(keep["qs_bits"]), ptr(keep["qz_bits"])
+        c.stats, c.rowptr, c.col, c.val = ptr(keep["stats"]), ptr(keep["rowptr"]), ptr(keep["col"]), ptr(keep["val"])
+    else:
+        c.qw, c.sw, c.s, c.s_inv = ptr(keep["qw"]), ptr(keep["sw"]), ptr(keep["s"]), ptr(keep["s_inv"])
+    h = ctypes.c_void_p()
+    _check(lib().qlin_import(int(fmt), int(N), int(K), ctypes.byref(c), ctypes.byref(h)), "qlin_import")
+    return Handle(h)
+
+
 # -------------------------------------------------------------------------------- torch front end
 
 class QLinear:
@@ -384,6 +415,17 @@ class QLinear:
 
     def export(self) -> dict:
         return qlin_export(self.handle)
+
+    def save(self, path) -> None:
+        """Writes the canonical packed arrays (the qlin_export layouts) to an .npz checkpoint."""
+        np.savez(path, format=np.int32(self.format), N=np.int32(self.N), K=np.int32(self.K), **self.export())
+
+    @classmethod
+    def load(cls, path):
+        """A layer from a checkpoint written by save(); the weights are not requantized."""
+        with np.load(path) as z:
+            fmt, N, K = int(z["format"]), int(z["N"]), int(z["K"])
+            return cls(qlin_import(fmt, N, K, {k: z[k] for k in _CANONICAL.get(fmt, {})}))
 
 
 def build(force: bool = False) -> str:

@@ -532,6 +532,9 @@ static void put_bits3(std::vector<uint8_t>& stream, size_t row_off, int idx, int
     if ((code >> b) & 1) stream[row_off + bit / 8] |= (uint8_t)(1u << (bit % 8));
 }
 
+static void build_spqr_image(qlin_layer* L, const std::vector<uint8_t>& q, const std::vector<uint8_t>& qs,
+                             const std::vector<uint8_t>& qz);
+
 static qlin_status build_spqr(qlin_layer* L, const float* W) {
   const int N = L->N, K = L->K;
   const int G = K / 16, S = K / kSpqrSuper;
@@ -642,8 +645,16 @@ static qlin_status build_spqr(qlin_layer* L, const float* W) {
     }
   });
   if (bad) return QLIN_ERR_INVALID_ARG;
+  build_spqr_image(L, q, qs, qz);
+  return QLIN_OK;
+}
 
-  // device image
+// Device image from the codes q [N][K], qs, qz [N][K/16] and the handle's stats and CSR.
+static void build_spqr_image(qlin_layer* L, const std::vector<uint8_t>& q, const std::vector<uint8_t>& qs,
+                             const std::vector<uint8_t>& qz) {
+  const int N = L->N, K = L->K;
+  const int G = K / 16, S = K / kSpqrSuper;
+  const int64_t nnz = L->nnz;
   const int RG = (N + kRowGroup - 1) / kRowGroup;
   L->RG = RG;
   L->KU = S;
@@ -776,11 +787,12 @@ static qlin_status build_spqr(qlin_layer* L, const float* W) {
       for (int q = 0; q < 8; ++q) e0[q] |= (esc ? 15u : cnt[q]) << 12;
     }
   }
-  return QLIN_OK;
 }
 
 // ------------------------------------------------------------------------------------
 // SmoothQuant W8
+
+static void build_w8_image(qlin_layer* L);
 
 static qlin_status build_w8(qlin_layer* L, const float* W, const float* act_absmax) {
   const int N = L->N, K = L->K;
@@ -823,7 +835,13 @@ static qlin_status build_w8(qlin_layer* L, const float* W, const float* act_absm
     }
   });
   if (bad) return QLIN_ERR_INVALID_ARG;
+  build_w8_image(L);
+  return QLIN_OK;
+}
 
+// Device image from the handle's qw, sw and s_inv.
+static void build_w8_image(qlin_layer* L) {
+  const int N = L->N, K = L->K;
   const int RG = (N + kRowGroup - 1) / kRowGroup, KB = K / kW8Block;
   L->RG = RG;
   L->KU = KB;
@@ -869,7 +887,6 @@ static qlin_status build_w8(qlin_layer* L, const float* W, const float* act_absm
   float* swd = reinterpret_cast<float*>(img + L->sec_sw);
   for (int n = 0; n < RG * kRowGroup; ++n) swd[n] = n < N ? L->sw[n] : 0.f;
   std::memcpy(img + L->sec_sinv, L->s_inv.data(), (size_t)K * 4);
-  return QLIN_OK;
 }
 
 // ------------------------------------------------------------------------------------
@@ -993,6 +1010,126 @@ qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xca
   L->K = K;
   try {
     st = build_w4_gptq(L, W, Xcal, S, damp);
+  } catch (const std::bad_alloc&) {
+    st = QLIN_ERR_INVALID_ARG;
+  }
+  if (st != QLIN_OK) {
+    delete L;
+    return st;
+  }
+  *out = L;
+  return QLIN_OK;
+}
+
+// Checkpoint load: a handle from canonical arrays (the layout qlin_export hands back), checked
+// and turned into the same device image a packer writes -- no quantization happens.
+static inline bool h_finite(uint16_t h) { return (h & 0x7C00u) != 0x7C00u; }
+static inline bool h_small_int(uint16_t h, int maxv) {  // fp16 holding an integer 0..maxv
+  const float v = h2f(h);
+  return h_finite(h) && v >= 0.f && v <= (float)maxv && std::nearbyint(v) == v && !(h & 0x8000u && v == 0.f);
+}
+static inline int get_bits3(const uint8_t* stream, size_t row_off, int idx) {
+  size_t bit = (size_t)3 * idx;
+  int v = 0;
+  for (int b = 0; b < 3; ++b, ++bit) v |= ((stream[row_off + bit / 8] >> (bit % 8)) & 1) << b;
+  return v;
+}
+
+static qlin_status import_w4(qlin_layer* L, const qlin_canonical* c) {
+  const int N = L->N, K = L->K, G = K / kW4Group;
+  if (!c->codes || !c->scale || !c->zero) return QLIN_ERR_INVALID_ARG;
+  for (size_t i = 0; i < (size_t)N * G; ++i) {
+    const uint16_t sc = c->scale[i];
+    if (!h_finite(sc) || (sc & 0x8000u) || (sc & 0x7FFFu) == 0 || !h_small_int(c->zero[i], 15))
+      return QLIN_ERR_INVALID_ARG;
+  }
+  L->scale.assign(c->scale, c->scale + (size_t)N * G);
+  L->zero.assign(c->zero, c->zero + (size_t)N * G);
+  std::vector<uint8_t> q((size_t)N * K);
+  parallel_for(N, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n)
+      for (int k = 0; k < K; ++k) q[(size_t)n * K + k] = (uint8_t)((c->codes[(size_t)n * (K / 8) + k / 8] >> (4 * (k % 8))) & 15u);
+  });
+  build_w4_image(L, q);
+  return QLIN_OK;
+}
+
+static qlin_status import_spqr(qlin_layer* L, const qlin_canonical* c) {
+  const int N = L->N, K = L->K, G = K / 16, S = K / kSpqrSuper;
+  if (!c->codes3 || !c->qs3 || !c->qz3 || !c->stats || !c->rowptr) return QLIN_ERR_INVALID_ARG;
+  if (c->rowptr[0] != 0) return QLIN_ERR_INVALID_ARG;
+  for (int n = 0; n < N; ++n) {
+    if (c->rowptr[n + 1] < c->rowptr[n] || c->rowptr[n + 1] - c->rowptr[n] > K) return QLIN_ERR_INVALID_ARG;
+    for (int32_t p = c->rowptr[n]; p < c->rowptr[n + 1]; ++p) {
+      if (!c->col || !c->val) return QLIN_ERR_INVALID_ARG;
+      if (c->col[p] < 0 || c->col[p] >= K || (p > c->rowptr[n] && c->col[p] <= c->col[p - 1])) return QLIN_ERR_INVALID_ARG;
+      if (!h_finite(c->val[p])) return QLIN_ERR_INVALID_ARG;
+    }
+  }
+  for (size_t i = 0; i < (size_t)N * S; ++i) {
+    const uint16_t* st = c->stats + 4 * i;
+    if (!h_finite(st[0]) || !h_finite(st[2]) || !h_small_int(st[1], 7) || !h_small_int(st[3], 7))
+      return QLIN_ERR_INVALID_ARG;
+  }
+  const int64_t nnz = c->rowptr[N];
+  L->nnz = nnz;
+  L->frac = (float)((double)nnz / ((double)N * K));
+  L->stats.assign(c->stats, c->stats + (size_t)N * S * 4);
+  L->rowptr.assign(c->rowptr, c->rowptr + N + 1);
+  L->col.assign(c->col ? c->col : nullptr, c->col ? c->col + nnz : nullptr);
+  L->val.assign(c->val ? c->val : nullptr, c->val ? c->val + nnz : nullptr);
+  const size_t cb = (size_t)3 * K / 8, sb = (size_t)3 * G / 8;
+  L->codes3.assign(c->codes3, c->codes3 + (size_t)N * cb);
+  L->qs3.assign(c->qs3, c->qs3 + (size_t)N * sb);
+  L->qz3.assign(c->qz3, c->qz3 + (size_t)N * sb);
+  std::vector<uint8_t> q((size_t)N * K), qs((size_t)N * G), qz((size_t)N * G);
+  parallel_for(N, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n) {
+      for (int k = 0; k < K; ++k) q[(size_t)n * K + k] = (uint8_t)get_bits3(c->codes3, n * cb, k);
+      for (int g = 0; g < G; ++g) {
+        qs[(size_t)n * G + g] = (uint8_t)get_bits3(c->qs3, n * sb, g);
+        qz[(size_t)n * G + g] = (uint8_t)get_bits3(c->qz3, n * sb, g);
+      }
+    }
+  });
+  build_spqr_image(L, q, qs, qz);
+  return QLIN_OK;
+}
+
+static qlin_status import_w8(qlin_layer* L, const qlin_canonical* c) {
+  const int N = L->N, K = L->K;
+  if (!c->qw || !c->sw || !c->s || !c->s_inv) return QLIN_ERR_INVALID_ARG;
+  for (size_t i = 0; i < (size_t)N * K; ++i)
+    if (c->qw[i] < -127) return QLIN_ERR_INVALID_ARG;
+  for (int n = 0; n < N; ++n)
+    if (!is_finite_f(c->sw[n]) || !(c->sw[n] > 0.f)) return QLIN_ERR_INVALID_ARG;
+  for (int k = 0; k < K; ++k)
+    if (!is_finite_f(c->s[k]) || !(c->s[k] > 0.f) || !is_finite_f(c->s_inv[k]) || !(c->s_inv[k] > 0.f))
+      return QLIN_ERR_INVALID_ARG;
+  L->qw.assign(c->qw, c->qw + (size_t)N * K);
+  L->sw.assign(c->sw, c->sw + N);
+  L->s.assign(c->s, c->s + K);
+  L->s_inv.assign(c->s_inv, c->s_inv + K);
+  build_w8_image(L);
+  return QLIN_OK;
+}
+
+qlin_status qlin_import(int format, int N, int K, const qlin_canonical* in, qlin_handle* out) {
+  if (!out) return QLIN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!in || N <= 0 || K <= 0) return QLIN_ERR_INVALID_ARG;
+  if (format == QLIN_FMT_W4G128 && K % kW4Group) return QLIN_ERR_INVALID_ARG;
+  if (format == QLIN_FMT_SPQR && (K % kSpqrSuper || K > 32768)) return QLIN_ERR_INVALID_ARG;
+  if (format == QLIN_FMT_W8A8 && K % kW8Block) return QLIN_ERR_INVALID_ARG;
+  if (format != QLIN_FMT_W4G128 && format != QLIN_FMT_SPQR && format != QLIN_FMT_W8A8) return QLIN_ERR_INVALID_ARG;
+  qlin_layer* L = nullptr;
+  QLIN_TRY_ALLOC(L = new qlin_layer());
+  L->format = format;
+  L->N = N;
+  L->K = K;
+  qlin_status st = QLIN_ERR_INVALID_ARG;
+  try {
+    st = format == QLIN_FMT_W4G128 ? import_w4(L, in) : format == QLIN_FMT_SPQR ? import_spqr(L, in) : import_w8(L, in);
   } catch (const std::bad_alloc&) {
     st = QLIN_ERR_INVALID_ARG;
   }

@@ -85,6 +85,27 @@ def test_w4_gptq_layer(qlin, M):
     _check(_y(layer, X, M), X, ref["w_hat"])
 
 
+@pytest.mark.parametrize("kind", ["w4", "spqr", "w8a8"])
+def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
+    """A layer saved and loaded back (qlin_import, no requantization) gives the same outputs
+    bit for bit as the layer that was saved, decode and prefill."""
+    N, K = 160, 1024
+    if kind == "w4":
+        W, X = synth.gptq_layer(N, K, 40, seed=41)
+        L = qlin.QLinear.from_w4g128(W)
+    elif kind == "spqr":
+        W, X = synth.spqr_layer(N, K, 40, seed=41)
+        L = qlin.QLinear.from_spqr(W, 0.02)
+    else:
+        W, X, absmax, _ = synth.smoothquant_layer(N, K, 40, seed=41)
+        L = qlin.QLinear.from_w8(W, absmax, 0.85)
+    L.save(tmp_path / "layer.npz")
+    L2 = qlin.QLinear.load(tmp_path / "layer.npz")
+    a, b = L.to("cuda", max_M=40), L2.to("cuda", max_M=40)
+    for M in (1, 40):
+        assert np.array_equal(_y(a, X[:M], M).view(np.uint32), _y(b, X[:M], M).view(np.uint32))
+
+
 # ----------------------------------------------------------------------------- SpQR
 
 @pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (64, 256, 0.0)])
