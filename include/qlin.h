@@ -78,6 +78,9 @@ typedef struct {
  *          qs3, qz3 uint8 [N][3(K/16)/8] same stream form, stats fp16 [N][K/256][4] =
  *          (ss, zs, sz, zz), rowptr int32 [N+1], col int16 [nnz], val fp16 [nnz].
  *  W8A8:   qw int8 [N][K], sw fp32 [N], s fp32 [K], s_inv fp32 [K].
+ *  W4G128 act-order (qlin_pack_w4g128_gptq with act_order): perm int32 [K], a permutation of
+ *          0..K-1; the codes, scales and zeros are those of the layer W[:, perm] (column j is
+ *          input channel perm[j]) and the forward multiplies by X[:, perm].  NULL otherwise.
  * fp16 values are passed as uint16_t bit patterns. */
 typedef struct {
   const uint32_t* codes;
@@ -94,6 +97,7 @@ typedef struct {
   const float* sw;
   const float* s;
   const float* s_inv;
+  const int32_t* perm;
 } qlin_canonical;
 
 /* ---- checkpoint load (host) --------------------------------------------------------- */
@@ -108,7 +112,8 @@ typedef struct {
  * may be NULL when nnz == 0).  Checked: shapes as for the packers; W4 scales positive finite,
  * zeros integers 0..15; SpQR stats finite with integer zs, zz in 0..7, rowptr starting at 0 and
  * non-decreasing with at most K entries per row, columns strictly ascending in [0, K), values
- * finite; W8 qw >= -127, sw, s, s_inv positive finite.  Anything else: INVALID_ARG.  The
+ * finite; W4 perm (optional) a permutation of 0..K-1; W8 qw >= -127, sw, s, s_inv positive
+ * finite.  Anything else: INVALID_ARG.  The
  * info fields alpha (W8A8) and outlier_frac (SpQR: nnz / (N K)) are informational. */
 qlin_status qlin_import(int format, int N, int K, const qlin_canonical* in, qlin_handle* out);
 
@@ -129,12 +134,18 @@ qlin_status qlin_pack_w4g128(const float* W, int N, int K, qlin_handle* out);
  * group's current weights (fp32); column k gets the round-to-nearest code with them, and
  * every later weight of the row moves by -e * U_kj, e = (w_k - w_hat_k) / U_kk (fp64).
  * With H = I the result equals qlin_pack_w4g128's bit for bit.
+ * act_order != 0 (same page, last paragraph: columns ordered by activation size, groups then
+ * irregular in the original order): the columns are taken by decreasing diag(H) (an
+ * always-zero input counted as 1, ties to the smaller index) and W[:, perm] is quantized as
+ * above under H[perm][perm]; the handle keeps perm (exported and imported with the codes),
+ * and every forward first gathers X[:, perm] into the workspace (one more kernel launch, the
+ * run-time price the page mentions; M <= the workspace's max_M).
  * W: host fp32 [N][K]; Xcal: host fp32 [S][K] calibration inputs (row-major); both read only,
  * not retained.  K % 128 == 0, K <= 8192 (H and its factors are K x K fp64 on the host),
  * S >= 1, damp > 0 (0.01 is the usual value), W and Xcal finite.  Returns INVALID_ARG on bad
  * shapes/values or if H + damping is not positive definite; the work is O(K^3 + N K^2). */
 qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xcal, int S, double damp,
-                                  qlin_handle* out);
+                                  int act_order, qlin_handle* out);
 
 /* SpQR 3-bit g16 bi-level + fp16 CSR outliers (SpQR page, see above).  The outliers are
  * the floor(f*N*K) largest |w| (ties: smaller linear index), standing in for the page's

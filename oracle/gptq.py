@@ -31,6 +31,13 @@ The page names the steps, not the formulae.  Readings taken:
 
 With H = I, every U_kj with j > k is 0, no weight moves, and the codes are the
 round-to-nearest codes bit for bit.
+
+Act-order (GPTQ page, "İddia ve Gerçeklik: GPTQ", last paragraph: columns sorted by
+activation size, at the price of irregular groups at run time).  Reading: the column order
+is perm = the columns by decreasing diag(H) (after reading 2, ties to the smaller index);
+the layer W[:, perm] is quantized as above under H[perm][:, perm], so its 128-groups are
+contiguous in the permuted order; the forward then multiplies by X[:, perm].  With diag(H)
+already non-increasing, perm is the identity and nothing changes.
 """
 import numpy as np
 
@@ -91,11 +98,31 @@ def quantize(W, H, damp: float = 0.01):
     return q, scale, zero
 
 
-def pack(W, Xcal, damp: float = 0.01):
-    """Canonical arrays (as oracle.gptq_w4.pack) plus the fp32 dequantized matrix."""
-    q, s, z = quantize(W, hessian(Xcal), damp)
-    return {"codes": gptq_w4.pack_codes(q), "scale": s, "zero": z, "q": q,
-            "w_hat": gptq_w4.dequantize(q, s, z)}
+def act_order(H) -> np.ndarray:
+    """perm: the columns by decreasing diag(H), dead columns counted as 1, ties to the smaller index."""
+    d = np.array(np.diag(np.asarray(H, dtype=np.float64)))
+    d[d == 0] = 1.0
+    return np.argsort(-d, kind="stable").astype(np.int32)
+
+
+def pack(W, Xcal, damp: float = 0.01, act: bool = False):
+    """Canonical arrays (as oracle.gptq_w4.pack) plus the fp32 dequantized matrix.
+
+    act: act-order; then codes/scale/zero are those of W[:, perm], "perm" is returned, and
+    "w_hat" is in the original column order (w_hat[:, perm] = the permuted dequantization).
+    """
+    H = hessian(Xcal)
+    if not act:
+        q, s, z = quantize(W, H, damp)
+        return {"codes": gptq_w4.pack_codes(q), "scale": s, "zero": z, "q": q,
+                "w_hat": gptq_w4.dequantize(q, s, z)}
+    perm = act_order(H)
+    q, s, z = quantize(np.asarray(W, dtype=np.float32)[:, perm], H[np.ix_(perm, perm)], damp)
+    w_perm = gptq_w4.dequantize(q, s, z)
+    w_hat = np.empty_like(w_perm)
+    w_hat[:, perm] = w_perm
+    return {"codes": gptq_w4.pack_codes(q), "scale": s, "zero": z, "q": q, "perm": perm,
+            "w_hat_perm": w_perm, "w_hat": w_hat}
 
 
 def output_error(W, w_hat, Xcal) -> float:

@@ -58,7 +58,7 @@ class LayerInfo(ctypes.Structure):
 
 class Canonical(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("codes", "scale", "zero", "codes3", "qs3", "qz3", "stats", "rowptr",
-                                               "col", "val", "qw", "sw", "s", "s_inv")]
+                                               "col", "val", "qw", "sw", "s", "s_inv", "perm")]
 
 
 _lock = threading.Lock()
@@ -79,7 +79,7 @@ def lib() -> ctypes.CDLL:
         H = ctypes.c_void_p
         sig = {
             "qlin_pack_w4g128": ([vp, i32, i32, ctypes.POINTER(H)], i32),
-            "qlin_pack_w4g128_gptq": ([vp, i32, i32, vp, i32, ctypes.c_double, ctypes.POINTER(H)], i32),
+            "qlin_pack_w4g128_gptq": ([vp, i32, i32, vp, i32, ctypes.c_double, i32, ctypes.POINTER(H)], i32),
             "qlin_pack_spqr": ([vp, i32, i32, f32, ctypes.POINTER(H)], i32),
             "qlin_pack_w8": ([vp, i32, i32, vp, f32, ctypes.POINTER(H)], i32),
             "qlin_device_bytes": ([H, ctypes.POINTER(sz)], i32),
@@ -181,14 +181,14 @@ def qlin_pack_w4g128(W) -> Handle:
     return Handle(h)
 
 
-def qlin_pack_w4g128_gptq(W, Xcal, damp: float = 0.01) -> Handle:
+def qlin_pack_w4g128_gptq(W, Xcal, damp: float = 0.01, act_order: bool = False) -> Handle:
     W = _f32(W)
     X = _f32(Xcal)
     if X.ndim != 2 or X.shape[1] != W.shape[1]:
         raise ValueError("Xcal must be [S, K] with the layer's K")
     h = ctypes.c_void_p()
     _check(lib().qlin_pack_w4g128_gptq(_vp(W), W.shape[0], W.shape[1], _vp(X), X.shape[0], float(damp),
-                                       ctypes.byref(h)), "qlin_pack_w4g128_gptq")
+                                       int(bool(act_order)), ctypes.byref(h)), "qlin_pack_w4g128_gptq")
     return Handle(h)
 
 
@@ -286,9 +286,12 @@ def qlin_export(h: Handle) -> dict:
         return np.frombuffer(buf, dtype=dtype).reshape(shape).copy()
 
     if inf.format == FMT_W4G128:
-        return {"codes": arr(c.codes, np.uint32, (N, K // 8)),
-                "scale": arr(c.scale, np.uint16, (N, K // 128)).view(np.float16),
-                "zero": arr(c.zero, np.uint16, (N, K // 128)).view(np.float16)}
+        out = {"codes": arr(c.codes, np.uint32, (N, K // 8)),
+               "scale": arr(c.scale, np.uint16, (N, K // 128)).view(np.float16),
+               "zero": arr(c.zero, np.uint16, (N, K // 128)).view(np.float16)}
+        if c.perm:  # act-order
+            out["perm"] = arr(c.perm, np.int32, (K,))
+        return out
     if inf.format == FMT_SPQR:
         return {"codes": arr(c.codes3, np.uint8, (N, 3 * K // 8)),
                 "qs_bits": arr(c.qs3, np.uint8, (N, 3 * (K // 16) // 8)),
@@ -320,6 +323,9 @@ def qlin_import(fmt: int, N: int, K: int, arrays: dict) -> Handle:
     ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p).value if a.size else None
     if fmt == FMT_W4G128:
         c.codes, c.scale, c.zero = ptr(keep["codes"]), ptr(keep["scale"]), ptr(keep["zero"])
+        if arrays.get("perm") is not None:  # act-order
+            keep["perm"] = np.ascontiguousarray(arrays["perm"], dtype=np.int32)
+            c.perm = ptr(keep["perm"])
     elif fmt == FMT_SPQR:
         c.codes3, c.qs3, c.qz3 = ptr(keep["codes"]), ptr(keep["qs_bits"]), ptr(keep["qz_bits"])
         c.stats, c.rowptr, c.col, c.val = ptr(keep["stats"]), ptr(keep["rowptr"]), ptr(keep["col"]), ptr(keep["val"])
@@ -348,8 +354,8 @@ class QLinear:
         return cls(qlin_pack_w4g128(W))
 
     @classmethod
-    def from_w4g128_gptq(cls, W, Xcal, damp: float = 0.01):
-        return cls(qlin_pack_w4g128_gptq(W, Xcal, damp))
+    def from_w4g128_gptq(cls, W, Xcal, damp: float = 0.01, act_order: bool = False):
+        return cls(qlin_pack_w4g128_gptq(W, Xcal, damp, act_order))
 
     @classmethod
     def from_spqr(cls, W, outlier_frac: float = 0.01):
@@ -425,7 +431,10 @@ class QLinear:
         """A layer from a checkpoint written by save(); the weights are not requantized."""
         with np.load(path) as z:
             fmt, N, K = int(z["format"]), int(z["N"]), int(z["K"])
-            return cls(qlin_import(fmt, N, K, {k: z[k] for k in _CANONICAL.get(fmt, {})}))
+            arrays = {k: z[k] for k in _CANONICAL.get(fmt, {})}
+            if "perm" in z.files:
+                arrays["perm"] = z["perm"]
+            return cls(qlin_import(fmt, N, K, arrays))
 
 
 def build(force: bool = False) -> str:

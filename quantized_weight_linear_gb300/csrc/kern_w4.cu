@@ -242,6 +242,87 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
 
 }  // namespace
 
+namespace {
+
+// Act-order layers (GPTQ page, "İddia ve Gerçeklik: GPTQ", last paragraph): the codes are in
+// the permuted column order, so the activations are gathered into it first,
+// Xp[m][j] = X[m][perm[j]], eight channels per thread and one 16-byte store.
+__global__ void __launch_bounds__(256)
+    w4_gather_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, uint16_t* __restrict__ Xp, int K) {
+  pdl_wait();  // the previous kernel on the stream may still read Xp
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int m = blockIdx.y;
+  const int j0 = 8 * (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  if (j0 >= K) return;
+  const uint16_t* xr = X + (int64_t)m * K;
+  const int4 p0 = *reinterpret_cast<const int4*>(perm + j0);
+  const int4 p1 = *reinterpret_cast<const int4*>(perm + j0 + 4);
+  const uint4 o = make_uint4((uint32_t)xr[p0.x] | ((uint32_t)xr[p0.y] << 16), (uint32_t)xr[p0.z] | ((uint32_t)xr[p0.w] << 16),
+                             (uint32_t)xr[p1.x] | ((uint32_t)xr[p1.y] << 16), (uint32_t)xr[p1.z] | ((uint32_t)xr[p1.w] << 16));
+  *reinterpret_cast<uint4*>(Xp + (int64_t)m * K + j0) = o;
+}
+
+// The same with the token's row staged in shared memory first (one coalesced read of the row,
+// then the permuted reads from shared memory): one CTA per token, K * 2 bytes of smem.
+__global__ void __launch_bounds__(256)
+    w4_gather_row_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, uint16_t* __restrict__ Xp,
+                         int K) {
+  extern __shared__ __align__(16) uint16_t xrow[];
+  pdl_wait();  // the previous kernel on the stream may still read Xp
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int m = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)m * K);
+  for (int i = threadIdx.x; i < K / 8; i += blockDim.x) reinterpret_cast<uint4*>(xrow)[i] = src[i];
+  __syncthreads();
+  for (int j0 = 8 * threadIdx.x; j0 < K; j0 += 8 * blockDim.x) {
+    const int4 p0 = *reinterpret_cast<const int4*>(perm + j0);
+    const int4 p1 = *reinterpret_cast<const int4*>(perm + j0 + 4);
+    const uint4 o = make_uint4((uint32_t)xrow[p0.x] | ((uint32_t)xrow[p0.y] << 16),
+                               (uint32_t)xrow[p0.z] | ((uint32_t)xrow[p0.w] << 16),
+                               (uint32_t)xrow[p1.x] | ((uint32_t)xrow[p1.y] << 16),
+                               (uint32_t)xrow[p1.z] | ((uint32_t)xrow[p1.w] << 16));
+    *reinterpret_cast<uint4*>(Xp + (int64_t)m * K + j0) = o;
+  }
+}
+
+constexpr int kGatherRowMaxK = 96 * 1024;  // K * 2 bytes of shared memory per CTA
+
+}  // namespace
+
+int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M, int K, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  if (K <= kGatherRowMaxK) {
+    static int attr_k = 0;  // largest K the smem attribute has been raised for
+    const size_t smem = (size_t)K * 2;
+    if (smem > 48 * 1024 && K > attr_k) {
+      const cudaError_t e = cudaFuncSetAttribute(w4_gather_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+      if (e != cudaSuccess) return (int)e;
+      attr_k = K;
+    }
+    cfg.gridDim = dim3((unsigned)M);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, w4_gather_row_kernel, X, perm, Xp, K);
+  }
+  cfg.gridDim = dim3((unsigned)((K / 8 + 255) / 256), (unsigned)M);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, w4_gather_kernel, X, perm, Xp, K);
+}
+
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
   grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms);

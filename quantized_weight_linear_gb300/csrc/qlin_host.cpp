@@ -172,6 +172,7 @@ struct qlin_layer {
   // canonical arrays
   std::vector<uint32_t> codes;
   std::vector<uint16_t> scale, zero;
+  std::vector<int32_t> perm;  // W4 act-order: permuted column j is input channel perm[j] (empty: none)
   std::vector<uint8_t> codes3, qs3, qz3;
   std::vector<uint16_t> stats;
   std::vector<int32_t> rowptr;
@@ -181,7 +182,7 @@ struct qlin_layer {
   std::vector<float> sw, s, s_inv;
   // device image and its sections
   std::vector<uint8_t> image;
-  size_t sec_units = 0, sec_offs = 0, sec_ents = 0, sec_sw = 0, sec_sinv = 0;
+  size_t sec_units = 0, sec_offs = 0, sec_ents = 0, sec_sw = 0, sec_sinv = 0, sec_perm = 0;
   int RG = 0, KU = 0;  // row groups, K units per row group
   // bound state
   uint8_t* dev = nullptr;
@@ -259,8 +260,11 @@ static void build_w4_image(qlin_layer* L, const std::vector<uint8_t>& q) {
   L->RG = RG;
   L->KU = G;
   L->sec_units = 0;
-  L->image.assign(align256((size_t)RG * G * kW4UnitBytes), 0);
+  const size_t units_bytes = align256((size_t)RG * G * kW4UnitBytes);
+  L->sec_perm = units_bytes;
+  L->image.assign(units_bytes + (L->perm.empty() ? 0 : align256((size_t)K * 4)), 0);
   uint8_t* img = L->image.data();
+  if (!L->perm.empty()) std::memcpy(img + L->sec_perm, L->perm.data(), (size_t)K * 4);
   parallel_for(RG, [&](int64_t b, int64_t e) {
     for (int64_t rg = b; rg < e; ++rg) {
       for (int g = 0; g < G; ++g) {
@@ -369,7 +373,8 @@ static bool gptq_inverse_factor(std::vector<double>& H, int K, std::vector<doubl
   return true;
 }
 
-static qlin_status build_w4_gptq(qlin_layer* L, const float* W, const float* Xcal, int S, double damp) {
+static qlin_status build_w4_gptq(qlin_layer* L, const float* W, const float* Xcal, int S, double damp,
+                                 bool act_order) {
   const int N = L->N, K = L->K, G = K / kW4Group;
   // H = Xcal^T Xcal over the calibration rows, in row order
   std::vector<double> H((size_t)K * K, 0.0);
@@ -383,6 +388,29 @@ static qlin_status build_w4_gptq(qlin_layer* L, const float* W, const float* Xca
         for (int j = 0; j < K; ++j) Hi[j] += xi * (double)x[j];
       }
   });
+  // act-order (GPTQ page, "İddia ve Gerçeklik: GPTQ", last paragraph): columns by decreasing
+  // diag(H) (an always-zero input counted as 1), ties to the smaller index; the permuted layer
+  // W[:, perm] is quantized under H[perm][perm], so its 128-groups are contiguous in that order
+  std::vector<float> Wp;
+  if (act_order) {
+    std::vector<double> d(K);
+    for (int k = 0; k < K; ++k) d[k] = H[(size_t)k * K + k] == 0.0 ? 1.0 : H[(size_t)k * K + k];
+    L->perm.resize(K);
+    for (int k = 0; k < K; ++k) L->perm[k] = k;
+    std::stable_sort(L->perm.begin(), L->perm.end(), [&](int32_t a, int32_t b) { return d[a] > d[b]; });
+    std::vector<double> Hp((size_t)K * K);
+    parallel_for(K, [&](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i)
+        for (int j = 0; j < K; ++j) Hp[(size_t)i * K + j] = H[(size_t)L->perm[i] * K + L->perm[j]];
+    });
+    H.swap(Hp);
+    Wp.resize((size_t)N * K);
+    parallel_for(N, [&](int64_t b, int64_t e) {
+      for (int64_t n = b; n < e; ++n)
+        for (int j = 0; j < K; ++j) Wp[(size_t)n * K + j] = W[(size_t)n * K + L->perm[j]];
+    });
+    W = Wp.data();
+  }
   std::vector<uint8_t> dead(K, 0);
   double diag = 0.0;
   for (int k = 0; k < K; ++k) {
@@ -929,7 +957,9 @@ static WsLayout ws_layout(const qlin_layer* L, int maxM) {
   w.tagged = w.counters + align256((size_t)L->RG * 4);
   w.qx = w.tagged + align256((size_t)grid * 2 * kRowGroup * 4 * 8);
   size_t qx_bytes = 0, sx_bytes = 0;
-  if (L->format == QLIN_FMT_W8A8) {
+  if (L->format == QLIN_FMT_W4G128 && !L->perm.empty()) {
+    qx_bytes = align256((size_t)std::max(maxM, 1) * L->K * 2);  // act-order: X in permuted channel order
+  } else if (L->format == QLIN_FMT_W8A8) {
     // row-major codes for the prefill GEMM, or the decode GEMV's blocked [K/64][M][72] (M <= 16)
     qx_bytes = align256(std::max((size_t)std::max(maxM, 1) * L->K * 2,
                                  (size_t)(L->K / 64) * std::min(std::max(maxM, 1), 16) * 72 * 2));
@@ -994,7 +1024,7 @@ qlin_status qlin_pack_w4g128(const float* W, int N, int K, qlin_handle* out) {
 }
 
 qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xcal, int S, double damp,
-                                  qlin_handle* out) {
+                                  int act_order, qlin_handle* out) {
   if (!out) return QLIN_ERR_INVALID_ARG;
   *out = nullptr;
   if (K % kW4Group || K > kGptqMaxK || !Xcal || S <= 0 || !(damp > 0.0) || !std::isfinite(damp))
@@ -1009,7 +1039,7 @@ qlin_status qlin_pack_w4g128_gptq(const float* W, int N, int K, const float* Xca
   L->N = N;
   L->K = K;
   try {
-    st = build_w4_gptq(L, W, Xcal, S, damp);
+    st = build_w4_gptq(L, W, Xcal, S, damp, act_order != 0);
   } catch (const std::bad_alloc&) {
     st = QLIN_ERR_INVALID_ARG;
   }
@@ -1042,6 +1072,15 @@ static qlin_status import_w4(qlin_layer* L, const qlin_canonical* c) {
     const uint16_t sc = c->scale[i];
     if (!h_finite(sc) || (sc & 0x8000u) || (sc & 0x7FFFu) == 0 || !h_small_int(c->zero[i], 15))
       return QLIN_ERR_INVALID_ARG;
+  }
+  if (c->perm) {  // act-order: must be a permutation of 0..K-1
+    std::vector<uint8_t> seen(K, 0);
+    for (int j = 0; j < K; ++j) {
+      const int32_t v = c->perm[j];
+      if (v < 0 || v >= K || seen[v]) return QLIN_ERR_INVALID_ARG;
+      seen[v] = 1;
+    }
+    L->perm.assign(c->perm, c->perm + K);
   }
   L->scale.assign(c->scale, c->scale + (size_t)N * G);
   L->zero.assign(c->zero, c->zero + (size_t)N * G);
@@ -1256,7 +1295,7 @@ static qlin_status check_forward(qlin_handle h, const void* X, const void* Y, in
   if (M == 0) return QLIN_OK;
   if (!X || !Y || ((uintptr_t)X & 15u) || ((uintptr_t)Y & 15u)) return QLIN_ERR_INVALID_ARG;
   if (!h->dev) return QLIN_ERR_NOT_BOUND;
-  if (!h->ws || (h->format == QLIN_FMT_W8A8 && M > h->ws_maxM)) return QLIN_ERR_WORKSPACE;
+  if (!h->ws || ((h->format == QLIN_FMT_W8A8 || !h->perm.empty()) && M > h->ws_maxM)) return QLIN_ERR_WORKSPACE;
   return QLIN_OK;
 }
 
@@ -1265,7 +1304,12 @@ static qlin_status run_decode(qlin_handle h, const uint16_t* X, uint16_t* Y, int
   int e = 0;
   switch (h->format) {
     case QLIN_FMT_W4G128:
-      e = launch_w4_decode(w4view(h), X, Y, M, h->wsv, h->grid, s);
+      if (!h->perm.empty()) {  // act-order: gather X's channels into the permuted order first
+        uint16_t* xp = reinterpret_cast<uint16_t*>(h->wsv.qx);
+        e = launch_w4_gather(X, reinterpret_cast<const int32_t*>(h->dev + h->sec_perm), xp, M, h->K, s);
+        X = xp;
+      }
+      if (!e) e = launch_w4_decode(w4view(h), X, Y, M, h->wsv, h->grid, s);
       break;
     case QLIN_FMT_SPQR:
       e = launch_spqr_decode(spqrview(h), X, Y, M, h->wsv, h->grid, s);
@@ -1287,7 +1331,12 @@ static qlin_status run_prefill(qlin_handle h, const uint16_t* X, uint16_t* Y, in
   int e = 0;
   switch (h->format) {
     case QLIN_FMT_W4G128:
-      e = launch_w4_prefill(w4view(h), X, Y, M, h->wsv.status, s);
+      if (!h->perm.empty()) {
+        uint16_t* xp = reinterpret_cast<uint16_t*>(h->wsv.qx);
+        e = launch_w4_gather(X, reinterpret_cast<const int32_t*>(h->dev + h->sec_perm), xp, M, h->K, s);
+        X = xp;
+      }
+      if (!e) e = launch_w4_prefill(w4view(h), X, Y, M, h->wsv.status, s);
       break;
     case QLIN_FMT_SPQR:
       e = launch_spqr_prefill(spqrview(h), X, Y, M, h->wsv.status, s);
@@ -1395,6 +1444,7 @@ qlin_status qlin_export(qlin_handle h, qlin_canonical* o) {
   o->sw = p(h->sw);
   o->s = p(h->s);
   o->s_inv = p(h->s_inv);
+  o->perm = p(h->perm);
   return QLIN_OK;
 }
 
@@ -1408,7 +1458,7 @@ qlin_status qlin_info(qlin_handle h, qlin_layer_info* o) {
   const int64_t N = h->N, K = h->K;
   int64_t pb = 0;
   switch (h->format) {
-    case QLIN_FMT_W4G128: pb = N * K / 2 + N * (K / kW4Group) * 4; break;
+    case QLIN_FMT_W4G128: pb = N * K / 2 + N * (K / kW4Group) * 4 + 4 * (int64_t)h->perm.size(); break;
     case QLIN_FMT_SPQR:
       pb = N * (3 * K / 8) + 2 * N * (3 * (K / 16) / 8) + N * (K / kSpqrSuper) * 8 + 4 * (N + 1) + 4 * h->nnz;
       break;

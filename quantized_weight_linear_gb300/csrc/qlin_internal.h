@@ -106,6 +106,8 @@ constexpr int kMaxCtasPerSm = 4;  // decode kernels run up to 4 CTAs per SM
 // ---- kernel launchers (kern_*.cu); all asynchronous, return cudaError_t as int ----
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws,
                      int grid, void* stream);
+// act-order W4: Xp[m][j] = X[m][perm[j]] (K % 8 == 0, 16-byte aligned rows)
+int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M, int K, void* stream);
 int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M,
                        const Workspace& ws, int grid, void* stream);
 int launch_w8_act_quant(const W8View& v, const uint16_t* X, int8_t* qx, float* sx, int M,

@@ -18,6 +18,7 @@ def _layers(qlin):
     return {
         "w4": lambda: qlin.QLinear.from_w4g128(W),
         "w4_gptq": lambda: qlin.QLinear.from_w4g128_gptq(Wg, synth.gptq_calibration(64, 256, seed=5)),
+        "w4_act": lambda: qlin.QLinear.from_w4g128_gptq(Wg, synth.gptq_calibration(64, 256, seed=5), act_order=True),
         "spqr_0": lambda: qlin.QLinear.from_spqr(W, 0.0),
         "spqr_1": lambda: qlin.QLinear.from_spqr(W, 0.01),
         "spqr_2": lambda: qlin.QLinear.from_spqr(W, 0.02),
@@ -25,7 +26,7 @@ def _layers(qlin):
     }
 
 
-@pytest.mark.parametrize("kind", ["w4", "w4_gptq", "spqr_0", "spqr_1", "spqr_2", "w8a8"])
+@pytest.mark.parametrize("kind", ["w4", "w4_gptq", "w4_act", "spqr_0", "spqr_1", "spqr_2", "w8a8"])
 def test_round_trip(qlin, kind, tmp_path):
     L = _layers(qlin)[kind]()
     ex = L.export()
@@ -54,6 +55,11 @@ def test_rejects_w4_arrays_no_packer_writes(qlin):
         bad[field][3, 1] = value
         _reject(qlin, qlin.FMT_W4G128, N, K, bad)
     _reject(qlin, qlin.FMT_W4G128, N, 200, ex)  # K % 128
+    act = _layers(qlin)["w4_act"]()
+    ea = act.export()
+    bad = {k: v.copy() for k, v in ea.items()}
+    bad["perm"][1] = bad["perm"][0]  # not a permutation
+    _reject(qlin, qlin.FMT_W4G128, act.N, act.K, bad)
 
 
 def test_rejects_spqr_arrays_no_packer_writes(qlin):

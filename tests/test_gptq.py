@@ -115,3 +115,46 @@ def test_packer_rejects_bad_arguments(qlin):
     big = np.zeros((2, 8320), dtype=np.float32)
     with pytest.raises(qlin.QlinError):
         qlin.qlin_pack_w4g128_gptq(big, big)  # K > 8192
+
+
+# ----------------------------------------------------------------------------- act-order
+
+def _uneven(X):
+    """Channel scales 1/4 .. 4 (powers of two keep X^T X exact)."""
+    K = X.shape[1]
+    return (X * (2.0 ** (np.arange(K) % 5 - 2))[None, :]).astype(np.float32)
+
+
+def test_act_order_sorts_by_decreasing_diagonal():
+    H = np.diag([3.0, 5.0, 0.0, 5.0, 2.0, 1.0])  # the dead input counts as 1; 5 vs 5 keeps index order
+    assert list(gptq.act_order(H)) == [1, 3, 0, 4, 2, 5]
+
+
+def test_act_order_is_invariant_to_input_order():
+    """Relabelling the input channels of W and of the calibration rows relabels W_hat the same
+    way: the order comes from diag(H) alone, and the codes follow their channels."""
+    N, K, S = 40, 256, 300
+    W = synth.normal(12, synth.KEY_W, 0.02, (N, K))
+    X = _uneven(synth.gptq_calibration(S, K, seed=12))
+    P = np.random.default_rng(12).permutation(K)
+    a = gptq.pack(W, X, act=True)
+    b = gptq.pack(W[:, P], X[:, P], act=True)
+    assert np.array_equal(b["w_hat"].view(np.uint32), a["w_hat"][:, P].view(np.uint32))
+
+
+def test_act_order_lowers_error_with_uneven_channels():
+    N, K, S = 64, 256, 256
+    W = synth.normal(7, synth.KEY_W, 0.02, (N, K))
+    X = _uneven(synth.gptq_calibration(S, K, seed=7))
+    act, plain = gptq.pack(W, X, act=True), gptq.pack(W, X)
+    assert gptq.output_error(W, act["w_hat"], X) < 0.8 * gptq.output_error(W, plain["w_hat"], X)
+
+
+@pytest.mark.parametrize("N,K,S", [(64, 256, 256), (100, 512, 300)])
+def test_packer_matches_oracle_act_order(qlin, N, K, S):
+    W = synth.normal(7, synth.KEY_W, 0.02, (N, K))
+    X = _uneven(synth.gptq_calibration(S, K, seed=7))
+    ex = qlin.qlin_export(qlin.qlin_pack_w4g128_gptq(W, X, act_order=True))
+    ref = gptq.pack(W, X, act=True)
+    for key in ("codes", "scale", "zero", "perm"):
+        assert np.array_equal(np.asarray(ex[key]).view(np.uint8), np.asarray(ref[key]).view(np.uint8)), key

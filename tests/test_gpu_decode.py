@@ -69,23 +69,27 @@ def test_w4_one_hot_rows_bit_exact(qlin):
         assert np.array_equal(y[i], bf16_round(w_hat[:, k]))
 
 
+@pytest.mark.parametrize("act", [False, True])
 @pytest.mark.parametrize("M", [1, 16, 40])
-def test_w4_gptq_layer(qlin, M):
+def test_w4_gptq_layer(qlin, M, act):
     """GPTQ-packed codes (error-compensated, same W4 g128 format): the same kernels read
-    them; dequantized weights bit-exact, outputs within tolerance (M = 40: prefill)."""
+    them; dequantized weights bit-exact, outputs within tolerance (M = 40: prefill).  With
+    act-order the codes are in the permuted column order and the forward gathers X[:, perm]
+    first."""
     from oracle import gptq
     N, K = 192, 1024
     W = synth.normal(21, synth.KEY_W, 0.02, (N, K))
     Xcal = synth.gptq_calibration(256, K, seed=21)
-    layer = qlin.QLinear.from_w4g128_gptq(W, Xcal).to("cuda")
-    ref = gptq.pack(W, Xcal)
+    Xcal = (Xcal * (2.0 ** (np.arange(K) % 5 - 2))[None, :]).astype(np.float32)
+    layer = qlin.QLinear.from_w4g128_gptq(W, Xcal, act_order=act).to("cuda", max_M=40)
+    ref = gptq.pack(W, Xcal, act=act)
     wd = layer.dequant_device().cpu().numpy()
-    assert np.array_equal(wd.view(np.uint32), ref["w_hat"].view(np.uint32))
+    assert np.array_equal(wd.view(np.uint32), ref["w_hat_perm" if act else "w_hat"].view(np.uint32))
     X = synth.activations_bf16(21, M, K)
     _check(_y(layer, X, M), X, ref["w_hat"])
 
 
-@pytest.mark.parametrize("kind", ["w4", "spqr", "w8a8"])
+@pytest.mark.parametrize("kind", ["w4", "w4_act", "spqr", "w8a8"])
 def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
     """A layer saved and loaded back (qlin_import, no requantization) gives the same outputs
     bit for bit as the layer that was saved, decode and prefill."""
@@ -93,6 +97,11 @@ def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
     if kind == "w4":
         W, X = synth.gptq_layer(N, K, 40, seed=41)
         L = qlin.QLinear.from_w4g128(W)
+    elif kind == "w4_act":
+        W, X = synth.gptq_layer(N, K, 40, seed=41)
+        Xcal = synth.gptq_calibration(128, K, seed=41)
+        L = qlin.QLinear.from_w4g128_gptq(W, (Xcal * (2.0 ** (np.arange(K) % 5 - 2))[None, :]).astype(np.float32),
+                                          act_order=True)
     elif kind == "spqr":
         W, X = synth.spqr_layer(N, K, 40, seed=41)
         L = qlin.QLinear.from_spqr(W, 0.02)
