@@ -208,7 +208,12 @@ qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stre
 qlin_status qlin_forward_spqr_static(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream);
 
 /* End-to-end form: copies X from host memory (X_host, pinned for full speed) into X_dev,
- * runs qlin_forward, copies Y_dev back into Y_host and waits for the stream. */
+ * runs qlin_forward, copies Y_dev back into Y_host and waits for the stream.  On a created
+ * stream the three steps are captured once into a CUDA graph per (X_host, Y_host, X_dev, Y_dev,
+ * bound weights, M, stream) and replayed on later calls with the same arguments (up to 64 kept
+ * per handle, least recently used dropped; qlin_set_workspace drops them all); on the legacy
+ * default stream, or while the stream is being captured by the caller, they are enqueued one by
+ * one.  The host buffers are read and written when the step runs, as with plain copies. */
 qlin_status qlin_forward_host(qlin_handle h, const void* X_host, void* Y_host, void* X_dev,
                               void* Y_dev, int M, qlin_stream stream);
 

@@ -164,7 +164,25 @@ static inline int rtn_code(float v, const RtnStats& st, int bits) {
 // ------------------------------------------------------------------------------------
 // the layer handle
 
+// qlin_forward_host's captured steps (H2D copy, forward, D2H copy), one per set of pointers
+struct HostGraph {
+  const void* xh;
+  void* yh;
+  void* xd;
+  void* yd;
+  const uint8_t* dev;
+  int M;
+  cudaStream_t stream;
+  cudaGraphExec_t exec;
+  uint64_t used;
+};
+
 struct qlin_layer {
+  ~qlin_layer() {
+    for (auto& g : host_graphs) cudaGraphExecDestroy(g.exec);  // errors at process exit are moot
+  }
+  std::vector<HostGraph> host_graphs;
+  uint64_t host_graph_clock = 0;
   int format = 0;
   int N = 0, K = 0;
   float alpha = 0.f, frac = 0.f;
@@ -1273,6 +1291,8 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
   // status word, partial slots and counters start at zero; counters return to zero after
   // every forward (the last contributor of a row group resets its counter)
   if (cudaMemsetAsync(dev_ws, 0, w.qx, (cudaStream_t)stream) != cudaSuccess) return QLIN_ERR_CUDA;
+  for (auto& g : h->host_graphs) cudaGraphExecDestroy(g.exec);  // they hold the old workspace
+  h->host_graphs.clear();
   h->ws = (uint8_t*)dev_ws;
   h->ws_bytes = bytes;
   h->ws_maxM = max_M;
@@ -1364,18 +1384,75 @@ qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stre
   return run_decode(h, (const uint16_t*)X, (uint16_t*)Y, nullptr, M, s);
 }
 
+// The step's three stream operations, enqueued on s.
+static qlin_status host_step(qlin_handle h, const void* X_host, void* Y_host, void* X_dev, void* Y_dev, int M,
+                             cudaStream_t s) {
+  if (cudaMemcpyAsync(X_dev, X_host, (size_t)M * h->K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QLIN_ERR_CUDA;
+  qlin_status st = qlin_forward(h, X_dev, Y_dev, M, (qlin_stream)s);
+  if (st != QLIN_OK) return st;
+  if (cudaMemcpyAsync(Y_host, Y_dev, (size_t)M * h->N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QLIN_ERR_CUDA;
+  return QLIN_OK;
+}
+
+static constexpr size_t kMaxHostGraphs = 64;
+
+// The step as one CUDA graph launch: captured the first time a set of pointers, M and stream is
+// seen (the copies, the kernels and their programmatic dependencies baked in), replayed after.
+// Returns QLIN_ERR_UNSUPPORTED (nothing enqueued) where capture is not possible.
+static qlin_status host_step_graph(qlin_handle h, const void* X_host, void* Y_host, void* X_dev, void* Y_dev, int M,
+                                   cudaStream_t s) {
+  if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return QLIN_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return QLIN_ERR_UNSUPPORTED;
+  ++h->host_graph_clock;
+  for (auto& g : h->host_graphs) {
+    if (g.xh == X_host && g.yh == Y_host && g.xd == X_dev && g.yd == Y_dev && g.dev == h->dev && g.M == M &&
+        g.stream == s) {
+      g.used = h->host_graph_clock;
+      return cudaGraphLaunch(g.exec, s) == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
+    }
+  }
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return QLIN_ERR_UNSUPPORTED;
+  }
+  const qlin_status st = host_step(h, X_host, Y_host, X_dev, Y_dev, M, s);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  if (st != QLIN_OK || ec != cudaSuccess || !graph) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return st != QLIN_OK ? st : QLIN_ERR_UNSUPPORTED;
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess || !exec) {
+    cudaGetLastError();
+    return QLIN_ERR_UNSUPPORTED;
+  }
+  if (h->host_graphs.size() >= kMaxHostGraphs) {  // drop the least recently used
+    size_t lru = 0;
+    for (size_t i = 1; i < h->host_graphs.size(); ++i)
+      if (h->host_graphs[i].used < h->host_graphs[lru].used) lru = i;
+    cudaGraphExecDestroy(h->host_graphs[lru].exec);
+    h->host_graphs.erase(h->host_graphs.begin() + (ptrdiff_t)lru);
+  }
+  h->host_graphs.push_back(HostGraph{X_host, Y_host, X_dev, Y_dev, h->dev, M, s, exec, h->host_graph_clock});
+  return cudaGraphLaunch(exec, s) == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
+}
+
 qlin_status qlin_forward_host(qlin_handle h, const void* X_host, void* Y_host, void* X_dev,
                               void* Y_dev, int M, qlin_stream stream) {
   if (!X_host || !Y_host) return QLIN_ERR_INVALID_ARG;
   qlin_status st = check_forward(h, X_dev, Y_dev, M);
   if (st != QLIN_OK || M == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(X_dev, X_host, (size_t)M * h->K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return QLIN_ERR_CUDA;
-  st = qlin_forward(h, X_dev, Y_dev, M, stream);
+  st = host_step_graph(h, X_host, Y_host, X_dev, Y_dev, M, s);
+  if (st == QLIN_ERR_UNSUPPORTED) st = host_step(h, X_host, Y_host, X_dev, Y_dev, M, s);
   if (st != QLIN_OK) return st;
-  if (cudaMemcpyAsync(Y_host, Y_dev, (size_t)M * h->N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return QLIN_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
 }
 

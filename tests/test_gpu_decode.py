@@ -115,6 +115,41 @@ def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
         assert np.array_equal(_y(a, X[:M], M).view(np.uint32), _y(b, X[:M], M).view(np.uint32))
 
 
+def test_forward_host_graph_replays(qlin):
+    """qlin_forward_host captures its copies and kernels into a graph per argument set and
+    replays it: new input contents, another output buffer, another M and re-attached weights
+    must all give qlin_forward's outputs bit for bit."""
+    N, K = 256, 1024
+    W, X = synth.spqr_layer(N, K, 8, seed=51)
+    layer = qlin.QLinear.from_spqr(W, 0.01).to("cuda", max_M=8)
+    stream = torch.cuda.Stream()
+    Xd = torch.empty((8, K), dtype=torch.bfloat16, device="cuda")
+    Yd = torch.empty((8, N), dtype=torch.bfloat16, device="cuda")
+    Xh = torch.empty((8, K), dtype=torch.bfloat16).pin_memory()
+    Yh = [torch.empty((8, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    X2 = synth.activations_bf16(52, 8, K)
+
+    def expect(xbits, M):
+        return _y(layer, xbits[:M], M).view(np.uint32)
+
+    def host(xbits, M, yh):
+        Xh[:M].copy_(torch.from_numpy(np.ascontiguousarray(xbits[:M])).view(torch.bfloat16))
+        qlin.qlin_forward_host(layer.handle, Xh, yh, Xd, Yd, M, stream)
+        return bits_to_f32(yh[:M].view(torch.int16).numpy().view(np.uint16)).view(np.uint32)
+
+    for M in (1, 1, 5):
+        assert np.array_equal(host(X, M, Yh[0]), expect(X, M))
+    assert np.array_equal(host(X2, 1, Yh[0]), expect(X2, 1))  # replay reads the new input
+    assert np.array_equal(host(X2, 1, Yh[1]), expect(X2, 1))  # another output buffer
+    nb = qlin.qlin_device_bytes(layer.handle)
+    image = layer.weights[(-layer.weights.data_ptr()) % 256:][:nb]
+    copy = torch.empty_like(image)  # a fresh allocation: 256-byte aligned
+    copy.copy_(image)
+    torch.cuda.synchronize()
+    qlin.qlin_attach(layer.handle, copy.data_ptr(), nb)
+    assert np.array_equal(host(X2, 5, Yh[1]), expect(X2, 5))  # other weights, same values
+
+
 # ----------------------------------------------------------------------------- SpQR
 
 @pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (64, 256, 0.0)])
