@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "qlin_internal.h"
@@ -63,6 +64,21 @@ inline bool encode_decode_x_map(CUtensorMap* map, const void* X, int64_t K, int 
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device): the attribute is per device, so a process driving several GPUs needs it on
+// each.  `done` holds one bit per device id < 64 (larger ids set it on every call).
+template <typename Kernel>
+inline int smem_attr_once(Kernel* kernel, size_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return 0;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return (int)e;
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return 0;
 }
 
 // Dynamic shared memory rounded up to a 128-byte boundary (the launch adds 128 bytes)

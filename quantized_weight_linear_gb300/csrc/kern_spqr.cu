@@ -581,13 +581,8 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
   CUtensorMap xmap{};
   if (MODE == 2 && !encode_decode_x_map(&xmap, X, v.K, M, kXHalfSp)) return (int)cudaErrorInvalidValue;
   const size_t smem = sizeof(SpSmem<XR>) + 128;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(spqr_decode_kernel<MODE, MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (const int e = smem_attr_once(spqr_decode_kernel<MODE, MT, OWN>, smem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(160);

@@ -763,12 +763,8 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
   const size_t smem = sizeof(TcSmem<F>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (const int e = smem_attr_once(tc_gemm_kernel<F>, smem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(((args.N + kBN - 1) / kBN) * ((args.M + BM - 1) / BM)));
   cfg.blockDim = dim3(tc_threads<F>());

@@ -221,12 +221,8 @@ int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const W
   CUtensorMap xmap{};
   if (!(MT == 1 && OWN == 1) && !encode_decode_x_map(&xmap, X, v.K, M, kXStrideW4)) return (int)cudaErrorInvalidValue;
   const size_t smem = sizeof(W4Smem<MT>) + 128;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4_decode_kernel<MT, OWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (const int e = smem_attr_once(w4_decode_kernel<MT, OWN>, smem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(160);
@@ -294,13 +290,10 @@ int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M
   // many tokens: stage each row (coalesced); a few tokens: one CTA per row would serialize the
   // row, so many CTAs gather straight from global memory (measured: M = 1 faster, M = 4096 slower)
   if (M > 16 && K <= kGatherRowMaxK) {
-    static int attr_k = 0;  // largest K the smem attribute has been raised for
+    static std::atomic<uint64_t> attr_done{0};  // raised to the largest size, once per device
     const size_t smem = (size_t)K * 2;
-    if (smem > 48 * 1024 && K > attr_k) {
-      const cudaError_t e = cudaFuncSetAttribute(w4_gather_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-      if (e != cudaSuccess) return (int)e;
-      attr_k = K;
+    if (smem > 48 * 1024) {
+      if (const int e = smem_attr_once(w4_gather_row_kernel, (size_t)kGatherRowMaxK * 2, attr_done)) return e;
     }
     cfg.gridDim = dim3((unsigned)M);
     cfg.blockDim = dim3(256);

@@ -391,12 +391,8 @@ template <int MT>
 int launch_w8_mt(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc, int M,
                  const Workspace& ws, int grid, void* stream) {
   const size_t smem = sizeof(W8Smem<MT>);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (const int e = smem_attr_once(w8_decode_kernel<MT>, smem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(160);

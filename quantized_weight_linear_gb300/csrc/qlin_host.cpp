@@ -212,17 +212,20 @@ struct qlin_layer {
   int grid = 0;
 };
 
+// SM count of the current device, looked up once per device
 static int sm_count_cached() {
-  static std::atomic<int> cached{0};
-  int v = cached.load();
-  if (v) return v;
+  static std::atomic<int> cached[64];
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  if (dev >= 0 && dev < 64 && (n = cached[dev].load()) > 0) return n;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 152;
   }
-  cached.store(n);
+  if (dev >= 0 && dev < 64) cached[dev].store(n);
   return n;
 }
 
