@@ -323,6 +323,35 @@ def _extra_configs(q, torch, stream, l2):
     return out
 
 
+def _decode_case(q, torch, stream, l2, spec, steps=4000):
+    """One decode configuration "fmt,K,N,M[,outlier_frac]" (fmt w4g128 | spqr | w8a8) on the
+    bench's timing scheme (rotated resident copies, CUDA graph replays): for profiling lines."""
+    import qlin_synth as synth
+    parts = spec.split(",")
+    fmt, K, N, M = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
+    frac = float(parts[4]) if len(parts) > 4 else 0.01
+    if fmt == "w4g128":
+        W, X = synth.gptq_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_w4g128(W).to("cuda", max_M=16)
+    elif fmt == "spqr":
+        W, X = synth.spqr_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_spqr(W, frac).to("cuda", max_M=16)
+    elif fmt == "w8a8":
+        W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=16)
+    else:
+        raise ValueError(f"unknown decode format {fmt}")
+    del W
+    nbytes = layer.handle.info.packed_bytes
+    R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
+    rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
+    rot.capture()
+    n, ms = _time_steps(rot, max(R, steps // R * R), 2 * R, DistCtx.__new__(_NoDist))
+    t = ms / n / 1e3
+    return {f"decode_{fmt}_K{K}_N{N}_M{M}": {"GB/s": round(nbytes / t / 1e9, 1), "us_per_forward": round(t * 1e6, 3),
+                                              "weight_bytes": nbytes}}
+
+
 def _prefill_configs(q, torch, stream, fmts=("w4g128", "spqr1pct", "w8a8")):
     """Prefill M=4096 on K=8192, N=28672 for the three formats (tensor-core path): TFLOP/s."""
     import qlin_synth as synth
@@ -466,6 +495,9 @@ def main():
     ap.add_argument("--_oracle_only", dest="oracle_only", action="store_true")
     ap.add_argument("--prefill-case", dest="prefill_case", choices=["w4g128", "spqr1pct", "w8a8"],
                     help="time only this M=4096 prefill configuration (for profiling) and print its line")
+    ap.add_argument("--decode-case", dest="decode_case",
+                    help="time only this decode configuration, fmt,K,N,M[,outlier_frac] with fmt in "
+                         "w4g128|spqr|w8a8 (for profiling), and print its line")
     args = ap.parse_args()
     if args.oracle_only:
         print(json.dumps(_oracle_spqr_forward_time()))
@@ -477,6 +509,18 @@ def main():
         build()
         q.lib()
         print(json.dumps(_prefill_configs(q, torch, torch.cuda.Stream(), (args.prefill_case,))))
+        return
+    if args.decode_case:
+        import torch
+        import quantized_weight_linear_gb300 as q
+        from quantized_weight_linear_gb300.build import build
+        build()
+        q.lib()
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            line = _decode_case(q, torch, stream, torch.cuda.get_device_properties(0).L2_cache_size, args.decode_case,
+                                args.steps if args.steps != 480000 else 4000)
+        print(json.dumps(line))
         return
     if args.warmup < 3:
         args.warmup = 3
