@@ -45,7 +45,7 @@ extern "C" {
 typedef enum {
   QLIN_OK = 0,
   QLIN_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, non-finite input */
-  QLIN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  QLIN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   QLIN_ERR_CUDA = 3,        /* a CUDA runtime call failed */
   QLIN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than qlin_workspace_bytes */
   QLIN_ERR_TIMEOUT = 5,     /* a device-side wait gave up after its iteration limit */
