@@ -113,7 +113,8 @@ __global__ void w8_export_kernel(W8View v, int8_t* __restrict__ out) {
     const int kb = k / kW8Block, kk = k % kW8Block, j = kk / 16, kr = kk % 16;
     const int g = r & 7, rowhi = r >> 3, khi = kr >= 8 ? 1 : 0, t = (kr - 8 * khi) >> 1, kodd = kr & 1;
     const uint8_t* unit = v.units + (rg * v.KB + kb) * (int64_t)kW8UnitBytes;
-    const uint8_t u = unit[((rt * 32 + 4 * g + t) * 32) + j * 8 + khi * 4 + rowhi * 2 + kodd];
+    const int lane = 4 * g + t;  // word 2j + khi of the lane: half j / 2, bytes (j % 2) * 8 + khi * 4 ..
+    const uint8_t u = unit[((rt * 2 + (j >> 1)) * 32 + lane) * 16 + (j & 1) * 8 + khi * 4 + rowhi * 2 + kodd];
     out[idx] = (int8_t)((int)u - 128);
   }
 }

@@ -272,9 +272,8 @@ __device__ __forceinline__ void convert_tile(uint8_t* bt, const uint8_t* unit, i
       sts32(bt, o1 + 1024u, bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero));
     }
   } else if constexpr (F == kW8) {
-    const uint8_t* src = unit + (rt * 32 + lane) * 32;
-    const uint4 w01 = *reinterpret_cast<const uint4*>(src);
-    const uint4 w23 = *reinterpret_cast<const uint4*>(src + 16);
+    const uint4 w01 = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + 0) * 32 + lane) * 16);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + 1) * 32 + lane) * 16);
     const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
     const uint32_t magic = 0x64646464u, off = 0x64806480u;
 #pragma unroll

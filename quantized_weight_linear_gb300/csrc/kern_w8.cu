@@ -347,9 +347,9 @@ __global__ void __launch_bounds__(160, MT == 1 ? 4 : 3)
       cur_rg = rg;
     }
     if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
-    const uint8_t* unit = sm.unit[s] + (warp * 32 + lane) * 32;
-    const uint4 w01 = *reinterpret_cast<const uint4*>(unit);
-    const uint4 w23 = *reinterpret_cast<const uint4*>(unit + 16);
+    // the lane's 8 words as two halves, each a contiguous 512 bytes across the warp
+    const uint4 w01 = *reinterpret_cast<const uint4*>(sm.unit[s] + ((warp * 2 + 0) * 32 + lane) * 16);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(sm.unit[s] + ((warp * 2 + 1) * 32 + lane) * 16);
     const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
     const uint32_t magic = 0x64646464u, off = 0x64806480u;  // fp16 1152 = 1024 + 128
 #pragma unroll

@@ -915,10 +915,9 @@ static void build_w8_image(qlin_layer* L) {
               const int v = n < N ? (int)L->qw[(size_t)n * K + k] : 0;
               return (uint8_t)(v + 128);
             };
-            uint8_t* dst = unit + ((size_t)rt * 32 + lane) * 32;
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; ++j) {  // words 2j, 2j+1: half j / 2, position 2 (j % 2)
               const int k0 = kb * kW8Block + 16 * j;
-              uint8_t* w0 = dst + j * 8;
+              uint8_t* w0 = unit + (((size_t)rt * 2 + (j >> 1)) * 32 + lane) * 16 + (j & 1) * 8;
               w0[0] = u(gq, k0 + 2 * t);
               w0[1] = u(gq, k0 + 2 * t + 1);
               w0[2] = u(gq + 8, k0 + 2 * t);

@@ -42,7 +42,9 @@
 //   (bits 12..15 of every other entry are zero).
 //
 // W8A8 unit = (row group, one 64-wide K block), 4096 bytes of codes:
-//   codes [4 row tiles][32 lanes][8 words] bytes u = q + 128 in A-fragment order; for
+//   codes [4 row tiles][2 halves][32 lanes][4 words] bytes u = q + 128 in A-fragment order
+//   (a lane's 8 words split in two halves of 16 bytes, so that a warp's 16-byte loads of a
+//   half are contiguous); lane word w (0..7) sits in half w / 4 at position w % 4; for
 //   k16 tile j: word 2j = (row g k 2t, row g k 2t+1, row g+8 k 2t, row g+8 k 2t+1),
 //   word 2j+1 = the same at k 2t+8, 2t+9; plus per-row fp32 sw and per-channel fp32
 //   s_inv in their own sections.
