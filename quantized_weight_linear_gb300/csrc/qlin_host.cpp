@@ -450,31 +450,50 @@ static qlin_status build_w4_gptq(qlin_layer* L, const float* W, const float* Xca
   L->zero.assign((size_t)N * G, 0);
   std::vector<uint8_t> q((size_t)N * K);
   std::atomic<bool> bad{false};
-  parallel_for(N, [&](int64_t b, int64_t e) {
-    std::vector<double> w(K);
+  // Rows are independent: they are taken kGptqTile at a time, transposed to [K][tile], so each
+  // element of U read from memory serves the whole tile and the update runs along contiguous
+  // rows.  Every weight still receives its updates one by one in column order, as products
+  // then differences (the oracle's arithmetic, bit for bit).
+  constexpr int kGptqTile = 32;
+  const int64_t tiles = (N + kGptqTile - 1) / kGptqTile;
+  parallel_for(tiles, [&](int64_t tb, int64_t tend) {
+    std::vector<double> wt((size_t)K * kGptqTile);
     std::vector<float> gv(kW4Group);
-    for (int64_t n = b; n < e; ++n) {
-      const float* row = W + (size_t)n * K;
-      for (int k = 0; k < K; ++k) w[k] = dead[k] ? 0.0 : (double)row[k];
-      RtnStats st{};
+    RtnStats st[kGptqTile];
+    double ek[kGptqTile];
+    for (int64_t tile = tb; tile < tend && !bad; ++tile) {
+      const int64_t n0 = tile * kGptqTile;
+      const int nr = (int)std::min<int64_t>(kGptqTile, N - n0);
+      for (int k = 0; k < K; ++k)
+        for (int r = 0; r < nr; ++r) wt[(size_t)k * kGptqTile + r] = dead[k] ? 0.0 : (double)W[(size_t)(n0 + r) * K + k];
       for (int k = 0; k < K; ++k) {
         const int g = k / kW4Group;
         if (k % kW4Group == 0) {
-          for (int i = 0; i < kW4Group; ++i) gv[i] = (float)w[k + i];
-          st = rtn_stats(gv.data(), nullptr, kW4Group, 4);
-          if (st.overflow) {
-            bad = true;
-            return;
+          for (int r = 0; r < nr; ++r) {
+            for (int i = 0; i < kW4Group; ++i) gv[i] = (float)wt[(size_t)(k + i) * kGptqTile + r];
+            st[r] = rtn_stats(gv.data(), nullptr, kW4Group, 4);
+            if (st[r].overflow) {
+              bad = true;
+              return;
+            }
+            L->scale[(size_t)(n0 + r) * G + g] = st[r].scale_h;
+            L->zero[(size_t)(n0 + r) * G + g] = f2h(st[r].zero);
           }
-          L->scale[(size_t)n * G + g] = st.scale_h;
-          L->zero[(size_t)n * G + g] = f2h(st.zero);
         }
-        const int code = rtn_code((float)w[k], st, 4);
-        q[(size_t)n * K + k] = (uint8_t)code;
-        const float w_hat = ((float)code - st.zero) * st.scale;
-        const double ek = (w[k] - (double)w_hat) / U[(size_t)k * K + k];
+        const double ukk = U[(size_t)k * K + k];
+        for (int r = 0; r < nr; ++r) {
+          const double wk = wt[(size_t)k * kGptqTile + r];
+          const int code = rtn_code((float)wk, st[r], 4);
+          q[(size_t)(n0 + r) * K + k] = (uint8_t)code;
+          const float w_hat = ((float)code - st[r].zero) * st[r].scale;
+          ek[r] = (wk - (double)w_hat) / ukk;
+        }
         const double* Uk = &U[(size_t)k * K];
-        for (int j = k + 1; j < K; ++j) w[j] -= ek * Uk[j];
+        for (int j = k + 1; j < K; ++j) {
+          const double u = Uk[j];
+          double* wj = &wt[(size_t)j * kGptqTile];
+          for (int r = 0; r < nr; ++r) wj[r] -= ek[r] * u;
+        }
       }
     }
   });
