@@ -83,6 +83,30 @@ def _traffic(kernel_key: str):
 
 # ------------------------------------------------------------------------------------ oracle arm
 
+def _host_cpu() -> dict:
+    """The host the oracle ran on: logical CPU count and the CPU's name as the OS reports it."""
+    import platform
+    model, impl, part = "", "", ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" not in line:
+                    continue
+                key, val = (x.strip() for x in line.split(":", 1))
+                key = key.lower()
+                if key in ("model name", "cpu model") and not model:
+                    model = val
+                elif key == "cpu implementer" and not impl:
+                    impl = val
+                elif key == "cpu part" and not part:
+                    part = val
+    except OSError:
+        pass
+    if not model and impl:  # Arm: implementer / part codes (0x41 / 0xd4f: Neoverse V2, as in Grace)
+        model = "Arm Neoverse V2" if (impl, part) == ("0x41", "0xd4f") else f"arm implementer {impl} part {part}"
+    return {"nproc": os.cpu_count(), "cpu": f"{model or platform.processor() or ''} ({platform.machine()})"}
+
+
 def _oracle_spqr_forward_time(reps_min: int = 2, budget_s: float = 12.0):
     """Times the oracle's forward (canonical arrays -> fp64 y) on the host; one thread."""
     import qlin_synth as synth
@@ -104,7 +128,8 @@ def _oracle_spqr_forward_time(reps_min: int = 2, budget_s: float = 12.0):
     t = statistics.median(times)
     return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"full layer 11008x4096 M=1, {len(times)} forwards (canonical arrays -> dequant -> fp64 GEMV), "
-                      f"median {t:.2f} s each, one host thread"}
+                      f"median {t:.2f} s each, one host thread",
+            "host": _host_cpu()}
 
 
 def cpu_baseline_subprocess():
@@ -420,7 +445,10 @@ def run_gpu(args):
 
     W, X = synth.spqr_layer(N_, K_, M_, seed=0)
     with torch.cuda.stream(stream):
-        layer = q.QLinear.from_spqr(W, FRAC).to("cuda", stream=stream)
+        t_pack = time.perf_counter()
+        packed = q.QLinear.from_spqr(W, FRAC)  # host packer (C++, host threads), reported apart
+        t_pack = time.perf_counter() - t_pack
+        layer = packed.to("cuda", stream=stream)
         nbytes = layer.handle.info.packed_bytes
         R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
         Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
@@ -449,7 +477,8 @@ def run_gpu(args):
                    "l2": f"inputs larger than L2: {R} resident weight copies rotated "
                          f"({R * q.qlin_device_bytes(layer.handle) / 1e6:.0f} MB > 4x {l2 / 1e6:.0f} MB L2)",
                    "issue": f"CUDA graph replays of {R} forwards, programmatic dependent launch between forwards",
-                   "parallelism": f"replicas x{dist_ctx.world}"},
+                   "parallelism": f"replicas x{dist_ctx.world}",
+                   "host_pack_s": round(t_pack, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("spqr_decode_m1"),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs: torch copy)",
