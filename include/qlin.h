@@ -165,7 +165,8 @@ qlin_status qlin_pack_w8(const float* W, int N, int K, const float* act_absmax, 
 qlin_status qlin_device_bytes(qlin_handle h, size_t* weight_bytes);
 
 /* Workspace a forward with up to max_M rows needs (partial sums of split output rows,
- * their arrival counters, the device status word, W8A8 int8 activations and scales). */
+ * their arrival counters, the device status word; W8A8: the activation codes and scales;
+ * act-order W4: X in the permuted channel order). */
 qlin_status qlin_workspace_bytes(qlin_handle h, int max_M, size_t* bytes);
 
 /* Copies the device image into caller-owned device memory dev_weights (>= weight_bytes,
@@ -187,7 +188,9 @@ qlin_status qlin_set_workspace(qlin_handle h, void* dev_ws, size_t bytes, int ma
 
 /* Y = X . W_hat^T.  X: device bf16 [M][K], Y: device bf16 [M][N], both 16-byte aligned.
  * Asynchronous on `stream`; returns launch errors only.  M == 0 is a no-op.  Decode
- * (1 <= M <= 16) runs the fused dequant GEMV kernels; larger M runs the tensor-core path. */
+ * (1 <= M <= 16) runs the fused dequant GEMV kernels; larger M runs the tensor-core path.
+ * W8A8 and act-order W4 handles keep per-token data in the workspace, so for them M must
+ * not exceed the workspace's max_M (QLIN_ERR_WORKSPACE otherwise). */
 qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream);
 
 /* The SpQR decode forward (format SPQR, 1 <= M <= 16) without any workspace: for callers
