@@ -232,7 +232,8 @@ qlin_status qlin_forward_acc(qlin_handle h, const void* X, int32_t* acc, int M,
 
 /* Writes the dequantized fp32 weights W_hat [N][K] decoded from the bound device image
  * (W4G128, SPQR), or the int8 codes qw [N][K] (W8A8, out viewed as int8).  Checks that
- * the device layout decodes to exactly the canonical arrays. */
+ * the device layout decodes to exactly the canonical arrays.  Act-order W4: the columns come
+ * in the codes' (permuted) order, column j being input channel perm[j]. */
 qlin_status qlin_dequant_device(qlin_handle h, void* out, qlin_stream stream);
 
 /* Waits for `stream`, then reads and clears the device status word: QLIN_OK or

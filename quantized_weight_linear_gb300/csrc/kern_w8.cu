@@ -5,16 +5,20 @@
 // product is accumulated in integers and scaled back.
 //
 // Act-quant: x' = x * s_inv (fp32), sx = max|x'| / 127 (1 if 0), q = clamp(rint(x'/sx), +-127),
-// IEEE division and round-half-to-even, one CTA per token.  The forward path stores the
-// codes as fp16 (exact for |q| <= 127) so the GEMV can feed them to the MMA directly.
+// IEEE division and round-half-to-even, one CTA per token that reads its row once and keeps
+// x' in registers (rows up to 32768 wide; a two-pass form for wider ones).  The forward path
+// stores the codes as fp16 (exact for |q| <= 127) so the MMA takes them directly: row-major
+// for the prefill GEMM's tensor map, K-blocked [K/64][M][72] for the decode GEMV, whose
+// X slice per unit is then one bulk copy.
 //
 // GEMV: Blackwell Ultra's int8 tensor rate is a small fraction of its fp16 rate, so the
 // integer product runs on the fp16 MMA instead: int8 codes are exact in fp16, products
 // (|q| <= 127^2) are exact in fp32, and any sum of at most 1024 of them stays below 2^24,
 // hence exact too.  The kernel drains the fp32 accumulators into int32 every 16 units
 // (1024 K) -- the int32 result equals the integer accumulator bit for bit.  Weight bytes are
-// stored as u = q + 128 in A-fragment order; one byte permute makes fp16 (1024 + u) and one
-// fp16 subtract of 1152 leaves q.  Epilogue y = bf16((fp32(acc) * sx_m) * sw_n).
+// stored as u = q + 128 in A-fragment order (a lane's 32 bytes as two 16-byte halves, so the
+// warp's loads are contiguous); one byte permute makes fp16 (1024 + u) and one fp16 subtract
+// of 1152 leaves q.  Epilogue y = bf16((fp32(acc) * sx_m) * sw_n).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
