@@ -85,6 +85,19 @@ static int host_threads() {
   return (int)std::min(n, 32u);
 }
 
+// fn(i) for i in [0, n), thread t of the pool taking i = t, t + T, t + 2T, ...: balances loops
+// whose work grows with i (triangular matrices)
+static void parallel_cyclic(int64_t n, const std::function<void(int64_t)>& fn) {
+  const int nt = (int)std::min<int64_t>(host_threads(), std::max<int64_t>(n, 1));
+  auto lane = [&](int t) {
+    for (int64_t i = t; i < n; i += nt) fn(i);
+  };
+  std::vector<std::thread> th;
+  for (int t = 1; t < nt; ++t) th.emplace_back(lane, t);
+  lane(0);
+  for (auto& x : th) x.join();
+}
+
 static void parallel_for(int64_t n, const std::function<void(int64_t, int64_t)>& fn) {
   int nt = host_threads();
   if (n < 64 || nt == 1) {
@@ -341,6 +354,20 @@ static void build_w4_image(qlin_layer* L, const std::vector<uint8_t>& q) {
 
 static constexpr int kGptqMaxK = 8192;  // H and its factors are K x K fp64 on the host
 
+// sum of a[p] * b[p], p < n, in four interleaved partial sums
+static inline double dot4(const double* a, const double* b, int64_t n) {
+  double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+  int64_t p = 0;
+  for (; p + 4 <= n; p += 4) {
+    s0 += a[p] * b[p];
+    s1 += a[p + 1] * b[p + 1];
+    s2 += a[p + 2] * b[p + 2];
+    s3 += a[p + 3] * b[p + 3];
+  }
+  for (; p < n; ++p) s0 += a[p] * b[p];
+  return (s0 + s1) + (s2 + s3);
+}
+
 // U with H^-1 = U^T U, U upper triangular with a positive diagonal: with J the order reversal,
 // J H J = L L^T (lower Cholesky factor L) gives H = V V^T for the upper V = J L J, and
 // H^-1 = (V^-1)^T V^-1, so U = V^-1.  H is overwritten.  Returns false if H is not positive
@@ -351,24 +378,49 @@ static bool gptq_inverse_factor(std::vector<double>& H, int K, std::vector<doubl
   for (int i = 0; i < K; ++i)
     for (int j = 0; j < K; ++j) A[(size_t)i * K + j] = H[(size_t)(K - 1 - i) * K + (K - 1 - j)];
   std::vector<double>().swap(H);
-  for (int j = 0; j < K; ++j) {
-    const double* Lj = &A[(size_t)j * K];
-    double d = A[(size_t)j * K + j];
-    for (int p = 0; p < j; ++p) d -= Lj[p] * Lj[p];
-    if (!(d > 0.0)) return false;
-    const double ljj = std::sqrt(d);
-    A[(size_t)j * K + j] = ljj;
-    auto rows = [&](int64_t b, int64_t e) {
-      for (int64_t i = b; i < e; ++i) {
-        double* Li = &A[(size_t)(j + 1 + i) * K];
+  // right-looking blocked Cholesky, panels of kB columns: factor the diagonal block, solve the
+  // rows below it, then subtract the panel's contribution from the trailing lower triangle
+  constexpr int kB = 64;
+  std::atomic<bool> not_pd{false};
+  for (int jb = 0; jb < K; jb += kB) {
+    const int je = std::min(K, jb + kB);
+    for (int j = jb; j < je; ++j) {  // diagonal block (columns of earlier panels already applied)
+      double* Lj = &A[(size_t)j * K];
+      double d = Lj[j];
+      for (int p = jb; p < j; ++p) d -= Lj[p] * Lj[p];
+      if (!(d > 0.0)) return false;
+      Lj[j] = std::sqrt(d);
+      for (int i = j + 1; i < je; ++i) {
+        double* Li = &A[(size_t)i * K];
         double v = Li[j];
-        for (int p = 0; p < j; ++p) v -= Li[p] * Lj[p];
-        Li[j] = v / ljj;
+        for (int p = jb; p < j; ++p) v -= Li[p] * Lj[p];
+        Li[j] = v / Lj[j];
+      }
+    }
+    const int64_t rest = K - je;
+    if (rest <= 0) break;
+    auto panel = [&](int64_t b, int64_t e) {  // rows below the block: L[i][jb..je)
+      for (int64_t r = b; r < e; ++r) {
+        double* Li = &A[(size_t)(je + r) * K];
+        for (int j = jb; j < je; ++j) {
+          const double* Lj = &A[(size_t)j * K];
+          Li[j] = (Li[j] - dot4(Li + jb, Lj + jb, j - jb)) / Lj[j];
+        }
       }
     };
-    const int64_t rest = K - 1 - j;
-    if ((int64_t)rest * j > (1 << 16)) parallel_for(rest, rows); else rows(0, rest);
+    auto trailing = [&](int64_t r) {  // row je + r: A[i][j] -= sum over the panel, je <= j <= i
+      const int64_t i = je + r;
+      double* Ai = &A[(size_t)i * K];
+      for (int64_t j = je; j <= i; ++j) Ai[j] -= dot4(Ai + jb, &A[(size_t)j * K + jb], je - jb);
+    };
+    if (rest * (je - jb) > (1 << 14)) parallel_for(rest, panel); else panel(0, rest);
+    if (rest * rest > (1 << 14)) {
+      parallel_cyclic(rest, trailing);
+    } else {
+      for (int64_t r = 0; r < rest; ++r) trailing(r);
+    }
   }
+  (void)not_pd;
   // V = J L J (upper): V[i][j] = L[K-1-i][K-1-j]; U = V^-1 column by column (back substitution),
   // column j of U kept as row j of UT so both operands are contiguous
   auto V = [&](int i, int j) { return A[(size_t)(K - 1 - i) * K + (K - 1 - j)]; };
@@ -377,15 +429,12 @@ static bool gptq_inverse_factor(std::vector<double>& H, int K, std::vector<doubl
     for (int j = i; j < K; ++j) Vr[(size_t)i * K + j] = V(i, j);
   std::vector<double>().swap(A);
   std::vector<double> UT((size_t)K * K, 0.0);
-  parallel_for(K, [&](int64_t b, int64_t e) {
-    for (int64_t j = b; j < e; ++j) {
-      double* u = &UT[(size_t)j * K];
-      for (int64_t i = j; i >= 0; --i) {
-        const double* Vi = &Vr[(size_t)i * K];
-        double v = (i == j) ? 1.0 : 0.0;
-        for (int64_t p = i + 1; p <= j; ++p) v -= Vi[p] * u[p];
-        u[i] = v / Vi[i];
-      }
+  parallel_cyclic(K, [&](int64_t j) {  // column j costs ~j^2: cyclic assignment balances them
+    double* u = &UT[(size_t)j * K];
+    for (int64_t i = j; i >= 0; --i) {
+      const double* Vi = &Vr[(size_t)i * K];
+      const double v = ((i == j) ? 1.0 : 0.0) - dot4(Vi + i + 1, u + i + 1, j - i);
+      u[i] = v / Vi[i];
     }
   });
   U.assign((size_t)K * K, 0.0);
