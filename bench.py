@@ -66,8 +66,8 @@ def _sources_sha256(names):
     return h.hexdigest()
 
 
-def _traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources are unchanged since."""
+def _capture(kernel_key: str):
+    """The committed ncu capture of a kernel (profiles/traffic.json), if its sources are unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -76,9 +76,21 @@ def _traffic(kernel_key: str):
             d = json.load(f).get(kernel_key)
         if not d or _sources_sha256(d["sources"]) != d["sources_sha256"]:
             return None
-        return float(d["dram_bytes_per_launch"])
+        return d
     except Exception:
         return None
+
+
+def _traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu capture (None once the kernel has changed)."""
+    d = _capture(kernel_key)
+    return float(d["dram_bytes_per_launch"]) if d else None
+
+
+def _ncu_cold_us(kernel_key: str):
+    """The same capture's single-launch gpu__time_duration (caches flushed, launches serialised)."""
+    d = _capture(kernel_key)
+    return d.get("gpu_time_duration_us_cold") if d else None
 
 
 # ------------------------------------------------------------------------------------ oracle arm
@@ -481,6 +493,7 @@ def run_gpu(args):
                    "host_pack_s": round(t_pack, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("spqr_decode_m1"),
+                     "ncu_single_launch_us_cold": _ncu_cold_us("spqr_decode_m1"),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs: torch copy)",
                      "kernel": "spqr_decode_kernel<1,1,1>", "bytes_per_launch": nbytes},
         "e2e": {"value": round(dist_ctx.world * nbytes / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
