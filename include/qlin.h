@@ -197,18 +197,29 @@ qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stre
  * that are given only X and Y and may not allocate device memory -- a layer inside an engine
  * that reserves all device memory for its own pools and hands plugins no workspace, or a
  * service that forbids device allocation once it is serving.  The pages have no counterpart;
- * this is a deployment form of qlin_forward, same kernel, same results.
- * The scratch (partial sums of split row groups, their counters or tags, a status word) is a fixed
- * array inside the library, about 8 MB, held on every GPU that loads the library until the
- * process exits; its address is looked up on the first call on each device, so make that
- * first call before any stream capture.  Limits: at most 640 CTAs (the grid the kernel picks
- * for the device) and N <= 524288; beyond them the call returns QLIN_ERR_WORKSPACE.  Each call
- * clears the counters and status it uses first; the array is shared by every call, so calls
- * whose kernels overlap on the GPU (other streams, other threads) race and must be
- * serialized by the caller.  Device-side wait limits are enforced but not reported here
- * (qlin_poll_status reads the handle's own workspace).  Allocates nothing: no cudaMalloc,
- * cudaFree or allocating library call. */
+ * this is a deployment form of qlin_forward: the same kernels, and the same outputs bit for
+ * bit.
+ * The scratch (partial sums of split row groups, their counters or tags, a status word) is a
+ * fixed array of about 8 MB inside the library.  It is taken on a device when the library's
+ * device module is loaded there -- under CUDA's lazy module loading, at the first qlin_bind
+ * or qlin_attach of a SpQR handle on that device, which look up its address for that reason
+ * (or else at the first call of this function) -- and held until the process exits.  Make
+ * that first bind or call before any stream capture and before the device's memory is
+ * reserved for other uses.
+ * Limits: layers of at most 81,600 units of 64 rows x 256 columns (ceil(N / 64) * K / 256), at
+ * most 524,288 rows, on devices of at most 160 SMs; beyond them the call returns
+ * QLIN_ERR_WORKSPACE.  Each call clears the counters it uses; the array is shared by every
+ * call, so calls whose kernels overlap on the GPU (other streams, other threads) race and
+ * must be serialized by the caller.  A device-side wait that gives up is recorded in the
+ * array's status word and reported by qlin_poll_static_status.  Allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call. */
 qlin_status qlin_forward_spqr_static(qlin_handle h, const void* X, void* Y, int M, qlin_stream stream);
+
+/* Status of the qlin_forward_spqr_static calls on the current device since the last poll:
+ * waits for `stream`, then reads and clears the fixed array's status word.  QLIN_OK, or
+ * QLIN_ERR_TIMEOUT if a device-side wait gave up (the outputs of that call are then
+ * incomplete).  No counterpart on the pages. */
+qlin_status qlin_poll_static_status(qlin_stream stream);
 
 /* End-to-end form: copies X from host memory (X_host, pinned for full speed) into X_dev,
  * runs qlin_forward, copies Y_dev back into Y_host and waits for the stream.  On a created

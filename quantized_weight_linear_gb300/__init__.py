@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "qlin_bind", "qlin_attach", "qlin_set_workspace", "qlin_forward", "qlin_forward_host", "qlin_act_quant",
     "qlin_forward_acc", "qlin_dequant_device", "qlin_poll_status", "qlin_export", "qlin_info",
     "qlin_destroy", "qlin_status_string", "qlin_sm_count", "qlin_debug_wait_timeout", "qlin_forward_spqr_static",
-    "qlin_import",
+    "qlin_poll_static_status", "qlin_import",
 )
 
 
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
             "qlin_sm_count": ([], i32),
             "qlin_debug_wait_timeout": ([vp, i32, vp], i32),
             "qlin_forward_spqr_static": ([H, vp, vp, i32, vp], i32),
+            "qlin_poll_static_status": ([vp], i32),
             "qlin_import": ([i32, i32, i32, ctypes.POINTER(Canonical), ctypes.POINTER(H)], i32),
         }
         for name, (args, res) in sig.items():
@@ -240,6 +241,12 @@ def qlin_forward_spqr_static(h: Handle, X, Y, M: int, stream=None):
     """SpQR decode forward (1 <= M <= 16) that uses the library's fixed scratch array instead
     of a workspace: for callers that may not allocate device memory (see include/qlin.h)."""
     _check(lib().qlin_forward_spqr_static(h.ptr, _vp(X), _vp(Y), M, _stream(stream)), "qlin_forward_spqr_static")
+
+
+def qlin_poll_static_status(stream=None) -> int:
+    """Status of the qlin_forward_spqr_static calls on the current device since the last poll
+    (waits for the stream; QLIN_OK or QLIN_ERR_TIMEOUT)."""
+    return lib().qlin_poll_static_status(_stream(stream))
 
 
 def qlin_forward_host(h: Handle, X_host, Y_host, X_dev, Y_dev, M: int, stream=None):

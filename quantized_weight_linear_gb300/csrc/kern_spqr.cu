@@ -1,32 +1,22 @@
-// SpQR decode GEMV (1 <= M <= 16): Y = X (D + S)^T, dense 3-bit bi-level part D and fp16
-// outliers S applied in the same pass.
+// SpQR decode GEMV for 2 <= M <= 16 tokens: Y = X (D + S)^T, dense 3-bit bi-level part D
+// and fp16 outliers S applied in the same pass.  (One token: kern_gemv1.cu.)
 //
 // SpQR page ("Makale Bülteni — SpQR", "İddia ve Gerçeklik: SpQR"): the kernel unpacks the
 // dense 3-bit codes while it runs the sparse fp16 product, and the page warns that
 // register pressure and warp divergence are the cost of the hybrid.  Design here:
 //
-// * same persistent weight stream as the W4 kernel: up to four CTAs per SM, equal contiguous
-//   ranges of (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group
-//   statistics and fp16 supergroup statistics), a producer warp with cp.async.bulk into a
-//   3-deep ring per CTA, the unit's outlier bucket and X slice staged alongside (with two or
-//   more tokens the slice is two 2D tensor copies of all M rows, not one copy per token);
+// * a persistent weight stream: up to three CTAs per SM, equal contiguous ranges of
+//   (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group statistics and
+//   fp16 supergroup statistics), a producer warp with cp.async.bulk into a 3-deep ring per
+//   CTA, the unit's outlier bucket and X slice staged alongside (the slice is two 2D tensor
+//   copies of all M rows, not one copy per token);
 // * code words hold five 3-bit fields per 16-bit half; one AND/OR turns a field pair into
-//   bf16 (base + q) with base 128 or 16 depending on the field, no shifts for 2 of 5;
-// * M == 1: the eight MMA columns carry eight different 16-groups (block-diagonal B), so
-//   each accumulator is one (row, group) partial sum of exact integer products; the
-//   bi-level statistics are applied once per (row, group) in fp32:
-//     y += s^_g * (sum (base + q) x - sum base x - z^_g * sum x)
-//   and every (row, group) pair belongs to exactly one thread (no redundant decoding);
-// * M >= 2: the same A pairs are dequantized to bf16 s^ (q - z^) in registers and the
-//   MMA columns carry the tokens;
+//   bf16 (base + q) with base 128 or 16 depending on the field;
+// * the A pairs are dequantized to bf16 s^ (q - z^) in registers and the MMA columns carry
+//   the tokens;
 // * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
-//   fp16 value; sorted by quad (row & 7), then row, then k).  M == 1: lane (g, t) of the
-//   MMA layout already owns the sums of rows g and g + 8, which are exactly quad g's run;
-//   the run's bounds come from the quad counts in the bucket's first entries, the quad's
-//   four lanes take every fourth entry into two registers, and the accumulator reduction
-//   over the quad adds them in (buckets too small or too crowded for the counts: a
-//   segmented warp sum over the row runs).  M >= 2: lane L owns row L % 16, finds its run by
-//   bisection and accumulates value * x[k] in registers.  Either way no two lanes ever add
+//   fp16 value; sorted by quad (row & 7), then row, then k).  Lane L owns row L % 16, finds
+//   its run by bisection and accumulates value * x[k] in registers, so no two lanes ever add
 //   into the same sum (no atomics; the page's warning about the sparse part is about exactly
 //   this scattered accumulation).
 #include "kern_decode_common.cuh"
@@ -35,21 +25,18 @@ namespace qlin {
 namespace {
 
 constexpr int kStagesSp = 3;
-constexpr int kXStrideSp = 264;    // M == 1: staged X row, 256 bf16 + 8 pad
-constexpr int kXHalfSp = 136;      // M >= 2: each 128-wide half of the slice as [XR][128 + 8 pad]
+constexpr int kXHalfSp = 136;      // each 128-wide half of the X slice as [XR][128 + 8 pad]
 constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
 constexpr int kOffsCap = 1024 + 16;  // offsets staged per CTA
 
-template <int XR>  // staged X rows (1 for the M == 1 kernel, 8 or 16 otherwise)
+template <int XR>  // staged X rows (8 or 16)
 struct SpSmem {
-  static constexpr int kXE = XR == 1 ? kXStrideSp : 2 * XR * kXHalfSp;  // X elements per stage
+  static constexpr int kXE = 2 * XR * kXHalfSp;  // X elements per stage
   __align__(128) uint8_t unit[kStagesSp][kSpqrUnitBytes];
   __align__(128) uint16_t x[kStagesSp][kXE];
   __align__(16) uint32_t out[kStagesSp][kOutCap + 8];
   __align__(16) uint32_t offs[kOffsCap];
-  __align__(16) uint32_t zeros[8];
   float rowacc[4][16][XR];
-  float orow[4][16];  // M == 1: outlier sums per row of each tile
   float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
@@ -103,11 +90,11 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
   return __funnelshift_r(lo, hi, bit & 31) & 63u;
 }
 
-template <int MODE, int MT, int OWN>  // MODE 1: M == 1; MODE 2: 2 <= M <= 8 MT; OWN: see below
-__global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
+template <int MT, int OWN>  // MT: 8-token column tiles (M <= 8 MT); OWN: see below
+__global__ void __launch_bounds__(160, MT == 1 ? 3 : 2)
     spqr_decode_kernel(const __grid_constant__ CUtensorMap xmap, SpqrView v, const uint16_t* __restrict__ X,
                        uint16_t* __restrict__ Y, int M, Workspace ws) {
-  constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
+  constexpr int XR = 8 * MT;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SpSmem<XR>& sm = *reinterpret_cast<SpSmem<XR>*>(smem_align128(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,7 +123,6 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   {
     uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0]);
     for (int i = threadIdx.x; i < kStagesSp * SpSmem<XR>::kXE / 2; i += blockDim.x) xz[i] = 0u;
-    if (threadIdx.x < 8) sm.zeros[threadIdx.x] = 0u;
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -146,7 +132,6 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     mbar_arrive_expect_tx(&sm.offs_bar, (uint32_t)(off_end - off_base) * 4);
     bulk_g2s(sm.offs, v.offs + off_base, (uint32_t)(off_end - off_base) * 4, &sm.offs_bar);
     if (!mbar_wait(&sm.offs_bar, 0, ws.status)) return;
-    const uint32_t xbytes = kSpqrSuper * 2;
     auto weights = [&](int s, int64_t u) -> uint32_t {  // returns bytes issued
       bulk_g2s(sm.unit[s], v.units + u * (int64_t)kSpqrUnitBytes, kSpqrUnitBytes, &sm.full[s]);
       const uint32_t e0 = offs(4 * u), e1 = offs(4 * u + 4);
@@ -165,17 +150,14 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     };
     // M == 1: one plain copy of the 256-wide slice; otherwise two boxes of xmap ([M][136] at
     // k0 and k0 + 128), one per half of the staged layout
-    const uint32_t xtx = MODE == 1 ? xbytes : 2u * (uint32_t)M * kXHalfSp * 2;
+    const uint32_t xtx = 2u * (uint32_t)M * kXHalfSp * 2;
     int kx = (int)(u0 % S);  // supergroup of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
       const int k0 = kx * kSpqrSuper;
       if (++kx == (int)S) kx = 0;
-      if constexpr (MODE == 1) {
-        bulk_g2s(&sm.x[s][0], X + k0, xbytes, &sm.full[s]);
-      } else {
-        tma_load_2d(&sm.x[s][0], &xmap, k0, 0, &sm.full[s]);
-        tma_load_2d(&sm.x[s][XR * kXHalfSp], &xmap, k0 + 128, 0, &sm.full[s]);
-      }
+      tma_load_2d(&sm.x[s][0], &xmap, k0, 0, &sm.full[s]);
+      tma_load_2d(&sm.x[s][XR * kXHalfSp], &xmap, k0 + 128, 0, &sm.full[s]);
+    
     };
     const int pro = n_units < kStagesSp ? n_units : kStagesSp;
     for (int i = 0; i < pro; ++i) {
@@ -200,7 +182,7 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   const int rt = warp;
   ConsumerSync cs{&sm.cons_bar, 0u, ws.status};
   if (!mbar_wait(&sm.offs_bar, 0, ws.status)) return;
-  constexpr int NACC = (MODE == 1) ? 4 : 4 * MT;
+  constexpr int NACC = 4 * MT;
   float acc[NACC];
 #pragma unroll
   for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
@@ -208,34 +190,26 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   // row L % 16 of the tile in registers; with up to eight tokens the two lanes of a row take
   // alternate outliers of the row and every token, with up to sixteen each takes every
   // outlier of the row and eight of the tokens.
-  constexpr int OT = (MODE == 1) ? 1 : 8;
-  constexpr bool kSplitEntries = (MODE == 1) || (MT == 1);
+  constexpr int OT = 8;
+  constexpr bool kSplitEntries = MT == 1;
   const int orow = lane & 15, ohalf = lane >> 4;
   const int otok0 = kSplitEntries ? 0 : 8 * ohalf;
   float oacc[OT];
 #pragma unroll
   for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
-  float oa = 0.f, ob = 0.f;  // M == 1: outlier sums of rows g and g + 8 (this lane's share)
-  if (lane < 16) sm.orow[rt][lane] = 0.f;
-  __syncwarp();
   int64_t cur_rg = u0 / S;
   UnitCursor cur{cur_rg, (int)(u0 - cur_rg * S), (int)S};
 
-  constexpr int NV = (MODE == 1) ? 2 : NACC;
+  constexpr int NV = NACC;
   int idx[NV];
-  if constexpr (MODE == 1) {
-    idx[0] = t == 0 ? (rt * 16 + g) * 16 : -1;
-    idx[1] = t == 0 ? (rt * 16 + g + 8) * 16 : -1;
-  } else {
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = g + ((i & 2) ? 8 : 0);
-        const int m = 2 * t + (i & 1) + 8 * mt;
-        idx[mt * 4 + i] = (m < M) ? (rt * 16 + r) * 16 + m : -1;
-      }
-  }
+    for (int i = 0; i < 4; ++i) {
+      const int r = g + ((i & 2) ? 8 : 0);
+      const int m = 2 * t + (i & 1) + 8 * mt;
+      idx[mt * 4 + i] = (m < M) ? (rt * 16 + r) * 16 + m : -1;
+    }
   auto done = [&](int64_t rg, const float (&out)[NV]) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
@@ -255,34 +229,25 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
   auto flush = [&](int64_t rg) {
     __syncwarp();
     float vals[NV];
-    if constexpr (MODE == 1) {
-      float r0 = (acc[0] + acc[1]) + oa, r1 = (acc[2] + acc[3]) + ob;
-      r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
-      r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
-      r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-      r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-      vals[0] = r0 + sm.orow[rt][g];
-      vals[1] = r1 + sm.orow[rt][g + 8];
-    } else {
-      if constexpr (kSplitEntries) {
+    if constexpr (kSplitEntries) {
 #pragma unroll
-        for (int j = 0; j < OT; ++j) oacc[j] += __shfl_xor_sync(0xffffffffu, oacc[j], 16);
-      }
-      if (!kSplitEntries || ohalf == 0) {
-#pragma unroll
-        for (int j = 0; j < OT; ++j)
-          if (otok0 + j < M) sm.rowacc[rt][orow][otok0 + j] = oacc[j];
-      }
-      __syncwarp();
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = g + ((i & 2) ? 8 : 0);
-          const int m = 2 * t + (i & 1) + 8 * mt;
-          vals[mt * 4 + i] = acc[mt * 4 + i] + (m < M ? sm.rowacc[rt][r][m] : 0.f);
-        }
+      for (int j = 0; j < OT; ++j) oacc[j] += __shfl_xor_sync(0xffffffffu, oacc[j], 16);
     }
+    if (!kSplitEntries || ohalf == 0) {
+#pragma unroll
+      for (int j = 0; j < OT; ++j)
+        if (otok0 + j < M) sm.rowacc[rt][orow][otok0 + j] = oacc[j];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = g + ((i & 2) ? 8 : 0);
+        const int m = 2 * t + (i & 1) + 8 * mt;
+        vals[mt * 4 + i] = acc[mt * 4 + i] + (m < M ? sm.rowacc[rt][r][m] : 0.f);
+      }
+  
     fin.stage(rg, vals, idx, done);
   };
 
@@ -300,11 +265,6 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
-      oa = 0.f;
-      ob = 0.f;
-      __syncwarp();
-      if (lane < 16) sm.orow[rt][lane] = 0.f;
-      __syncwarp();
       cur_rg = rg;
     }
     if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
@@ -315,141 +275,57 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
     const float ssA = h2f_dev(ra[0]), zsA = h2f_dev(ra[1]), szA = h2f_dev(ra[2]), zzA = h2f_dev(ra[3]);
     const float ssB = h2f_dev(rb[0]), zsB = h2f_dev(rb[1]), szB = h2f_dev(rb[2]), zzB = h2f_dev(rb[3]);
 
-    if constexpr (MODE == 1) {
-      // per-group X sums of the unit: lane l covers group l/2, half l%2
-      const uint16_t* x0 = &sm.x[s][0];
-      float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
+      uint32_t w[6];
       {
-        const int gl = lane >> 1, h = lane & 1;
-        const uint4 xv = *reinterpret_cast<const uint4*>(x0 + gl * 16 + h * 8);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-        float xf[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
-        // fields 0..9 of a group have base 128, fields 10..15 base 16
-        const float s01 = xf[0] + xf[1];
-        const float shi = ((xf[2] + xf[3]) + (xf[4] + xf[5])) + (xf[6] + xf[7]);
-        sa = h ? s01 : s01 + shi;
-        sb = h ? shi : 0.f;
-        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-        sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+        const uint2 p0 = *reinterpret_cast<const uint2*>(cw);
+        const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
+        const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
+        w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
       }
-      const float bsum = 128.f * sa + 16.f * sb, xsum = sa + sb;
-      // per-field constants of the (qs, qz) decode: pair i uses row g (i < 2) or g + 8;
-      // qs sits at bit 6i of the lane's 24-bit field, qz at bit 6i of the field shifted by 3
-      float kcs[4], kms[4], kcz[4], kmz[4];
+      // A-side statistics: (row g, group t), (row g+8, group t), (row g, group t+4), (row g+8, group t+4)
+      const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+      uint32_t sh2[4], ch2[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float ps = (float)(1u << (6 * i)), pz = ps;
-        kcs[i] = 8388608.f + (i < 2 ? zsA : zsB) * ps;
-        kms[i] = (i < 2 ? ssA : ssB) * (1.f / ps);
-        kcz[i] = 8388608.f + (i < 2 ? zzA : zzB) * pz;
-        kmz[i] = (i < 2 ? szA : szB) * (1.f / pz);
+      for (int r = 0; r < 4; ++r) {
+        const int row = g + ((r & 1) ? 8 : 0), gb = t + ((r & 2) ? 4 : 0);
+        const uint32_t e = qsqz_entry(qarea, row, gb);
+        const float ss = (r & 1) ? ssB : ssA, zs = (r & 1) ? zsB : zsA;
+        const float sz = (r & 1) ? szB : szA, zz = (r & 1) ? zzB : zzA;
+        const float sh = __fmul_rn(__fsub_rn((float)(e & 7u), zs), ss);
+        const float zh = __fmul_rn(__fsub_rn((float)(e >> 3), zz), sz);
+        sh2[r] = pack_bf16x2(sh, sh);
+        const float cz = -sh * zh;
+        ch2[r] = pack_bf16x2(cz, cz);
       }
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
-        uint32_t w[6];
-        {
-          const uint2 p0 = *reinterpret_cast<const uint2*>(cw);
-          const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
-          const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
-          w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
-        }
-        const uint16_t* xb = x0 + blk * 128 + 16 * g;
-        const uint32_t* pb0 = (g == t) ? reinterpret_cast<const uint32_t*>(xb) : sm.zeros;
-        const uint32_t* pb1 = (g == t + 4) ? reinterpret_cast<const uint32_t*>(xb) : sm.zeros;
-        const uint4 bx0 = *reinterpret_cast<const uint4*>(pb0);
-        const uint4 bx1 = *reinterpret_cast<const uint4*>(pb1);
-        const uint4 by0 = *reinterpret_cast<const uint4*>(pb0 == sm.zeros ? sm.zeros : pb0 + 4);
-        const uint4 by1 = *reinterpret_cast<const uint4*>(pb1 == sm.zeros ? sm.zeros : pb1 + 4);
-        const uint32_t b0v[8] = {bx0.x, bx0.y, bx0.z, bx0.w, by0.x, by0.y, by0.z, by0.w};
-        const uint32_t b1v[8] = {bx1.x, bx1.y, bx1.z, bx1.w, by1.x, by1.y, by1.z, by1.w};
-        // group sums of the two accumulator columns 2t, 2t+1 of this block
-        const int l0 = 2 * (blk * 8 + 2 * t);
-        const float B0 = __shfl_sync(0xffffffffu, bsum, l0), S0 = __shfl_sync(0xffffffffu, xsum, l0);
-        const float B1 = __shfl_sync(0xffffffffu, bsum, l0 + 2), S1 = __shfl_sync(0xffffffffu, xsum, l0 + 2);
-        // two independent accumulator chains (even / odd j) keep the MMA pipe busy; the even
-        // chain starts at -sum(base x) of its column's group
-        float c[4] = {-B0, -B1, -B0, -B1}, d[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < 8; ++j) {
         uint32_t a[4];
-        spqr_frag<0>(w, a); mma_bf16(c, a, b0v[0], b1v[0]);
-        spqr_frag<1>(w, a); mma_bf16(d, a, b0v[1], b1v[1]);
-        spqr_frag<2>(w, a); mma_bf16(c, a, b0v[2], b1v[2]);
-        spqr_frag<3>(w, a); mma_bf16(d, a, b0v[3], b1v[3]);
-        spqr_frag<4>(w, a); mma_bf16(c, a, b0v[4], b1v[4]);
-        spqr_frag<5>(w, a); mma_bf16(d, a, b0v[5], b1v[5]);
-        spqr_frag<6>(w, a); mma_bf16(c, a, b0v[6], b1v[6]);
-        spqr_frag<7>(w, a); mma_bf16(d, a, b0v[7], b1v[7]);
-        const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(qarea);
-        const int bit = 24 * lane;
-        const uint32_t f24 = __funnelshift_r(qw[bit >> 5], qw[(bit >> 5) + 1], bit & 31) & 0xFFFFFFu;
-        const uint32_t z24 = f24 >> 3;  // qz fields at bits 6i: every field stays below bit 23
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // field at bit p <= 18, OR-ed under the exponent of 2^23: the float 2^23 + q 2^p, exact;
-          // subtracting 2^23 + z 2^p and scaling by s 2^-p gives (q - z) s with one rounding
-          const float xs = __uint_as_float((f24 & (7u << (6 * i))) | 0x4B000000u);
-          const float xz = __uint_as_float((z24 & (7u << (6 * i))) | 0x4B000000u);
-          const float sh = __fmul_rn(__fsub_rn(xs, kcs[i]), kms[i]);
-          const float zh = __fmul_rn(__fsub_rn(xz, kcz[i]), kmz[i]);
-          const float Sg = (i & 1) ? S1 : S0;
-          acc[i] += sh * ((c[i] + d[i]) - zh * Sg);
+        switch (j) {
+          case 0: spqr_frag<0>(w, a); break;
+          case 1: spqr_frag<1>(w, a); break;
+          case 2: spqr_frag<2>(w, a); break;
+          case 3: spqr_frag<3>(w, a); break;
+          case 4: spqr_frag<4>(w, a); break;
+          case 5: spqr_frag<5>(w, a); break;
+          case 6: spqr_frag<6>(w, a); break;
+          default: spqr_frag<7>(w, a); break;
         }
-      }
-    } else {
+        const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
-        uint32_t w[6];
-        {
-          const uint2 p0 = *reinterpret_cast<const uint2*>(cw);
-          const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
-          const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
-          w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
-        }
-        // A-side statistics: (row g, group t), (row g+8, group t), (row g, group t+4), (row g+8, group t+4)
-        const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
-        uint32_t sh2[4], ch2[4];
+        for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = g + ((r & 1) ? 8 : 0), gb = t + ((r & 2) ? 4 : 0);
-          const uint32_t e = qsqz_entry(qarea, row, gb);
-          const float ss = (r & 1) ? ssB : ssA, zs = (r & 1) ? zsB : zsA;
-          const float sz = (r & 1) ? szB : szA, zz = (r & 1) ? zzB : zzA;
-          const float sh = __fmul_rn(__fsub_rn((float)(e & 7u), zs), ss);
-          const float zh = __fmul_rn(__fsub_rn((float)(e >> 3), zz), sz);
-          sh2[r] = pack_bf16x2(sh, sh);
-          const float cz = -sh * zh;
-          ch2[r] = pack_bf16x2(cz, cz);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t a[4];
-          switch (j) {
-            case 0: spqr_frag<0>(w, a); break;
-            case 1: spqr_frag<1>(w, a); break;
-            case 2: spqr_frag<2>(w, a); break;
-            case 3: spqr_frag<3>(w, a); break;
-            case 4: spqr_frag<4>(w, a); break;
-            case 5: spqr_frag<5>(w, a); break;
-            case 6: spqr_frag<6>(w, a); break;
-            default: spqr_frag<7>(w, a); break;
-          }
-          const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint16_t* xr = &sm.x[s][(blk * XR + g + 8 * mt) * kXHalfSp];
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + 16 * t + 2 * j);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 16 * (t + 4) + 2 * j);
-            mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
-          }
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint16_t* xr = &sm.x[s][(blk * XR + g + 8 * mt) * kXHalfSp];
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr + 16 * t + 2 * j);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 16 * (t + 4) + 2 * j);
+          mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
         }
       }
     }
+  
 
     // outliers of this row tile in this unit; the bucket is sorted by row (then k), so each
     // row's outliers form one run.  M == 1: 32 entries at a time, a segmented sum over the
@@ -469,94 +345,28 @@ __global__ void __launch_bounds__(160, MODE == 1 ? 4 : (MT == 1 ? 3 : 2))
       // a warp-uniform branch: a select between the two would issue the global load as well.
       auto from_smem = [bs](int i) -> uint32_t { return bs[i]; };
       auto from_gmem = [bg](int i) -> uint32_t { return __ldg(bg + i); };
-      if constexpr (MODE == 1) {
-        // quad counts: bits 12..15 of the bucket's first eight entries (n >= 8, no escape)
-        uint32_t qc = 0u;
-        if (n >= 8) {
-          if (staged) {
-            if (lane < 8) qc = (bs[lane] >> 12) & 15u;
-          } else {
-            if (lane < 8) qc = (__ldg(bg + lane) >> 12) & 15u;
-          }
+      // lane q <= 16 finds the first entry whose row position (2 (row & 7) + row / 8, the
+      // bucket's order) is >= q; row r's run starts at its position's answer
+      auto pos = [](uint32_t e) { return (int)(((e & 7u) << 1) | ((e >> 3) & 1u)); };
+      const int rpos = ((orow & 7) << 1) | (orow >> 3);
+      auto rows = [&](auto ld) {
+        int lo = 0, hi = n;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (pos(ld(mid)) < lane) lo = mid + 1; else hi = mid;
         }
-        const bool by_quad = n >= 8 && __shfl_sync(0xffffffffu, qc, 0) != 15u;  // warp-uniform
-        auto add = [&](uint32_t e) {  // entry of row g (bit 3 clear) or g + 8
-          const float pv = h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]);
-          if (e & 8u) ob += pv; else oa += pv;
-        };
-        if (by_quad) {
-          uint32_t qe = qc;  // inclusive prefix sum over lanes 0..7: end of quad `lane`
+        const int beg = __shfl_sync(0xffffffffu, lo, rpos), end = __shfl_sync(0xffffffffu, lo, rpos + 1);
+        for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
+          const uint32_t e = ld(p);
+          const int k = (int)((e >> 4) & 255u);
+          const float val = h2f_dev((uint16_t)(e >> 16));
 #pragma unroll
-          for (int d = 1; d < 8; d <<= 1) {
-            const uint32_t w = __shfl_up_sync(0xffffffffu, qe, d);
-            if (lane >= d) qe += w;
-          }
-          const int qend = (int)__shfl_sync(0xffffffffu, qe, g);
-          const int beg = qend - (int)__shfl_sync(0xffffffffu, qc, g) + t;
-          const int end = qend < n ? qend : n;  // the counts never point past the bucket
-          if (staged) {
-            // the first three entries of each lane loaded together (a quad rarely has more
-            // than twelve), then the rest
-            uint32_t e[3];
-#pragma unroll
-            for (int i = 0; i < 3; ++i) e[i] = (beg + 4 * i < end) ? bs[beg + 4 * i] : 0u;
-#pragma unroll
-            for (int i = 0; i < 3; ++i)
-              if (beg + 4 * i < end) add(e[i]);
-            for (int p = beg + 12; p < end; p += 4) add(bs[p]);
-          } else {
-            for (int p = beg; p < end; p += 4) add(__ldg(bg + p));
-          }
-        } else {
-          // chunks of 32 entries: segmented sum over each row's run (runs are contiguous),
-          // and the last lane of a run adds it to the row's sum
-          auto chunks = [&](auto ld) {
-            for (int c0 = 0; c0 < n; c0 += 32) {
-              const int i = c0 + lane;
-              const bool valid = i < n;
-              uint32_t e = 0u;
-              if (valid) e = ld(i);
-              const int r = valid ? (int)(e & 15u) : 16;
-              float vsum = valid ? h2f_dev((uint16_t)(e >> 16)) * bf2f(sm.x[s][(e >> 4) & 255u]) : 0.f;
-              // runs from head flags: lane l's run starts at the last head at or below l
-              const int rprev = __shfl_up_sync(0xffffffffu, r, 1);
-              const uint32_t heads = __ballot_sync(0xffffffffu, lane == 0 || rprev != r);
-              const int start = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
-#pragma unroll
-              for (int d = 1; d < 32; d <<= 1) {
-                const float vu = __shfl_up_sync(0xffffffffu, vsum, d);
-                if (lane - d >= start) vsum += vu;
-              }
-              const bool run_end = lane == 31 || ((heads >> (lane + 1)) & 1u);
-              if (run_end && r < 16) sm.orow[rt][r] += vsum;
-              __syncwarp();
-            }
-          };
-          if (staged) chunks(from_smem); else chunks(from_gmem);
+          for (int j = 0; j < OT; ++j)
+            if (otok0 + j < M) oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
         }
-      } else {
-        // lane q <= 16 finds the first entry whose row position (2 (row & 7) + row / 8, the
-        // bucket's order) is >= q; row r's run starts at its position's answer
-        auto pos = [](uint32_t e) { return (int)(((e & 7u) << 1) | ((e >> 3) & 1u)); };
-        const int rpos = ((orow & 7) << 1) | (orow >> 3);
-        auto rows = [&](auto ld) {
-          int lo = 0, hi = n;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (pos(ld(mid)) < lane) lo = mid + 1; else hi = mid;
-          }
-          const int beg = __shfl_sync(0xffffffffu, lo, rpos), end = __shfl_sync(0xffffffffu, lo, rpos + 1);
-          for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
-            const uint32_t e = ld(p);
-            const int k = (int)((e >> 4) & 255u);
-            const float val = h2f_dev((uint16_t)(e >> 16));
-#pragma unroll
-            for (int j = 0; j < OT; ++j)
-              if (otok0 + j < M) oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
-          }
-        };
-        if (staged) rows(from_smem); else rows(from_gmem);
-      }
+      };
+      if (staged) rows(from_smem); else rows(from_gmem);
+    
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
@@ -574,15 +384,15 @@ static_assert(offsetof(SpSmem<8>, x) % 128 == 0 && offsetof(SpSmem<16>, x) % 128
                   (SpSmem<8>::kXE * 2) % 128 == 0 && (SpSmem<16>::kXE * 2) % 128 == 0 && (8 * kXHalfSp * 2) % 128 == 0,
               "TMA destinations");
 
-template <int MODE, int MT, int OWN>
+template <int MT, int OWN>
 int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                   void* stream) {
-  constexpr int XR = (MODE == 1) ? 1 : 8 * MT;
+  constexpr int XR = 8 * MT;
   CUtensorMap xmap{};
-  if (MODE == 2 && !encode_decode_x_map(&xmap, X, v.K, M, kXHalfSp)) return (int)cudaErrorInvalidValue;
+  if (!encode_decode_x_map(&xmap, X, v.K, M, kXHalfSp)) return (int)cudaErrorInvalidValue;
   const size_t smem = sizeof(SpSmem<XR>) + 128;
   static std::atomic<uint64_t> attr_done{0};
-  if (const int e = smem_attr_once(spqr_decode_kernel<MODE, MT, OWN>, smem, attr_done)) return e;
+  if (const int e = smem_attr_once(spqr_decode_kernel<MT, OWN>, smem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(160);
@@ -593,7 +403,7 @@ int launch_spqr_t(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, cons
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MODE, MT, OWN>, xmap, v, X, Y, M, ws);
+  return (int)cudaLaunchKernelEx(&cfg, spqr_decode_kernel<MT, OWN>, xmap, v, X, Y, M, ws);
 }
 
 }  // namespace
@@ -602,7 +412,7 @@ int spqr_decode_grid(const SpqrView& v, int M, int sms) {
   // several CTAs per SM hide the unpack latency; every CTA stages its slice of the bucket
   // offsets, so ranges stay below kOffsCap entries
   const int64_t U = (int64_t)v.RG * v.S;
-  const int cps = std::min(M == 1 ? 4 : (M <= 8 ? 3 : 2), QLIN_DECODE_CPS_MAX);
+  const int cps = std::min(M <= 8 ? 3 : 2, QLIN_DECODE_CPS_MAX);
   int64_t grid = std::min<int64_t>(U, (int64_t)cps * sms);
   const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
   if (grid < need) grid = std::min<int64_t>(U, need);
@@ -611,12 +421,12 @@ int spqr_decode_grid(const SpqrView& v, int M, int sms) {
 
 int launch_spqr_decode(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                        void* stream) {
+  if (M == 1) return launch_spqr_gemv1(v, X, Y, ws, stream);
   grid = spqr_decode_grid(v, M, ws.sms);
   if (grid > ws.grid) return (int)cudaErrorInvalidValue;
-  if (M == 1) return launch_spqr_t<1, 1, 1>(v, X, Y, M, ws, grid, stream);
-  if (M <= 4) return launch_spqr_t<2, 1, 4>(v, X, Y, M, ws, grid, stream);
-  if (M <= 8) return launch_spqr_t<2, 1, 0>(v, X, Y, M, ws, grid, stream);
-  return launch_spqr_t<2, 2, 0>(v, X, Y, M, ws, grid, stream);
+  if (M <= 4) return launch_spqr_t<1, 4>(v, X, Y, M, ws, grid, stream);
+  if (M <= 8) return launch_spqr_t<1, 0>(v, X, Y, M, ws, grid, stream);
+  return launch_spqr_t<2, 0>(v, X, Y, M, ws, grid, stream);
 }
 
 }  // namespace qlin

@@ -1,4 +1,5 @@
-// W4 g128 decode GEMV (1 <= M <= 16): Y[m, n] = sum_k x[m, k] * (q[n, k] - z) * s.
+// W4 g128 decode GEMV for 2 <= M <= 16 tokens: Y[m, n] = sum_k x[m, k] * (q[n, k] - z) * s.
+// (One token: kern_gemv1.cu.)
 //
 // GPTQ page ("Makale Bülteni — GPTQ", "İddia ve Gerçeklik: GPTQ"): weight-only 4-bit
 // groups pay off at small batch because the layer is bound by weight bandwidth.  The
@@ -35,12 +36,10 @@ struct W4Smem {
   float own[kRowGroup * 4];  // up to 4 tokens: this CTA's partial sums of the row group it owns
 };
 
-template <int MT, int OWN>  // OWN: 1 or 4 (M <= OWN, owner-reduces split completion), 0 counted
+template <int MT, int OWN>  // OWN: 4 (M <= 4, owner-reduces split completion), 0 counted
 __global__ void __launch_bounds__(160, 4)
     w4_decode_kernel(const __grid_constant__ CUtensorMap xmap, W4View v, const uint16_t* __restrict__ X,
                      uint16_t* __restrict__ Y, int M, Workspace ws) {
-  // M == 1: the X slice is one plain bulk copy; otherwise one box of xmap ([M][136] at k0)
-  constexpr bool kTmaX = !(MT == 1 && OWN == 1);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   W4Smem<MT>& sm = *reinterpret_cast<W4Smem<MT>*>(smem_align128(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -70,15 +69,12 @@ __global__ void __launch_bounds__(160, 4)
 
   if (warp == 4) {
     if (lane != 0) return;
-    const uint32_t xbytes = kTmaX ? (uint32_t)M * kXStrideW4 * 2 : kW4Group * 2;
+    const uint32_t xbytes = (uint32_t)M * kXStrideW4 * 2;  // one box of xmap: [M][136] at k0
     const uint32_t tx = kW4UnitBytes + xbytes;
     int kx = (int)(u0 % G);  // K group of the next X slice (units are issued in order)
     auto load_x = [&](int s) {
       const int k0 = kx * kW4Group;
-      if constexpr (kTmaX)
-        tma_load_2d(&sm.x[s][0][0], &xmap, k0, 0, &sm.full[s]);
-      else
-        bulk_g2s(&sm.x[s][0][0], X + k0, xbytes, &sm.full[s]);
+      tma_load_2d(&sm.x[s][0][0], &xmap, k0, 0, &sm.full[s]);
       if (++kx == (int)G) kx = 0;
     };
     const int pro = n_units < kStagesW4 ? n_units : kStagesW4;
@@ -219,7 +215,7 @@ template <int MT, int OWN>
 int launch_w4_mt(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                  void* stream) {
   CUtensorMap xmap{};
-  if (!(MT == 1 && OWN == 1) && !encode_decode_x_map(&xmap, X, v.K, M, kXStrideW4)) return (int)cudaErrorInvalidValue;
+  if (!encode_decode_x_map(&xmap, X, v.K, M, kXStrideW4)) return (int)cudaErrorInvalidValue;
   const size_t smem = sizeof(W4Smem<MT>) + 128;
   static std::atomic<uint64_t> attr_done{0};
   if (const int e = smem_attr_once(w4_decode_kernel<MT, OWN>, smem, attr_done)) return e;
@@ -320,8 +316,8 @@ int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M
 
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
+  if (M == 1) return launch_w4_gemv1(v, X, Y, ws, stream);
   grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms);
-  if (M == 1) return launch_w4_mt<1, 1>(v, X, Y, M, ws, grid, stream);
   if (M <= 4) return launch_w4_mt<1, 4>(v, X, Y, M, ws, grid, stream);
   if (M <= 8) return launch_w4_mt<1, 0>(v, X, Y, M, ws, grid, stream);
   return launch_w4_mt<2, 0>(v, X, Y, M, ws, grid, stream);

@@ -1027,9 +1027,21 @@ int qlin_spqr_view_of(qlin_layer* h, SpqrView* out) {
   return QLIN_OK;
 }
 
+// Partial-sum slots the decode launches of a layer may use (one per CTA, or per worker of
+// the single-token kernels), for the workspace sizing.
 static int decode_grid(const qlin_layer* L) {
   const int64_t units = (int64_t)L->RG * L->KU;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)kMaxCtasPerSm * sm_count_cached()));
+  const int sms = sm_count_cached();
+  int64_t g = std::min<int64_t>(units, (int64_t)kMaxCtasPerSm * sms);
+  if (L->format == QLIN_FMT_W4G128 || L->format == QLIN_FMT_SPQR)
+    g = std::max<int64_t>(g, gemv1_slots(units, sms, L->format == QLIN_FMT_SPQR));
+  if (L->format == QLIN_FMT_SPQR) {
+    SpqrView v{};
+    v.RG = L->RG;
+    v.S = L->KU;
+    for (int M = 2; M <= 16; ++M) g = std::max<int64_t>(g, spqr_decode_grid(v, M, sms));
+  }
+  return (int)std::max<int64_t>(1, g);
 }
 
 // workspace carve-up
@@ -1343,6 +1355,9 @@ qlin_status qlin_bind(qlin_handle h, void* dev_weights, size_t bytes, qlin_strea
   if (e != cudaSuccess) return QLIN_ERR_CUDA;
   h->dev = (uint8_t*)dev_weights;
   h->dev_bytes = bytes;
+  // the allocation-free SpQR forward's scratch array goes onto the device now, while device
+  // memory is free (best effort: qlin_forward_spqr_static reports a failure itself)
+  if (h->format == QLIN_FMT_SPQR) qlin_static_scratch_prepare();
   return QLIN_OK;
 }
 
@@ -1351,6 +1366,7 @@ qlin_status qlin_attach(qlin_handle h, void* dev_weights, size_t bytes) {
   if (bytes < h->image.size() || ((uintptr_t)dev_weights & 255u)) return QLIN_ERR_INVALID_ARG;
   h->dev = (uint8_t*)dev_weights;
   h->dev_bytes = bytes;
+  if (h->format == QLIN_FMT_SPQR) qlin_static_scratch_prepare();  // as in qlin_bind
   return QLIN_OK;
 }
 

@@ -125,6 +125,14 @@ int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M
 int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, const int32_t* kbound, uint16_t* Y,
                       int32_t* acc, int M, int32_t* status, void* stream);
 int spqr_decode_grid(const SpqrView& v, int M, int sms);
+// Single-token (M == 1) decode of W4 and SpQR (kern_gemv1.cu); the multi-token launchers
+// above hand M == 1 to these.  gemv1_slots: partial-sum slots (workers) such a launch uses.
+int launch_spqr_gemv1(const SpqrView& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream);
+int launch_w4_gemv1(const W4View& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream);
+int gemv1_slots(int64_t units, int sms, bool spqr);
+// Loads the allocation-free SpQR forward's fixed scratch array on the current device
+// (kern_static_ws.cu); returns a qlin_status.
+int qlin_static_scratch_prepare();
 
 }  // namespace qlin
 
