@@ -150,6 +150,24 @@ def spqr_layer(N: int, K: int, M: int, seed: int = 0):
     return W, X
 
 
+def spqr_quiet_group_layer(N: int, K: int, seed: int = 0):
+    """An SpQR test layer with one near-silent 16-group per row.
+
+    W ~ N(0, 0.02^2); in row r the entries of 16-group (5 r) mod (K / 16) are scaled by 1e-3,
+    except one (entry r mod 16 of the group), which is set to 1 + r 2^-10 -- larger than every
+    other weight, distinct per row.  With N outliers the large values are exactly the outlier
+    set, and the group's other entries are far below its supergroup's scales (the case where
+    a group's 3-bit scale code is 0).
+    """
+    W = normal(seed, KEY_W, 0.02, (N, K))
+    G = K // 16
+    for r in range(N):
+        g = (5 * r) % G
+        W[r, 16 * g:16 * g + 16] *= np.float32(1e-3)
+        W[r, 16 * g + r % 16] = np.float32(1.0 + r * 2.0 ** -10)
+    return W.astype(np.float32)
+
+
 def gptq_calibration(S: int, K: int, seed: int = 0, block: int = 16) -> np.ndarray:
     """Calibration rows for the GPTQ packer: fp32 [S, K] of bf16 values.
 

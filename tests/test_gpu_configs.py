@@ -28,6 +28,17 @@ def _rows(Y, rows_m, rows_n):
     return bits_to_f32(y.cpu().numpy().view(np.uint16))
 
 
+def _tile_sample(n, tile, seed):
+    """One index in every tile of `tile` consecutive indices, at an offset that moves from tile
+    to tile (so every tile of the kernel's grid, and every position class inside a tile, is
+    reached), plus the first and the last index."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, n, tile)
+    offs = (rng.integers(0, tile, size=len(starts)) + 37 * np.arange(len(starts))) % tile
+    s = np.minimum(starts + offs, n - 1)
+    return np.unique(np.concatenate([s, [0, n - 1]]))
+
+
 def _sample(n, count, seed):
     rng = np.random.default_rng(seed)
     s = np.sort(rng.choice(n, size=min(count, n), replace=False))
@@ -115,9 +126,11 @@ def test_decode_sweep_spqr(qlin, K, N, frac):
 @pytest.mark.parametrize("K,N", [(8192, 28672), (28672, 8192)])
 @pytest.mark.parametrize("fmt", ["w4", "spqr", "w8a8"])
 def test_prefill_4096(qlin, K, N, fmt):
+    """Every 128-row weight tile and every 256-token tile of the M = 4096 grid is sampled at
+    least once (one row / token per tile at a moving offset, plus extra tokens)."""
     M = 4096
-    ms = _sample(M, 24, 4)
-    ns = _sample(N, 160, 5)
+    ms = np.union1d(_tile_sample(M, 256, 4), _sample(M, 12, 6))
+    ns = _tile_sample(N, 128, 5)
     if fmt == "w8a8":
         W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
         layer = qlin.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)

@@ -92,7 +92,8 @@ def test_w4_gptq_layer(qlin, M, act):
 @pytest.mark.parametrize("kind", ["w4", "w4_act", "spqr", "w8a8"])
 def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
     """A layer saved and loaded back (qlin_import, no requantization) gives the same outputs
-    bit for bit as the layer that was saved, decode and prefill."""
+    bit for bit as the layer that was saved, decode and prefill, and matches the oracle run on
+    the loaded canonical arrays (W8A8 bit for bit, the others within the tolerance)."""
     N, K = 160, 1024
     if kind == "w4":
         W, X = synth.gptq_layer(N, K, 40, seed=41)
@@ -111,8 +112,27 @@ def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
     L.save(tmp_path / "layer.npz")
     L2 = qlin.QLinear.load(tmp_path / "layer.npz")
     a, b = L.to("cuda", max_M=40), L2.to("cuda", max_M=40)
+    # the oracle on the loaded canonical arrays alone (no packer involved)
+    c = L2.export()
+    x = bits_to_f32(X)
+    if kind == "w8a8":
+        qx, sx = smoothquant.quantize_activations(x, c["s_inv"])
+        y_ora = smoothquant.epilogue(smoothquant.accumulate(qx, c["qw"]), sx, c["sw"])
+    elif kind == "spqr":
+        w_hat = spqr.dequantize_canonical(N, K, c["codes"], c["qs_bits"], c["qz_bits"], c["stats"], c["rowptr"],
+                                          c["col"], c["val"])
+    else:
+        w_hat = gptq_w4.dequantize(gptq_w4.unpack_codes(c["codes"]), c["scale"], c["zero"])
+        if kind == "w4_act":  # codes of W[:, perm]: the forward multiplies by X[:, perm]
+            x = x[:, c["perm"]]
     for M in (1, 40):
-        assert np.array_equal(_y(a, X[:M], M).view(np.uint32), _y(b, X[:M], M).view(np.uint32))
+        yb = _y(b, X[:M], M)
+        assert np.array_equal(_y(a, X[:M], M).view(np.uint32), yb.view(np.uint32))
+        if kind == "w8a8":
+            assert np.array_equal(yb.view(np.uint32), y_ora[:M].view(np.uint32))
+        else:
+            ok, worst = forward.within_tolerance(yb, *forward.reference(x[:M], w_hat))
+            assert ok, (M, worst)
 
 
 def test_forward_host_graph_replays(qlin):
@@ -164,8 +184,7 @@ def test_spqr_device_dequant_bit_exact(qlin, N, K, frac):
 @pytest.mark.parametrize("N,K,frac", [(128, 512, 0.01), (100, 768, 0.02), (1000, 2048, 0.01), (192, 1024, 0.001)])
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
 def test_spqr_forward_tolerance(qlin, N, K, frac, M):
-    """frac = 0.001 leaves most (unit, row tile) buckets with fewer than eight outliers, the
-    size below which the M == 1 kernel does not use the quad counts."""
+    """frac = 0.001 leaves most (unit, row tile) outlier buckets nearly empty; 0.02 fills them."""
     W, X = synth.spqr_layer(N, K, M, seed=M)
     layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
@@ -228,6 +247,28 @@ def test_spqr_one_hot_rows(qlin):
         ref = w_hat[:, k].astype(np.float64)
         bound = 2.0 ** -7 * (np.abs(ref) + sh[:, k] * (7 + zh[:, k])) + 1e-9
         assert np.all(np.abs(y[i] - ref) <= bound), k
+
+
+def test_spqr_zero_dequantized_scale_groups(qlin):
+    """Groups whose 3-bit scale code is 0 (dequantized scale exactly 0, codes 0, the group's
+    outlier kept as fp16(w)): device dequantization bit-exact, decode (M = 1, 5) and prefill
+    (M = 40) within tolerance, and the one-hot columns of the outliers bit-exact at M = 1."""
+    N, K = 128, 512
+    W = synth.spqr_quiet_group_layer(N, K, seed=4)
+    frac = (N + 0.5) / (N * K)
+    p = spqr.pack(W, frac)
+    layer = qlin.QLinear.from_spqr(W, frac).to("cuda", max_M=40)
+    assert layer.handle.info.nnz == N
+    wd = layer.dequant_device().cpu().numpy()
+    assert np.array_equal(wd.view(np.uint32), p["w_hat"].view(np.uint32))
+    for M in (1, 5, 40):
+        X = synth.activations_bf16(4, M, K)
+        _check(_y(layer, X, M), X, p["w_hat"])
+    for k in sorted({int(np.flatnonzero(p["mask"][r])[0]) for r in range(0, N, 9)}):
+        X = np.zeros((1, K), dtype=np.float32)
+        X[0, k] = 1.0
+        y = _y(layer, synth.f32_to_bf16(X), 1)
+        assert np.array_equal(y[0], bf16_round(p["w_hat"][:, k])), k
 
 
 # ----------------------------------------------------------------------------- W8A8

@@ -250,6 +250,39 @@ def test_spqr_all_outlier_group():
     assert float(p["s_g"][0, 0]) == 1.0 and float(p["z_g"][0, 0]) == 0.0
 
 
+def test_spqr_zero_dequantized_scale_group():
+    """SpQR page, "İddia ve Gerçeklik: SpQR" (bi-level statistics), reading 3: the 16 group
+    scales of a supergroup are themselves 3-bit RTN codes; scales are non-negative, so the
+    second-level zero zs is 0 and a group whose scale is below ss / 2 gets qs = 0, a
+    dequantized scale of exactly 0, every dense code 0 (reading 5) and D = 0 -- so an outlier
+    in that group keeps fp16(w) itself (reading 7: the residual w - D with D = 0)."""
+    N, K = 8, 512
+    W = synth.spqr_quiet_group_layer(N, K, seed=3)
+    frac = (N + 0.5) / (N * K)
+    p = spqr.pack(W, frac)
+    G = K // 16
+    assert int(p["mask"].sum()) == N == spqr.outlier_count(N, K, frac)
+    assert np.all(p["stats"][:, :, 1].astype(np.float32) == 0)  # zs = 0: scales are >= 0
+    for r in range(N):
+        g = (5 * r) % G
+        sl = slice(16 * g, 16 * g + 16)
+        ss = float(p["stats"][r, g // 16, 0])
+        assert float(p["s_g"][r, g]) < ss / 2  # the first-level scale rounds to code 0
+        assert p["qs"][r, g] == 0 and p["s_hat"][r, g] == 0
+        assert np.all(p["q"][r, sl] == 0) and np.all(p["D"][r, sl] == 0)
+        k = int(np.flatnonzero(p["mask"][r])[0])
+        assert k == 16 * g + r % 16
+        v = p["val"][p["rowptr"][r]]
+        assert v == np.float16(W[r, k]) and p["w_hat"][r, k] == np.float32(np.float16(W[r, k]))
+        others = np.delete(p["w_hat"][r, sl], r % 16)
+        assert np.all(others == 0)
+    # the quiet groups are the only zero scales; everything else dequantizes normally
+    assert int((p["s_hat"] != 0).sum()) == N * G - N
+    wc = spqr.dequantize_canonical(N, K, p["codes"], p["qs_bits"], p["qz_bits"], p["stats"], p["rowptr"],
+                                   p["col"], p["val"])
+    assert np.array_equal(wc.view(np.uint32), p["w_hat"].view(np.uint32))
+
+
 def test_spqr_bits_per_param_in_page_range(figures):
     lo, hi = figures["spqr_bits_per_param_range"]
     N, K = 32, 4096
