@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -159,10 +160,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "_work", f"clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="qlin_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
@@ -237,34 +238,48 @@ class Rotated:
         self.q.qlin_attach(self.layer.handle, self.copies[i % self.R].data_ptr(), self.nb)
         self.q.qlin_forward(self.layer.handle, self.X, self.Y, self.X.shape[0], self.stream)
 
-    def capture(self):
+    def _graph(self, n):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(n):
+                self.forward(i)
+        torch.cuda.synchronize()
+        return g
+
+    def capture(self, rem: int = 0):
+        """A graph of R forwards (one per copy) and, if rem > 0, one of the first rem forwards,
+        so that any step count is timed exactly (R-graphs, then the remainder)."""
         import torch
         for i in range(self.R):  # warm: sets kernel attributes outside capture
             self.forward(i)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=self.stream):
-            for i in range(self.R):
-                self.forward(i)
-        torch.cuda.synchronize()
-        self.graph = g
-        return g
+        self.graph = self._graph(self.R)
+        self.graph_rem = self._graph(rem) if rem > 0 else None
+        self.rem = rem
+        return self.graph
 
 
 def _time_steps(rot, steps, warmup, dist_ctx):
+    """Times exactly `steps` forwards: steps // R replays of the R-forward graph, then the
+    remainder graph (captured by rot.capture(steps % R))."""
     import torch
     R = rot.R
+    steps = max(1, steps)
+    reps, rem = divmod(steps, R)
+    if rem and (rot.graph_rem is None or rem != rot.rem):
+        raise ValueError("capture the remainder graph with rot.capture(steps % R) first")
     for _ in range(max(1, math.ceil(warmup / R))):
         rot.graph.replay()
     torch.cuda.synchronize()
-    reps = max(1, steps // R)
-    steps = reps * R
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()
     torch.cuda.synchronize()
     ev0.record(rot.stream)
     for _ in range(reps):
         rot.graph.replay()
+    if rem:
+        rot.graph_rem.replay()
     ev1.record(rot.stream)
     torch.cuda.synchronize()
     dist_ctx.barrier()
@@ -339,7 +354,7 @@ def _extra_configs(q, torch, stream, l2):
         R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
         rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
         rot.capture()
-        steps, ms = _time_steps(rot, 20000, 200, DistCtx.__new__(_NoDist))
+        steps, ms = _time_steps(rot, (20000 // R) * R, 200, DistCtx.__new__(_NoDist))
         out["w4g128_4096x4096_M1"] = {"GB/s": round(nbytes / (ms / steps / 1e3) / 1e9, 1),
                                       "us_per_forward": round(ms / steps * 1e3, 3), "weight_bytes": nbytes}
         del rot, layer
@@ -349,7 +364,7 @@ def _extra_configs(q, torch, stream, l2):
         R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
         rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
         rot.capture()
-        steps, ms = _time_steps(rot, 20000, 200, DistCtx.__new__(_NoDist))
+        steps, ms = _time_steps(rot, (20000 // R) * R, 200, DistCtx.__new__(_NoDist))
         t = ms / steps / 1e3
         out["w8a8_4096x4096_M16"] = {"GB/s": round(nbytes / t / 1e9, 1), "us_per_forward": round(t * 1e6, 3),
                                      "TOPS": round(2 * 16 * 4096 * 4096 / t / 1e12, 2), "weight_bytes": nbytes}
@@ -465,7 +480,7 @@ def run_gpu(args):
         R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
         Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
         rot = Rotated(q, layer, Xd, R, stream)
-        rot.capture()
+        rot.capture(max(1, args.steps) % R)
         with ClockSampler(dist_ctx.local) as clk:
             steps, ms = _time_steps(rot, args.steps, args.warmup, dist_ctx)
         clocks = clk.summary()
