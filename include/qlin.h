@@ -206,7 +206,7 @@ qlin_status qlin_forward(qlin_handle h, const void* X, void* Y, int M, qlin_stre
  * (or else at the first call of this function) -- and held until the process exits.  Make
  * that first bind or call before any stream capture and before the device's memory is
  * reserved for other uses.
- * Limits: layers of at most 81,600 units of 64 rows x 256 columns (ceil(N / 64) * K / 256), at
+ * Limits: layers of at most 162,560 units of 64 rows x 256 columns (ceil(N / 64) * K / 256), at
  * most 524,288 rows, on devices of at most 160 SMs; beyond them the call returns
  * QLIN_ERR_WORKSPACE.  Each call clears the counters it uses; the array is shared by every
  * call, so calls whose kernels overlap on the GPU (other streams, other threads) race and

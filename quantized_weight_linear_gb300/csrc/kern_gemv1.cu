@@ -12,10 +12,11 @@
 //   for W4, a 256-wide supergroup for SpQR) and its own shared-memory ring, which its
 //   producer fills with cp.async.bulk while it prefetches the units after the ring into L2
 //   (the streamed copies are marked evict-first, so they do not push prefetched lines out);
-// * one CTA per SM, held to half of an SM's registers and (for the common widths) shared
-//   memory, so that under programmatic dependent launch the CTAs of the next forward on the
-//   stream become resident beside it and fill their rings with weights (which never depend
-//   on the previous kernel) while this forward still computes;
+// * two CTAs per SM (sixteen consumer warps keep the issue slots busy; the work is issue
+//   bound).  Under programmatic dependent launch a CTA of the next forward issues its first
+//   weight copies and L2 prefetches (weights never depend on the previous kernel) as soon as
+//   a CTA of this one leaves its SM.  (Measured alternatives: one CTA of four groups, and one
+//   co-resident CTA of two groups per forward, were as fast or slower.);
 // * the token's activations are copied into shared memory once per CTA (the K units its
 //   range touches, after griddepcontrol.wait) and the sums of x that the formulation needs
 //   are prepared once per CTA, so a unit costs only its weight bytes;
@@ -35,8 +36,15 @@
 namespace qlin {
 namespace {
 
-constexpr int kG1Groups = 2;                         // workers per CTA
-constexpr int kG1Consumers = 4 * kG1Groups;          // consumer warps
+#ifndef QLIN_G1_GROUPS
+#define QLIN_G1_GROUPS 2
+#endif
+#ifndef QLIN_G1_CTAS_PER_SM
+#define QLIN_G1_CTAS_PER_SM 2
+#endif
+constexpr int kG1Groups = QLIN_G1_GROUPS;                     // workers per CTA
+constexpr int kG1CtasPerSm = QLIN_G1_CTAS_PER_SM;             // CTAs of one forward per SM
+constexpr int kG1Consumers = 4 * kG1Groups;                    // consumer warps
 constexpr int kG1Threads = 32 * (kG1Consumers + kG1Groups);  // + one producer warp per group
 constexpr int kG1MaxStages = 8;
 #ifndef QLIN_G1_SP_STAGES
@@ -45,7 +53,7 @@ constexpr int kG1MaxStages = 8;
 #ifndef QLIN_G1_W4_STAGES
 #define QLIN_G1_W4_STAGES 4
 #endif
-constexpr int kG1SpStages = QLIN_G1_SP_STAGES;
+constexpr int kG1SpStages = QLIN_G1_SP_STAGES;  // ring depth per group (one less if it does not fit)
 constexpr int kG1W4Stages = QLIN_G1_W4_STAGES;
 // units a producer prefetches into L2 ahead of its shared-memory ring: with the ring this
 // keeps about 100 KB per group in flight from DRAM, and the co-resident next forward's
@@ -55,14 +63,10 @@ constexpr int kG1W4Stages = QLIN_G1_W4_STAGES;
 #endif
 constexpr int kG1SpPrefetch = QLIN_G1_PREFETCH ? 12 : 0;
 constexpr int kG1W4Prefetch = QLIN_G1_PREFETCH ? 24 : 0;
-constexpr uint32_t kG1WaitHintNs = 20000;
-#ifndef QLIN_G1_CTAS_PER_SM
-#define QLIN_G1_CTAS_PER_SM 2
-#endif
-constexpr int kG1CtasPerSm = QLIN_G1_CTAS_PER_SM;  // CTAs of one forward per SM  // suspend-time hint of a consumer's barrier poll
+constexpr uint32_t kG1WaitHintNs = 20000;  // suspend-time hint of a consumer's barrier poll
 constexpr int kG1OutCap = 504;    // outlier entries staged with a unit (more: read from global)
 constexpr int kG1OutWords = 512;  // words of a stage's outlier area (the copy is 16-byte aligned)
-constexpr int kG1OffsCap = 1024;  // staged bucket offsets per CTA: ranges of at most 255 units
+constexpr int kG1OffsCap = 2048;  // staged bucket offsets per CTA: ranges of at most 511 units
 constexpr int kG1MaxUnitsPerCta = kG1OffsCap / 4 - 1;
 constexpr size_t kG1MaxSmem = 227 * 1024;  // dynamic shared memory limit of a CTA
 
@@ -104,12 +108,12 @@ namespace {
 
 inline uint32_t al128(uint32_t x) { return (x + 127u) & ~127u; }
 
-G1Layout g1_layout(bool spqr, int xn) {
+G1Layout g1_layout(bool spqr, int xn, int stages) {
   G1Layout L{};
   uint32_t o = al128((uint32_t)sizeof(G1Hdr));
   L.stage_bytes = spqr ? al128(kSpqrUnitBytes + kG1OutWords * 4) : al128(kW4UnitBytes);
   L.ring = o;
-  o += L.stage_bytes * kG1Groups * (spqr ? kG1SpStages : kG1W4Stages);
+  o += L.stage_bytes * kG1Groups * stages;
   if (spqr) {
     L.offs = o;
     o = al128(o + kG1OffsCap * 4);
@@ -138,7 +142,7 @@ __device__ __forceinline__ int64_t g1_div(int64_t a, int64_t b) {
   return (int64_t)((uint32_t)a / (uint32_t)b);
 }
 
-// Work plan of a CTA, computed by warp 0: the two workers' unit ranges, where their ranges
+// Work plan of a CTA, computed by warp 0: its workers' unit ranges, where their ranges
 // share row groups with other workers, and the K units of x the CTA needs.  Worker w owns
 // units [w U / W, (w + 1) U / W); the owner of unit u is ((u + 1) W - 1) / U.
 __device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane) {
@@ -176,6 +180,13 @@ __device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane) {
           }
         }
       }
+    } else if (s == 0 && u0 < U) {
+      // an empty range (more workers than units) that sits inside a shared row group still
+      // counts among its contributors: it contributes zeros
+      const int64_t r = g1_div(u0, per_rg);
+      const int64_t first = g1_div((r * per_rg + 1) * W - 1, U);
+      const int64_t last = g1_div((r * per_rg + per_rg) * W - 1, U);
+      if (first < w && w <= last) out = (int)r;
     }
     h.rg[g][s] = out;
   }
@@ -416,7 +427,7 @@ __device__ __forceinline__ void sp_mma(const uint32_t (&w)[6], const SpOr& k, co
 }
 
 template <int STAGES>
-__global__ void __launch_bounds__(kG1Threads, 2)
+__global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     spqr_gemv1_kernel(SpqrView v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, Workspace ws,
                       G1Layout L) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -770,13 +781,17 @@ __global__ void __launch_bounds__(kG1Threads, 2)
     ++cur_rg;
     kq = 0;
   }
+  if (n_units == 0 && fin.rg0 >= 0 && t == 0) {  // an empty range inside a shared row group
+    fin.stage(fin.rg0, rt * 16 + g, 0.f, done);
+    fin.stage(fin.rg0, rt * 16 + g + 8, 0.f, done);
+  }
   fin.finish(cs, threadIdx.x - grp * 128, done);
 }
 
 // ---------------------------------------------------------------------------------- W4
 
 template <int STAGES>
-__global__ void __launch_bounds__(kG1Threads, 2)
+__global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     w4_gemv1_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, Workspace ws, G1Layout L) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sb = smem_align128(smem_raw);
@@ -952,6 +967,10 @@ __global__ void __launch_bounds__(kG1Threads, 2)
     ++cur_rg;
     kq = 0;
   }
+  if (n_units == 0 && fin.rg0 >= 0 && t == 0) {  // an empty range inside a shared row group
+    fin.stage(fin.rg0, rt * 16 + g, 0.f, done);
+    fin.stage(fin.rg0, rt * 16 + g + 8, 0.f, done);
+  }
   fin.finish(cs, threadIdx.x - grp * 128, done);
 }
 
@@ -961,17 +980,21 @@ int g1_grid(int64_t U, int sms, bool spqr) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(grid, 1 << 30));
 }
 
-template <typename Kernel, typename View>
-int g1_launch(Kernel* kernel, std::atomic<uint64_t>& attr_done, const View& v, int64_t U, int64_t per_rg, bool spqr,
-              const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
+// Launches with the deepest ring (of `deep` stages, or one less) whose shared memory fits.
+template <typename KDeep, typename KShallow, typename View>
+int g1_launch(KDeep* kdeep, KShallow* kshallow, int deep, std::atomic<uint64_t>* attr_done, const View& v, int64_t U,
+              int64_t per_rg, bool spqr, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
   const int grid = g1_grid(U, ws.sms, spqr);
   if ((int64_t)grid * kG1Groups > ws.grid) return (int)cudaErrorInvalidValue;  // workspace slots
   const int xn = (int)std::min<int64_t>(per_rg, (U + grid - 1) / grid);
-  const G1Layout L = g1_layout(spqr, xn);
+  int stages = deep;
+  G1Layout L = g1_layout(spqr, xn, stages);
+  if ((size_t)L.bytes + 128 > kG1MaxSmem) {
+    stages = deep - 1;
+    L = g1_layout(spqr, xn, stages);
+  }
   const size_t smem = (size_t)L.bytes + 128;
   if (smem > kG1MaxSmem) return (int)cudaErrorInvalidValue;
-  // raised once per device to the largest size any layer needs
-  if (const int e = smem_attr_once(kernel, kG1MaxSmem, attr_done)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kG1Threads);
@@ -982,7 +1005,13 @@ int g1_launch(Kernel* kernel, std::atomic<uint64_t>& attr_done, const View& v, i
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, kernel, v, X, Y, ws, L);
+  // the shared-memory limit is raised once per device to the largest size any layer needs
+  if (stages == deep) {
+    if (const int e = smem_attr_once(kdeep, kG1MaxSmem, attr_done[0])) return e;
+    return (int)cudaLaunchKernelEx(&cfg, kdeep, v, X, Y, ws, L);
+  }
+  if (const int e = smem_attr_once(kshallow, kG1MaxSmem, attr_done[1])) return e;
+  return (int)cudaLaunchKernelEx(&cfg, kshallow, v, X, Y, ws, L);
 }
 
 }  // namespace
@@ -990,13 +1019,15 @@ int g1_launch(Kernel* kernel, std::atomic<uint64_t>& attr_done, const View& v, i
 int gemv1_slots(int64_t units, int sms, bool spqr) { return g1_grid(units, sms, spqr) * kG1Groups; }
 
 int launch_spqr_gemv1(const SpqrView& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
-  static std::atomic<uint64_t> attr_done{0};
-  return g1_launch(spqr_gemv1_kernel<kG1SpStages>, attr_done, v, (int64_t)v.RG * v.S, v.S, true, X, Y, ws, stream);
+  static std::atomic<uint64_t> attr_done[2];
+  return g1_launch(spqr_gemv1_kernel<kG1SpStages>, spqr_gemv1_kernel<kG1SpStages - 1>, kG1SpStages, attr_done, v,
+                   (int64_t)v.RG * v.S, v.S, true, X, Y, ws, stream);
 }
 
 int launch_w4_gemv1(const W4View& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
-  static std::atomic<uint64_t> attr_done{0};
-  return g1_launch(w4_gemv1_kernel<kG1W4Stages>, attr_done, v, (int64_t)v.RG * v.G, v.G, false, X, Y, ws, stream);
+  static std::atomic<uint64_t> attr_done[2];
+  return g1_launch(w4_gemv1_kernel<kG1W4Stages>, w4_gemv1_kernel<kG1W4Stages - 1>, kG1W4Stages, attr_done, v,
+                   (int64_t)v.RG * v.G, v.G, false, X, Y, ws, stream);
 }
 
 }  // namespace qlin

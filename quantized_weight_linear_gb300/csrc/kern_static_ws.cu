@@ -10,7 +10,7 @@
 // `g_spqr_static_scratch` below.
 //
 // Limits of the fixed array: partial-sum slots for at most kStaticMaxGrid CTAs or workers,
-// which holds every layer of at most 81,600 units of 64 rows x 256 columns (RG x K / 256) on a
+// which holds every layer of at most 162,560 units of 64 rows x 256 columns (RG x K / 256) on a
 // device of at most 160 SMs, and kStaticMaxRowGroups row groups of 64 output rows
 // (N <= 524288); larger requests return QLIN_ERR_WORKSPACE.  The array (about 8 MB) is part of
 // this library's device module: it is taken on a device when the module is loaded there --

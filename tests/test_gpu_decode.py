@@ -271,6 +271,22 @@ def test_spqr_zero_dequantized_scale_groups(qlin):
         assert np.array_equal(y[0], bf16_round(p["w_hat"][:, k])), k
 
 
+@pytest.mark.parametrize("fmt,N,K", [("w4", 64, 128), ("w4", 64, 256), ("w4", 128, 384), ("w4", 192, 640),
+                                     ("spqr", 64, 256), ("spqr", 64, 512), ("spqr", 128, 768), ("spqr", 200, 1024)])
+def test_single_token_tiny_layers(qlin, fmt, N, K):
+    """Layers with fewer units than the single-token kernel has workers: some workers get no
+    units (and must still complete the row groups they sit in), twice in a row."""
+    if fmt == "w4":
+        W, X = synth.gptq_layer(N, K, 1, seed=61)
+        layer, w_hat = qlin.QLinear.from_w4g128(W).to("cuda"), gptq_w4.pack(W)["w_hat"]
+    else:
+        W, X = synth.spqr_layer(N, K, 1, seed=61)
+        layer, w_hat = qlin.QLinear.from_spqr(W, 0.01).to("cuda"), spqr.pack(W, 0.01)["w_hat"]
+    y0 = _y(layer, X, 1)
+    _check(y0, X, w_hat)
+    assert np.array_equal(_y(layer, X, 1).view(np.uint32), y0.view(np.uint32))
+
+
 # ----------------------------------------------------------------------------- W8A8
 
 @pytest.mark.parametrize("N,K", [(128, 512), (100, 256), (256, 2048)])

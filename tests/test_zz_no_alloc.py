@@ -74,14 +74,15 @@ def _zero_spqr_layer(qlin, N, K):
     return qlin.QLinear(qlin.qlin_import(qlin.FMT_SPQR, N, K, arrays))
 
 
-# just past the array's limits: 8193 row groups of 64 rows; 638 row groups x 128 supergroups
-# = 81,664 units of 64 x 256 (the limit is 81,600)
-@pytest.mark.parametrize("N,K", [(8193 * 64, 256), (638 * 64, 32768)])
+# past the array's limits: 8193 row groups of 64 rows; 1278 row groups x 128 supergroups
+# = 163,584 units of 64 x 256 (the stated limit is 162,560; one token alone fits up to 163,520)
+@pytest.mark.parametrize("N,K", [(8193 * 64, 256), (1278 * 64, 32768)])
 def test_static_scratch_rejects_layers_beyond_its_limits(qlin, N, K):
-    layer = _zero_spqr_layer(qlin, N, K).to("cuda", max_M=1)
-    X = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
-    Y = torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(qlin.QlinError) as e:
-        qlin.qlin_forward_spqr_static(layer.handle, X, Y, 1)
-    assert e.value.status == qlin.QLIN_ERR_WORKSPACE
+    layer = _zero_spqr_layer(qlin, N, K).to("cuda", max_M=2)
+    for M in (1, 2):
+        X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(qlin.QlinError) as e:
+            qlin.qlin_forward_spqr_static(layer.handle, X, Y, M)
+        assert e.value.status == qlin.QLIN_ERR_WORKSPACE, M
     assert qlin.qlin_poll_static_status() == qlin.QLIN_OK
