@@ -234,6 +234,13 @@ class Rotated:
         self.Y = torch.empty((X.shape[0], layer.N), dtype=torch.bfloat16, device="cuda")
         self.stream = stream
 
+    def set_input(self, X):
+        """New activations (another M): fresh output buffer and graphs."""
+        import torch
+        self.X = X
+        self.Y = torch.empty((X.shape[0], self.layer.N), dtype=torch.bfloat16, device="cuda")
+        self.capture()
+
     def forward(self, i):
         self.q.qlin_attach(self.layer.handle, self.copies[i % self.R].data_ptr(), self.nb)
         self.q.qlin_forward(self.layer.handle, self.X, self.Y, self.X.shape[0], self.stream)
@@ -337,63 +344,174 @@ class DistCtx:
             self.pg.destroy_process_group()
 
 
+def _config(world: int) -> dict:
+    """The workload description both arms print (GPU and reference).  22,278,432 bytes are the
+    layer's canonical packed bytes (codes, statistics and CSR outliers at 3.95 bits per
+    weight), which the full-size parity test asserts for the packed handle."""
+    return {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "outlier_frac": FRAC, "weight_bytes": 22278432,
+            "bits_per_param": round(8 * 22278432 / (N_ * K_), 4), "parallelism": f"replicas x{world}"}
+
+
 def whole_job_gbs(nbytes: int, ms_max: float, steps: int, world: int) -> float:
     """Weight GB/s of the whole job: every rank streams its own copy of the layer once per
     step, and the job takes as long as its slowest rank (ms_max over `steps` steps)."""
     return world * nbytes / (ms_max / steps / 1e3) / 1e9
 
 
-def _extra_configs(q, torch, stream, l2):
-    """cfg0 (W4 g128 4096^2 M=1) and cfg2 (W8A8 4096^2 M=16) on the same timing scheme."""
+# ------------------------------------------------------------------------------------ all configurations
+
+DECODE_SHAPES = [(8192, 8192), (8192, 28672), (28672, 8192)]  # (K, N), the 70B-class decode sweep
+PREFILL_SHAPES = [(8192, 28672), (28672, 8192)]
+
+
+def _decode_layer(q, fmt, K, N, M, frac=0.01, seed=0):
+    """Packs a decode layer (host) and binds it; returns (layer, X bits [M, K])."""
     import qlin_synth as synth
+    if fmt == "w4g128":
+        W, X = synth.gptq_layer(N, K, M, seed=seed)
+        layer = q.QLinear.from_w4g128(W)
+    elif fmt == "spqr":
+        W, X = synth.spqr_layer(N, K, M, seed=seed)
+        layer = q.QLinear.from_spqr(W, frac)
+    elif fmt == "w8a8":
+        W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=seed)
+        layer = q.QLinear.from_w8(W, absmax, 0.85)
+    else:
+        raise ValueError(f"unknown decode format {fmt}")
+    del W
+    return layer.to("cuda", max_M=max(16, M)), X
+
+
+def _decode_kernel_name(fmt, M):
+    if fmt == "w8a8":
+        return "w8_act_quant_reg_kernel + w8_decode_kernel"
+    if M == 1:
+        return "w4_gemv1_kernel" if fmt == "w4g128" else "spqr_gemv1_kernel"
+    return "w4_decode_kernel" if fmt == "w4g128" else "spqr_decode_kernel"
+
+
+def _time_rotated(rot, torch, min_s=0.3):
+    """Exact-step timing of graph replays lasting at least min_s, with clocks sampled."""
+    R = rot.R
+    rot.graph.replay()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rot.graph.replay()
+    torch.cuda.synchronize()
+    per = max(time.perf_counter() - t0, 1e-6)
+    steps = R * max(2, math.ceil(min_s / per))
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        steps, ms = _time_steps(rot, steps, 3 * R, DistCtx.__new__(_NoDist))
+    return steps, ms, clk.summary()
+
+
+def _decode_entries(q, torch, stream, l2, peaks, fmt, K, N, Ms, frac=0.01):
+    """One layer, timed at each M on the bench's scheme: GB/s of packed weights vs HBM."""
+    layer, X = _decode_layer(q, fmt, K, N, max(Ms), frac)
+    nbytes = layer.handle.info.packed_bytes
+    R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
+    Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
+    rot = Rotated(q, layer, Xd[:Ms[0]], R, stream)
     out = {}
-    try:
-        W, X = synth.gptq_layer(4096, 4096, 1, seed=0)
-        layer = q.QLinear.from_w4g128(W).to("cuda")
-        nbytes = layer.handle.info.packed_bytes
-        R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
-        rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
-        rot.capture()
-        steps, ms = _time_steps(rot, (20000 // R) * R, 200, DistCtx.__new__(_NoDist))
-        out["w4g128_4096x4096_M1"] = {"GB/s": round(nbytes / (ms / steps / 1e3) / 1e9, 1),
-                                      "us_per_forward": round(ms / steps * 1e3, 3), "weight_bytes": nbytes}
-        del rot, layer
-        W, X, absmax, _ = synth.smoothquant_layer(4096, 4096, 16, seed=0)
-        layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=16)
-        nbytes = layer.handle.info.packed_bytes
-        R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
-        rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
-        rot.capture()
-        steps, ms = _time_steps(rot, (20000 // R) * R, 200, DistCtx.__new__(_NoDist))
+    for M in Ms:
+        rot.set_input(Xd[:M])
+        steps, ms, clocks = _time_rotated(rot, torch)
         t = ms / steps / 1e3
-        out["w8a8_4096x4096_M16"] = {"GB/s": round(nbytes / t / 1e9, 1), "us_per_forward": round(t * 1e6, 3),
-                                     "TOPS": round(2 * 16 * 4096 * 4096 / t / 1e12, 2), "weight_bytes": nbytes}
-        del rot, layer
-    except Exception as e:  # extra lines must never break the headline
-        out["error"] = repr(e)[:300]
-    out.update(_prefill_configs(q, torch, stream))
+        gbs = nbytes / t / 1e9
+        tag = f"{fmt}{'' if fmt != 'spqr' else f'_{frac * 100:g}pct'}_K{K}_N{N}_M{M}"
+        e = {"us_per_forward": round(t * 1e6, 3), "GB/s": round(gbs, 1), "weight_bytes": nbytes,
+             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(gbs / peaks["hbm_gbs"], 4)},
+             "kernel": _decode_kernel_name(fmt, M), "steps": steps, "clocks": clocks}
+        if fmt == "w8a8":
+            e["TOPS"] = round(2 * M * N * K / t / 1e12, 2)
+        out["decode_" + tag] = e
+    del rot, layer
+    return out
+
+
+def _prefill_entry(q, torch, stream, peaks, fmt, K, N, M=4096, min_s=0.3):
+    """M-token tensor-core forward: TFLOP/s (TOPS for W8A8) vs the measured bf16 dense peak."""
+    import qlin_synth as synth
+    if fmt == "w8a8":
+        W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)
+    elif fmt == "w4g128":
+        W, X = synth.gptq_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_w4g128(W).to("cuda")
+    else:
+        W, X = synth.spqr_layer(N, K, M, seed=0)
+        layer = q.QLinear.from_spqr(W, 0.01).to("cuda")
+    del W
+    Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        q.qlin_forward(layer.handle, Xd, Y, M, stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    q.qlin_forward(layer.handle, Xd, Y, M, stream)
+    torch.cuda.synchronize()
+    reps = max(10, math.ceil(min_s / max(time.perf_counter() - t0, 1e-6)))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for _ in range(reps):
+            q.qlin_forward(layer.handle, Xd, Y, M, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    t = ev0.elapsed_time(ev1) / reps / 1e3
+    st = q.qlin_poll_status(layer.handle, stream)
+    flops = 2.0 * M * N * K
+    tf = flops / t / 1e12
+    unit = "TOPS" if fmt == "w8a8" else "TFLOP/s"
+    kern = {"w4g128": "tc_gemm_kernel<W4>", "spqr": "tc_gemm_kernel<SpQR>",
+            "w8a8": "w8 act-quant + tc_gemm_kernel<W8> (int8 codes on the fp16 pipe)"}[fmt]
+    tag = f"prefill_{fmt}{'_1pct' if fmt == 'spqr' else ''}_M{M}_K{K}_N{N}"
+    del layer, Xd, Y
+    return {tag: {"ms_per_forward": round(t * 1e3, 4), unit: round(tf, 1),
+                  "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                               "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                               "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                               "peak_note": "measured bf16 dense peak (cuBLAS burst); the fp16 pipe runs at the "
+                                            "same rate" + ("; tcgen05 kind::i8 is not available on sm_103a" if
+                                                           fmt == "w8a8" else "")},
+                  "kernel": kern, "reps": reps, "status": st, "clocks": clk.summary()}}
+
+
+def _all_configs(q, torch, stream, l2, peaks):
+    """Every configuration of the workload list other than the headline (SpQR 11008 x 4096,
+    M = 1): W4 g128 4096^2 M = 1; W8A8 4096^2 at M = 16 and 2048; the 70B-class decode sweep
+    (M = 1, 4, 16; W4 g128 and SpQR at 0.5 / 1 / 2 % outliers); prefill M = 4096 on both
+    shapes for the three formats.  Each entry carries its roofline fraction and its clocks."""
+    out = {}
+
+    def guard(name, fn):
+        try:
+            out.update(fn())
+        except Exception as e:  # one failing entry must not lose the others or the headline
+            out[name + "_error"] = repr(e)[:300]
+
+    guard("cfg0", lambda: _decode_entries(q, torch, stream, l2, peaks, "w4g128", 4096, 4096, (1,)))
+    guard("cfg2_decode", lambda: _decode_entries(q, torch, stream, l2, peaks, "w8a8", 4096, 4096, (16,)))
+    guard("cfg2_prefill", lambda: _prefill_entry(q, torch, stream, peaks, "w8a8", 4096, 4096, M=2048))
+    for K, N in DECODE_SHAPES:
+        guard(f"cfg3_w4_{K}_{N}", lambda: _decode_entries(q, torch, stream, l2, peaks, "w4g128", K, N, (1, 4, 16)))
+        for frac in (0.005, 0.01, 0.02):
+            guard(f"cfg3_spqr_{frac}_{K}_{N}",
+                  lambda: _decode_entries(q, torch, stream, l2, peaks, "spqr", K, N, (1, 4, 16), frac))
+    for K, N in PREFILL_SHAPES:
+        for fmt in ("w4g128", "spqr", "w8a8"):
+            guard(f"cfg4_{fmt}_{K}_{N}", lambda: _prefill_entry(q, torch, stream, peaks, fmt, K, N))
     return out
 
 
 def _decode_case(q, torch, stream, l2, spec, steps=4000):
     """One decode configuration "fmt,K,N,M[,outlier_frac]" (fmt w4g128 | spqr | w8a8) on the
     bench's timing scheme (rotated resident copies, CUDA graph replays): for profiling lines."""
-    import qlin_synth as synth
     parts = spec.split(",")
     fmt, K, N, M = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
     frac = float(parts[4]) if len(parts) > 4 else 0.01
-    if fmt == "w4g128":
-        W, X = synth.gptq_layer(N, K, M, seed=0)
-        layer = q.QLinear.from_w4g128(W).to("cuda", max_M=16)
-    elif fmt == "spqr":
-        W, X = synth.spqr_layer(N, K, M, seed=0)
-        layer = q.QLinear.from_spqr(W, frac).to("cuda", max_M=16)
-    elif fmt == "w8a8":
-        W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
-        layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=16)
-    else:
-        raise ValueError(f"unknown decode format {fmt}")
-    del W
+    layer, X = _decode_layer(q, fmt, K, N, M, frac)
     nbytes = layer.handle.info.packed_bytes
     R = max(2, math.ceil(4 * l2 / q.qlin_device_bytes(layer.handle)))
     rot = Rotated(q, layer, torch.from_numpy(X).cuda().view(torch.bfloat16), R, stream)
@@ -404,44 +522,11 @@ def _decode_case(q, torch, stream, l2, spec, steps=4000):
                                               "weight_bytes": nbytes}}
 
 
-def _prefill_configs(q, torch, stream, fmts=("w4g128", "spqr1pct", "w8a8")):
-    """Prefill M=4096 on K=8192, N=28672 for the three formats (tensor-core path): TFLOP/s."""
-    import qlin_synth as synth
+def _prefill_configs(q, torch, stream, fmts=("w4g128", "spqr", "w8a8")):
+    """Prefill M=4096 on K=8192, N=28672 (profiling entry point)."""
     out = {}
-    M, K, N = 4096, 8192, 28672
-    flops = 2.0 * M * N * K
     for fmt in fmts:
-        try:
-            if fmt == "w8a8":
-                W, X, absmax, _ = synth.smoothquant_layer(N, K, M, seed=0)
-                layer = q.QLinear.from_w8(W, absmax, 0.85).to("cuda", max_M=M)
-            elif fmt == "w4g128":
-                W, X = synth.gptq_layer(N, K, M, seed=0)
-                layer = q.QLinear.from_w4g128(W).to("cuda")
-            else:
-                W, X = synth.spqr_layer(N, K, M, seed=0)
-                layer = q.QLinear.from_spqr(W, 0.01).to("cuda")
-            del W
-            Xd = torch.from_numpy(X).cuda().view(torch.bfloat16)
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-            for _ in range(3):
-                q.qlin_forward(layer.handle, Xd, Y, M, stream)
-            torch.cuda.synchronize()
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 10
-            ev0.record(stream)
-            for _ in range(reps):
-                q.qlin_forward(layer.handle, Xd, Y, M, stream)
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            t = ev0.elapsed_time(ev1) / reps / 1e3
-            out[f"prefill_{fmt}_M4096_K8192_N28672"] = {"TFLOP/s": round(flops / t / 1e12, 1),
-                                                         "ms_per_forward": round(t * 1e3, 3),
-                                                         "pipe": "fp16 tensor (exact int8 codes)" if fmt == "w8a8"
-                                                         else "bf16 tensor"}
-            del layer, Xd, Y
-        except Exception as e:
-            out[f"prefill_{fmt}_error"] = repr(e)[:300]
+        out.update(_prefill_entry(q, torch, stream, _peaks(), fmt, 8192, 28672, min_s=0.05))
     return out
 
 
@@ -491,7 +576,7 @@ def run_gpu(args):
         value = whole_job_gbs(nbytes, ms_max, steps, dist_ctx.world)
         e2e_t, h2d, d2h = _e2e(q, layer, rot, M_, args.e2e_steps)
         e2e_t = dist_ctx.max(e2e_t)
-        extra = _extra_configs(q, torch, stream, l2) if (dist_ctx.rank == 0 and not args.no_extra) else {}
+        extra = _all_configs(q, torch, stream, l2, peaks) if (dist_ctx.rank == 0 and not args.no_extra) else {}
 
     achieved = nbytes / (ms / steps / 1e3) / 1e9  # this rank's kernel
     line = {
@@ -499,13 +584,10 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(ms_max / steps, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32 (3-bit codes, fp16 stats/outliers)",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "outlier_frac": FRAC, "weight_bytes": nbytes,
-                   "bits_per_param": round(layer.handle.info.bits_per_param, 4),
-                   "l2": f"inputs larger than L2: {R} resident weight copies rotated "
-                         f"({R * q.qlin_device_bytes(layer.handle) / 1e6:.0f} MB > 4x {l2 / 1e6:.0f} MB L2)",
-                   "issue": f"CUDA graph replays of {R} forwards, programmatic dependent launch between forwards",
-                   "parallelism": f"replicas x{dist_ctx.world}",
-                   "host_pack_s": round(t_pack, 3)},
+        "config": dict(_config(dist_ctx.world), host_pack_s=round(t_pack, 3),
+                       l2=f"inputs larger than L2: {R} resident weight copies rotated "
+                          f"({R * q.qlin_device_bytes(layer.handle) / 1e6:.0f} MB > 4x {l2 / 1e6:.0f} MB L2)",
+                       issue=f"CUDA graph replays of {R} forwards, programmatic dependent launch between forwards"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("spqr_decode_m1"),
                      "ncu_single_launch_us_cold": _ncu_cold_us("spqr_decode_m1"),
@@ -534,7 +616,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "outlier_frac": FRAC},
+            "config": _config(world),
             "cpu_baseline": r,
             "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -550,7 +632,7 @@ def main():
     ap.add_argument("--no-extra", dest="no_extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
     ap.add_argument("--_oracle_only", dest="oracle_only", action="store_true")
-    ap.add_argument("--prefill-case", dest="prefill_case", choices=["w4g128", "spqr1pct", "w8a8"],
+    ap.add_argument("--prefill-case", dest="prefill_case", choices=["w4g128", "spqr", "w8a8"],
                     help="time only this M=4096 prefill configuration (for profiling) and print its line")
     ap.add_argument("--decode-case", dest="decode_case",
                     help="time only this decode configuration, fmt,K,N,M[,outlier_frac] with fmt in "
