@@ -592,7 +592,7 @@ def run_gpu(args):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("spqr_decode_m1"),
                      "ncu_single_launch_us_cold": _ncu_cold_us("spqr_decode_m1"),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs: torch copy)",
-                     "kernel": "spqr_decode_kernel<1,1,1>", "bytes_per_launch": nbytes},
+                     "kernel": "spqr_gemv1_kernel<3>", "bytes_per_launch": nbytes},
         "e2e": {"value": round(dist_ctx.world * nbytes / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "call": "qlin_forward_host (pinned host X/Y, stream sync per step)"},
         "gpu_launches": steps,
