@@ -19,8 +19,13 @@
 //   accumulators in TMEM) from one elected thread, committing each k-block back to its
 //   shared-memory stage;
 // * converter warps (8 for W4 and W8A8, 16 in two groups for SpQR): turn packed codes into
-//   the bf16 / fp16 K-major 128B-swizzled weight operand; for W4 / SpQR they then run the
-//   epilogue (tcgen05.ld -> bf16 -> Y);
+//   the bf16 / fp16 weight operand; for W4 / SpQR they then run the epilogue
+//   (tcgen05.ld -> bf16 -> Y).  W4 writes the operand straight into TMEM (tcgen05.st, one
+//   32-column stage of 128 lanes x 64 k per k-block, beside the 256-column accumulator) and the
+//   MMA reads A from TMEM: shared memory then carries only the X tiles and the packed units.
+//   Writing the bf16 tile to shared memory and reading it back in the MMA made shared-memory
+//   bandwidth the limit (measured: the same loop without conversion runs at the cuBLAS rate);
+//   SpQR and W8A8 still build a K-major 128B-swizzled tile in shared memory;
 // * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
 //   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds of
 //   sum |qx| that the act-quant kernel gathers), so the fp32 chunk accumulators (TMEM
@@ -54,6 +59,9 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #ifndef QLIN_W8_NPK
 #define QLIN_W8_NPK 4
 #endif
+#ifndef QLIN_W4_ATMEM
+#define QLIN_W4_ATMEM 1
+#endif
 #ifndef QLIN_W4_ST
 #define QLIN_W4_ST 4
 #endif
@@ -69,16 +77,23 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #ifndef QLIN_SP_NPK
 #define QLIN_SP_NPK 2
 #endif
+#ifndef QLIN_W4_CONV
+#define QLIN_W4_CONV 8
+#endif
+#ifndef QLIN_W4_GROUPS
+#define QLIN_W4_GROUPS 1
+#endif
 
 template <int F>
 struct TcCfg;
 template <>
 struct TcCfg<kW4> {
-  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = 8, kStages = QLIN_W4_ST;
-  static constexpr int kConvGroups = 1;
+  static constexpr int kUnitBytes = kW4UnitBytes, kBlocksPerUnit = 2, kMH = 2, kConv = QLIN_W4_CONV, kStages = QLIN_W4_ST;
+  static constexpr int kConvGroups = QLIN_W4_GROUPS;
   static constexpr int kNPK = QLIN_W4_NPK;  // packed-unit stages (each covers kBlocksPerUnit k-blocks)
   static constexpr uint32_t kAType = 1;  // bf16
   static constexpr bool kRowsInLanes = true;  // D = weight rows (TMEM lanes) x tokens (columns)
+  static constexpr bool kATmem = QLIN_W4_ATMEM;  // converted weights go to TMEM, not shared memory
 };
 template <>
 struct TcCfg<kSpqr> {
@@ -87,6 +102,7 @@ struct TcCfg<kSpqr> {
   static constexpr int kNPK = QLIN_SP_NPK;
   static constexpr uint32_t kAType = 1;
   static constexpr bool kRowsInLanes = false;  // D = tokens (lanes) x weight rows (columns)
+  static constexpr bool kATmem = false;
 };
 template <>
 struct TcCfg<kW8> {
@@ -95,13 +111,14 @@ struct TcCfg<kW8> {
   static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
   static constexpr bool kRowsInLanes = true;  // (the drain epilogue assumes this)
+  static constexpr bool kATmem = false;  // TMEM is full: chunk accumulators + int32 partials
 };
 
 template <int F>
 struct TcSmem {
   using C = TcCfg<F>;
   __align__(1024) uint8_t a[C::kStages][C::kMH * kTileBytes];
-  __align__(1024) uint8_t b[C::kStages][kTileBytes];
+  __align__(1024) uint8_t b[C::kStages][C::kATmem ? 16 : kTileBytes];
   __align__(16) uint8_t pk[C::kNPK][2 * C::kUnitBytes];
   __align__(16) uint32_t out[F == kSpqr ? C::kNPK : 1][2][F == kSpqr ? kOutCapTc + 8 : 4];
   __align__(16) uint32_t offs[2][F == kSpqr ? kOffsCapTc : 4];
@@ -148,6 +165,16 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// same, with the A operand (M rows in TMEM lanes, K packed two 16-bit values per column) read
+// from tensor memory instead of shared memory
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
 }
 
@@ -378,6 +405,50 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 lanes x 32 columns from the mma.sync-style fragment: register 2r + h holds lane g + 8h,
+// column 4r + t of the lane quadrant's 16-lane slice at taddr (g = lane / 4, t = lane % 4)
+__device__ __forceinline__ void tmem_st16x128b_x8(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// W4 converter into TMEM: one 16-row tile, k-block kb of the packed stage, as the A operand of
+// the MMA (row = TMEM lane, column c = k pair 2c, 2c + 1).  A lane's word j carries the pairs
+// (row g, k = 16 j + 2 t), (row g + 8, same k), (row g, k + 8), (row g + 8, k + 8): k pair
+// 8 j + t and 8 j + 4 + t, i.e. columns 4 (2 j) + t and 4 (2 j + 1) + t.
+__device__ __forceinline__ void convert_w4_tmem(uint32_t taddr, const uint8_t* unit, int kb, int rt, int lane,
+                                                bool valid) {
+  uint32_t v[16];
+  if (!valid) {  // rows past N: zero operand
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0u;
+  } else {
+    const int g = lane >> 2;
+    const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + kb) * 32 + lane) * 16);
+    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+    const uint32_t* st = reinterpret_cast<const uint32_t*>(unit + kW4CodeBytes);
+    const uint32_t sz0 = st[rt * 16 + g], sz1 = st[rt * 16 + g + 8];
+    const float s0 = h2f_dev((uint16_t)(sz0 & 0xFFFFu)), s1 = h2f_dev((uint16_t)(sz1 & 0xFFFFu));
+    const float z0 = h2f_dev((uint16_t)(sz0 >> 16)), z1 = h2f_dev((uint16_t)(sz1 >> 16));
+    const uint32_t zp0 = pack_bf16x2(128.f + z0, 128.f + z0), zp1 = pack_bf16x2(128.f + z1, 128.f + z1);
+    const uint32_t sp0 = pack_bf16x2(s0, s0), sp1 = pack_bf16x2(s1, s1);
+    const uint32_t zero = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w = words[j];
+      v[4 * j + 0] = bf16x2_fma(bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero);
+      v[4 * j + 1] = bf16x2_fma(bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero);
+      v[4 * j + 2] = bf16x2_fma(bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zp0), sp0, zero);
+      v[4 * j + 3] = bf16x2_fma(bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zp1), sp1, zero);
+    }
+  }
+  tmem_st16x128b_x8(taddr, v);
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 template <int F>
 __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -408,7 +479,12 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   constexpr bool kRowsInLanes = C::kRowsInLanes;
   static_assert(F != kW8 || kRowsInLanes, "the W8A8 drain reads weight rows from TMEM lanes");
   constexpr uint32_t idesc = kRowsInLanes ? idesc_f16(C::kAType, BM, kBN) : idesc_f16(C::kAType, kBN, 128);
-  constexpr uint32_t tmem_cols = F == kW8 ? 512u : 128u * MH;  // W8A8: fp32 chunk sums + int32 partials
+  // W8A8: fp32 chunk sums + int32 partials; W4: the accumulator, then one 32-column A operand
+  // (128 rows x 64 k) per stage
+  constexpr uint32_t tmem_cols = (F == kW8 || C::kATmem) ? 512u : 128u * MH;
+  constexpr uint32_t kACol = 128u * MH;
+  static_assert(!C::kATmem || (kRowsInLanes && kACol + 32u * NST <= 512u && NCONV / NGRP == 8),
+                "TMEM operand stages must fit beside the accumulator; 8 converter warps per k-block");
   // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
   int64_t off_base[2] = {0, 0};
   uint32_t off_len[2] = {0, 0};
@@ -547,7 +623,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         }
         tc_fence_after();
         const uint64_t dw = umma_desc_sw128(sm.b[s]);  // weights, 128 rows
-        if constexpr (kRowsInLanes) {
+        if constexpr (C::kATmem) {
+          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
+          const uint32_t ta = tmem + kACol + 32u * (uint32_t)s;  // weights, 128 lanes x 32 columns
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16_ta(tmem + dcol, ta + 8u * kk, dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        } else if constexpr (kRowsInLanes) {
           const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
@@ -577,7 +659,10 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     const int cw = (warp - 2) % GCONV;
     constexpr int RPW = 128 / GCONV;  // rows per converter warp: 16 or 32
     const LaneSwz swz = lane_swz(lane);
-    const int rg_local = (cw * RPW) / 64;
+    // TMEM operand: a warp may only reach the lane quadrant warp % 4, so converter warp cw
+    // takes rows 32 ((2 + cw) % 4) + 16 (cw / 4) (the group's first warp index is 2 mod 4)
+    const int row_t = C::kATmem ? 32 * ((2 + cw) % 4) + 16 * (cw / 4) : cw * RPW;
+    const int rg_local = row_t / 64;
     const bool rg_valid = rg0 + rg_local < a.RG;
     if constexpr (F == kSpqr) {
       if (!mbar_wait(&sm.offs_bar, 0, a.status)) ok = false;
@@ -598,23 +683,30 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
           ok = false;
           break;
         }
+        if constexpr (C::kATmem) {
+          tc_fence_after();
+          convert_w4_tmem(tmem + ((uint32_t)row_t << 16) + kACol + 32u * (uint32_t)s, unit, b, (row_t % 64) / 16, lane,
+                          rg_valid);
+          tc_fence_before();
+        } else {
 #pragma unroll
-        for (int h = 0; h < RPW / 16; ++h) {
-          const int row0 = cw * RPW + 16 * h;
-          const int rt = (row0 % 64) / 16;
-          convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid, swz);
-          if constexpr (F == kSpqr) {
-            if (rg_valid) {
-              __syncwarp();
-              const int64_t u = (rg0 + rg_local) * a.KU + ui;
-              const uint32_t e0 = soffs(rg_local, 4 * u), e1 = soffs(rg_local, 4 * u + 4);
-              const bool staged = e1 > e0 && e1 - e0 <= (uint32_t)kOutCapTc;
-              spqr_outliers_tile(sm.b[s], staged ? sm.out[p][rg_local] : nullptr, e0 & ~3u, a.ents,
-                                 soffs(rg_local, 4 * u + rt), soffs(rg_local, 4 * u + rt + 1), b, row0, lane);
+          for (int h = 0; h < RPW / 16; ++h) {
+            const int row0 = cw * RPW + 16 * h;
+            const int rt = (row0 % 64) / 16;
+            convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid, swz);
+            if constexpr (F == kSpqr) {
+              if (rg_valid) {
+                __syncwarp();
+                const int64_t u = (rg0 + rg_local) * a.KU + ui;
+                const uint32_t e0 = soffs(rg_local, 4 * u), e1 = soffs(rg_local, 4 * u + 4);
+                const bool staged = e1 > e0 && e1 - e0 <= (uint32_t)kOutCapTc;
+                spqr_outliers_tile(sm.b[s], staged ? sm.out[p][rg_local] : nullptr, e0 & ~3u, a.ents,
+                                   soffs(rg_local, 4 * u + rt), soffs(rg_local, 4 * u + rt + 1), b, row0, lane);
+              }
             }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ab_full[s]);
       }
