@@ -28,10 +28,13 @@
 //   SpQR and W8A8 still build a K-major 128B-swizzled tile in shared memory;
 // * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
 //   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds of
-//   sum |qx| that the act-quant kernel gathers), so the fp32 chunk accumulators (TMEM
-//   columns 0..255) hold exact integers; after each chunk these warps add them into int32
-//   partial sums kept in the other half of TMEM (columns 256..511), release the accumulator
-//   to the next chunk, and after the last one write y = bf16((acc * sx) * sw) (or acc).
+//   sum |qx| that the act-quant kernel gathers), so the fp32 accumulators (TMEM columns
+//   0..255) hold exact integers; after each chunk but the last these warps split every
+//   accumulator v into v = 2^16 hi + lo (0 <= lo < 2^16), add hi into a 16-bit high part kept
+//   in TMEM (columns 256..383, two tokens per column), write lo back as the accumulator the
+//   next chunk continues from, and release it; after the last chunk the int32 result is
+//   2^16 high + accumulator, written as y = bf16((acc * sx) * sw) (or acc).  The 16-bit high
+//   part covers every int32 result; columns 384..511 hold the weight operand stages.
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
 #include "kern_common.cuh"
 
@@ -41,10 +44,11 @@ namespace {
 constexpr int kBN = 128, kBK = 64;
 constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
 // W8A8 exact chunks: a chunk of k-blocks is accumulated in fp32 as long as the sum of its
-// blocks' bounds (max over the tile's tokens of sum |qx| per block) stays <= kExactL1, so every
-// partial sum is an integer of magnitude <= 127 * kExactL1 < 2^24 and fp32 holds it exactly.
-// A block's bound is at most 64 * 127, so a chunk holds at least 16 blocks (1024 K).
-constexpr int kExactL1 = 132104;  // floor(2^24 / 127)
+// blocks' bounds (max over the tile's tokens of sum |qx| per block) stays <= kExactL1.  A
+// chunk starts from a carried low part in [0, 2^16) (see the drain), so every partial sum is
+// an integer of magnitude < 2^16 + 127 * kExactL1 <= 2^24 and fp32 holds it exactly.  A
+// block's bound is at most 64 * 127, so a chunk holds at least 16 blocks (1024 K).
+constexpr int kExactL1 = 131588;  // floor((2^24 - 2^16) / 127)
 constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
 constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
 #ifndef QLIN_TC_RASTER_G
@@ -65,8 +69,11 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #ifndef QLIN_W4_ST
 #define QLIN_W4_ST 4
 #endif
+#ifndef QLIN_W8_ATMEM
+#define QLIN_W8_ATMEM 1
+#endif
 #ifndef QLIN_W8_ST
-#define QLIN_W8_ST 3
+#define QLIN_W8_ST (QLIN_W8_ATMEM ? 4 : 3)
 #endif
 #ifndef QLIN_W8_CONV
 #define QLIN_W8_CONV 8
@@ -111,7 +118,7 @@ struct TcCfg<kW8> {
   static constexpr int kNPK = QLIN_W8_NPK;  // a W8 unit covers one k-block: prefetch deeper
   static constexpr uint32_t kAType = 0;  // fp16
   static constexpr bool kRowsInLanes = true;  // (the drain epilogue assumes this)
-  static constexpr bool kATmem = false;  // TMEM is full: chunk accumulators + int32 partials
+  static constexpr bool kATmem = QLIN_W8_ATMEM;
 };
 
 template <int F>
@@ -415,16 +422,35 @@ __device__ __forceinline__ void tmem_st16x128b_x8(uint32_t taddr, const uint32_t
       : "memory");
 }
 
-// W4 converter into TMEM: one 16-row tile, k-block kb of the packed stage, as the A operand of
-// the MMA (row = TMEM lane, column c = k pair 2c, 2c + 1).  A lane's word j carries the pairs
-// (row g, k = 16 j + 2 t), (row g + 8, same k), (row g, k + 8), (row g + 8, k + 8): k pair
-// 8 j + t and 8 j + 4 + t, i.e. columns 4 (2 j) + t and 4 (2 j + 1) + t.
-__device__ __forceinline__ void convert_w4_tmem(uint32_t taddr, const uint8_t* unit, int kb, int rt, int lane,
-                                                bool valid) {
+// W4 / W8 converter into TMEM: one 16-row tile, k-block kb of the packed stage, as the A
+// operand of the MMA (row = TMEM lane, column c = k pair 2c, 2c + 1).  The packed fragment of
+// lane (g, t) carries, per 16-wide k step j, the pairs (row g, k = 16 j + 2 t), (row g + 8,
+// same k), (row g, k + 8), (row g + 8, k + 8): k pair 8 j + t and 8 j + 4 + t, i.e. columns
+// 4 (2 j) + t and 4 (2 j + 1) + t, registers 4 j .. 4 j + 3 of the 16x128b.x8 store.
+template <int F>
+__device__ __forceinline__ void convert_tmem(uint32_t taddr, const uint8_t* unit, int kb, int rt, int lane,
+                                             bool valid) {
   uint32_t v[16];
   if (!valid) {  // rows past N: zero operand
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0u;
+  } else if constexpr (F == kW8) {  // offset-binary int8 codes -> fp16 (1024 + c) - 1152
+    const uint4 w01 = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + 0) * 32 + lane) * 16);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + 1) * 32 + lane) * 16);
+    const uint32_t words[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+    const uint32_t magic = 0x64646464u, off = 0x64806480u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t d;
+      asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+      v[4 * j + 0] = f16x2_sub(d, off);
+      asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j]), "r"(magic));
+      v[4 * j + 1] = f16x2_sub(d, off);
+      asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+      v[4 * j + 2] = f16x2_sub(d, off);
+      asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(d) : "r"(words[2 * j + 1]), "r"(magic));
+      v[4 * j + 3] = f16x2_sub(d, off);
+    }
   } else {
     const int g = lane >> 2;
     const uint4 wv = *reinterpret_cast<const uint4*>(unit + ((rt * 2 + kb) * 32 + lane) * 16);
@@ -446,6 +472,24 @@ __device__ __forceinline__ void convert_w4_tmem(uint32_t taddr, const uint8_t* u
     }
   }
   tmem_st16x128b_x8(taddr, v);
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -482,7 +526,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   // W8A8: fp32 chunk sums + int32 partials; W4: the accumulator, then one 32-column A operand
   // (128 rows x 64 k) per stage
   constexpr uint32_t tmem_cols = (F == kW8 || C::kATmem) ? 512u : 128u * MH;
-  constexpr uint32_t kACol = 128u * MH;
+  constexpr uint32_t kACol = F == kW8 ? 384u : 128u * MH;
   static_assert(!C::kATmem || (kRowsInLanes && kACol + 32u * NST <= 512u && NCONV / NGRP == 8),
                 "TMEM operand stages must fit beside the accumulator; 8 converter warps per k-block");
   // SpQR: staged bucket offsets of the two row groups, global indices [4 rg S, 4 rg S + 4 S]
@@ -601,10 +645,10 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         bool first = (i == 0);
         bool chunk_end = false;
         if constexpr (F == kW8) {
-          // one fp32 accumulator: chunk c starts once the drain has read chunk c - 1
+          // one fp32 accumulator: chunk c starts once the drain has split chunk c - 1's
+          // accumulators and written back their low parts, and continues from them
           const int bi = kb[i];
           if (i > 0 && bound + bi > kExactL1) {
-            first = true;
             ++chunk;
             if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(chunk - 1) & 1u, a.status)) {
               ok = false;
@@ -685,7 +729,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         }
         if constexpr (C::kATmem) {
           tc_fence_after();
-          convert_w4_tmem(tmem + ((uint32_t)row_t << 16) + kACol + 32u * (uint32_t)s, unit, b, (row_t % 64) / 16, lane,
+          convert_tmem<F>(tmem + ((uint32_t)row_t << 16) + kACol + 32u * (uint32_t)s, unit, b, (row_t % 64) / 16, lane,
                           rg_valid);
           tc_fence_before();
         } else {
@@ -760,13 +804,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     }
   } else if constexpr (F == kW8) {
     // ------------------------------------------------------------------ exact int32 drain + epilogue
-    // warps 6..13: TMEM lane quadrant q = warp % 4 (weight rows 32q..32q+31), token half
-    // mh = (warp - 6) / 4 (accumulator columns 128 mh.., int32 partials 256 + 128 mh..)
+    // warps 10..17: TMEM lane quadrant q = warp % 4 (weight rows 32q..32q+31), token half
+    // mh = (warp - 10) / 4 (accumulator columns 128 mh.., 16-bit high parts 256 + 64 mh..)
     pdl_wait();
     const int q = warp & 3;
     const int mh = (warp - 2 - NCONV) / 4;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const uint32_t fcol = 128u * mh, icol = 256u + 128u * mh;
+    const uint32_t fcol = 128u * mh, hcol = 256u + 64u * mh;
     const int n = n_tile * kBN + 32 * q + lane;  // this lane's weight row
     const float swn = n < a.N ? a.sw[n] : 0.f;
     int nchunks = 1;  // the MMA issuer's chunking, replayed
@@ -788,20 +832,34 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       const bool last = c == nchunks - 1;
 #pragma unroll 1
       for (int cb = 0; cb < kBN / 32; ++cb) {
-        uint32_t r[32];
+        uint32_t r[32], h[16];
         tmem_ld32(tmem + lane_base + fcol + 32u * cb, r);
         if (c > 0) {
-          uint32_t p[32];
-          tmem_ld32(tmem + lane_base + icol + 32u * cb, p);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = (uint32_t)((int32_t)p[i] + __float2int_rn(__uint_as_float(r[i])));
+          tmem_ld16(tmem + lane_base + hcol + 16u * cb, h);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = (uint32_t)__float2int_rn(__uint_as_float(r[i]));
+          for (int i = 0; i < 16; ++i) h[i] = 0u;
         }
-        if (!last) {
-          tmem_st32(tmem + lane_base + icol + 32u * cb, r);
+        if (!last) {  // v = 2^16 hi + lo: hi into the high part, lo back into the accumulator
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int32_t v0 = __float2int_rn(__uint_as_float(r[2 * i]));
+            const int32_t v1 = __float2int_rn(__uint_as_float(r[2 * i + 1]));
+            const int32_t h0 = (int32_t)(int16_t)(h[i] & 0xFFFFu) + (v0 >> 16);
+            const int32_t h1 = (int32_t)(int16_t)(h[i] >> 16) + (v1 >> 16);
+            h[i] = ((uint32_t)h0 & 0xFFFFu) | ((uint32_t)h1 << 16);
+            r[2 * i] = __float_as_uint((float)(v0 & 0xFFFF));
+            r[2 * i + 1] = __float_as_uint((float)(v1 & 0xFFFF));
+          }
+          tmem_st32(tmem + lane_base + fcol + 32u * cb, r);
+          tmem_st16(tmem + lane_base + hcol + 16u * cb, h);
           continue;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int32_t h0 = (int32_t)(int16_t)(h[i] & 0xFFFFu), h1 = (int32_t)(int16_t)(h[i] >> 16);
+          r[2 * i] = (uint32_t)((int32_t)((uint32_t)h0 << 16) + __float2int_rn(__uint_as_float(r[2 * i])));
+          r[2 * i + 1] = (uint32_t)((int32_t)((uint32_t)h1 << 16) + __float2int_rn(__uint_as_float(r[2 * i + 1])));
         }
         // columns are tokens m0 + i; a warp's store of one token writes 32 consecutive outputs
         const int m0 = m_tile * BM + 128 * mh + 32 * cb;
