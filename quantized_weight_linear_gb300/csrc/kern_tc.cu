@@ -12,9 +12,10 @@
 //   tile as B, N = 128), tokens in the lanes (each orientation measured faster for its formats);
 // * grouped raster: consecutive CTAs take 4 token tiles of one weight tile before the next,
 //   so the CTAs of a wave share weight tiles through L2;
-// * warp 0: TMA producer -- X tiles through a 2-D tensor map (128B swizzle) and the packed
-//   weight units of the tile (the device image the decode kernels stream; SpQR: plus the
-//   unit's outlier buckets) through cp.async.bulk into a packed ring;
+// * warp 0: X producer -- X tiles through a 2-D tensor map (128B swizzle) into the operand
+//   ring; the last warp: loader -- the packed weight units of the tile (the device image the
+//   decode kernels stream; SpQR: plus the unit's outlier buckets) through cp.async.bulk into a
+//   packed ring, apart from the X producer so that neither waits on the other's ring;
 // * warp 1: allocates TMEM and issues tcgen05.mma (kind::f16, bf16 or fp16 operands, fp32
 //   accumulators in TMEM) from one elected thread, committing each k-block back to its
 //   shared-memory stage;
@@ -79,7 +80,7 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #define QLIN_W8_CONV 8
 #endif
 #ifndef QLIN_W4_NPK
-#define QLIN_W4_NPK 2
+#define QLIN_W4_NPK 3
 #endif
 #ifndef QLIN_SP_NPK
 #define QLIN_SP_NPK 2
@@ -396,8 +397,13 @@ __device__ __forceinline__ void spqr_outliers_tile(uint8_t* bt, const uint32_t* 
 }
 
 template <int F>
-constexpr int tc_threads() {  // producer + MMA + converters (+ W8A8 drain warps)
-  return 32 * (2 + TcCfg<F>::kConv + (F == kW8 ? 8 : 0));
+constexpr int tc_loader_warp() {  // after the X producer, the MMA issuer, converters (+ W8A8 drains)
+  return 2 + TcCfg<F>::kConv + (F == kW8 ? 8 : 0);
+}
+
+template <int F>
+constexpr int tc_threads() {  // ... and the packed-unit loader
+  return 32 * (tc_loader_warp<F>() + 1);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -502,6 +508,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   constexpr int MH = C::kMH, NCONV = C::kConv, NST = C::kStages;
   constexpr int NGRP = C::kConvGroups, GCONV = NCONV / NGRP;  // converter warps per k-block
   constexpr int BM = 128 * MH;
+  constexpr int kLoaderWarp = tc_loader_warp<F>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // grouped raster: consecutive CTAs walk kRasterG token tiles of one weight tile before the
   // next weight tile, so a wave reads each weight tile from HBM once and shares it through L2
@@ -572,8 +579,12 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   bool ok = true;
   auto soffs = [&](int r, int64_t gi) -> uint32_t { return sm.offs[r][gi - off_base[r]]; };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------------ packed-unit loader
+    // Weights do not depend on the previous kernel, so this warp never waits for it.  It runs
+    // apart from the X producer: the packed ring's slots are released by the converters, and
+    // waiting for them in the thread that issues the X tiles would put the X load latency back
+    // on every k-block.
     if (lane == 0) {
       if constexpr (F == kSpqr) {
         uint32_t bytes = 0;
@@ -583,10 +594,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
           if (off_len[r]) bulk_g2s(sm.offs[r], a.offs + off_base[r], off_len[r] * 4, &sm.offs_bar);
         ok = mbar_wait(&sm.offs_bar, 0, a.status);
       }
-      auto load_units = [&](int ui) -> bool {
+      for (int ui = 0; ui < nunits && ok; ++ui) {
         const int p = ui % C::kNPK;
         const uint32_t ph = (uint32_t)(ui / C::kNPK) & 1u;
-        if (!mbar_wait(&sm.pk_empty[p], ph ^ 1u, a.status)) return false;
+        if (!mbar_wait(&sm.pk_empty[p], ph ^ 1u, a.status)) {
+          ok = false;
+          break;
+        }
         uint32_t bytes = 0;
         uint32_t e_lo[2] = {0, 0}, e_hi[2] = {0, 0};
         for (int r = 0; r < 2; ++r) {
@@ -611,18 +625,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
             if (e_hi[r] > e_lo[r]) bulk_g2s(sm.out[p][r], a.ents + e_lo[r], (e_hi[r] - e_lo[r]) * 4, &sm.pk_full[p]);
           }
         }
-        return true;
-      };
-      // weights do not depend on the previous kernel: prefetch before the dependency wait
-      int next_unit = 0;
-      for (; next_unit < C::kNPK && next_unit < nunits && ok; ++next_unit) ok = load_units(next_unit);
-      pdl_wait();
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ X producer
+    pdl_wait();
+    if (lane == 0) {
       for (int i = 0; i < nkb && ok; ++i) {
-        if (i % bpu == 0 && i / bpu + C::kNPK - 1 >= next_unit && next_unit < nunits) {
-          ok = load_units(next_unit);
-          ++next_unit;
-          if (!ok) break;
-        }
         const int s = i % NST;
         const uint32_t ph = (uint32_t)(i / NST) & 1u;
         if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
