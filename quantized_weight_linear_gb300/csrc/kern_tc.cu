@@ -406,18 +406,6 @@ constexpr int tc_threads() {  // ... and the packed-unit loader
   return 32 * (tc_loader_warp<F>() + 1);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // 16 lanes x 32 columns from the mma.sync-style fragment: register 2r + h holds lane g + 8h,
 // column 4r + t of the lane quadrant's 16-lane slice at taddr (g = lane / 4, t = lane % 4)
 __device__ __forceinline__ void tmem_st16x128b_x8(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -488,6 +476,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -840,18 +842,18 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       tc_fence_after();
       const bool last = c == nchunks - 1;
 #pragma unroll 1
-      for (int cb = 0; cb < kBN / 32; ++cb) {
-        uint32_t r[32], h[16];
-        tmem_ld32(tmem + lane_base + fcol + 32u * cb, r);
+      for (int cb = 0; cb < 8; ++cb) {  // 16 tokens at a time
+        uint32_t r[16], h[8];
+        tmem_ld16(tmem + lane_base + fcol + 16u * cb, r);
         if (c > 0) {
-          tmem_ld16(tmem + lane_base + hcol + 16u * cb, h);
+          tmem_ld8(tmem + lane_base + hcol + 8u * cb, h);
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) h[i] = 0u;
+          for (int i = 0; i < 8; ++i) h[i] = 0u;
         }
         if (!last) {  // v = 2^16 hi + lo: hi into the high part, lo back into the accumulator
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 8; ++i) {
             const int32_t v0 = __float2int_rn(__uint_as_float(r[2 * i]));
             const int32_t v1 = __float2int_rn(__uint_as_float(r[2 * i + 1]));
             const int32_t h0 = (int32_t)(int16_t)(h[i] & 0xFFFFu) + (v0 >> 16);
@@ -860,28 +862,40 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
             r[2 * i] = __float_as_uint((float)(v0 & 0xFFFF));
             r[2 * i + 1] = __float_as_uint((float)(v1 & 0xFFFF));
           }
-          tmem_st32(tmem + lane_base + fcol + 32u * cb, r);
-          tmem_st16(tmem + lane_base + hcol + 16u * cb, h);
+          tmem_st16(tmem + lane_base + fcol + 16u * cb, r);
+          tmem_st8(tmem + lane_base + hcol + 8u * cb, h);
           continue;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const int32_t h0 = (int32_t)(int16_t)(h[i] & 0xFFFFu), h1 = (int32_t)(int16_t)(h[i] >> 16);
           r[2 * i] = (uint32_t)((int32_t)((uint32_t)h0 << 16) + __float2int_rn(__uint_as_float(r[2 * i])));
           r[2 * i + 1] = (uint32_t)((int32_t)((uint32_t)h1 << 16) + __float2int_rn(__uint_as_float(r[2 * i + 1])));
         }
         // columns are tokens m0 + i; a warp's store of one token writes 32 consecutive outputs
-        const int m0 = m_tile * BM + 128 * mh + 32 * cb;
+        const int m0 = m_tile * BM + 128 * mh + 16 * cb;
         if (n >= a.N) continue;
         if (a.acc_out) {
           int32_t* dst = a.acc_out + (int64_t)m0 * a.N + n;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 16; ++i)
             if (m0 + i < a.M) dst[(int64_t)i * a.N] = (int32_t)r[i];
+        } else if (m0 + 16 <= a.M) {  // whole 16-token slice: token scales as 16-byte loads
+          uint16_t* dst = a.Y + (int64_t)m0 * a.N + n;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(a.sx + m0) + v);
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 4 * v + e;
+              dst[(int64_t)i * a.N] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[i]), sv[e]), swn));
+            }
+          }
         } else {
           uint16_t* dst = a.Y + (int64_t)m0 * a.N + n;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 16; ++i)
             if (m0 + i < a.M)
               dst[(int64_t)i * a.N] = f2bf(__fmul_rn(__fmul_rn(__int2float_rn((int32_t)r[i]), a.sx[m0 + i]), swn));
         }
