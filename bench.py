@@ -370,6 +370,11 @@ def _decode_layer(q, fmt, K, N, M, frac=0.01, seed=0):
     if fmt == "w4g128":
         W, X = synth.gptq_layer(N, K, M, seed=seed)
         layer = q.QLinear.from_w4g128(W)
+    elif fmt == "w4act":  # the same W4 g128 codes read in an act-order column permutation
+        W, X = synth.gptq_layer(N, K, M, seed=seed)
+        c = q.QLinear.from_w4g128(W).export()
+        c["perm"] = np.random.default_rng(seed).permutation(K).astype(np.int32)
+        layer = q.QLinear(q.qlin_import(q.FMT_W4G128, N, K, c))
     elif fmt == "spqr":
         W, X = synth.spqr_layer(N, K, M, seed=seed)
         layer = q.QLinear.from_spqr(W, frac)

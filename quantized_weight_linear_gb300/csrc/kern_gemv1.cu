@@ -102,13 +102,14 @@ struct G1Layout {
   uint32_t xs;           // staged x, plain order
   uint32_t xf;           // W4: staged x in B-fragment order
   uint32_t bytes;        // total
+  uint32_t xfull;        // W4 act-order: the whole x row (input channel order)
 };
 
 namespace {
 
 inline uint32_t al128(uint32_t x) { return (x + 127u) & ~127u; }
 
-G1Layout g1_layout(bool spqr, int xn, int stages) {
+G1Layout g1_layout(bool spqr, int xn, int stages, int xfull_k = 0) {
   G1Layout L{};
   uint32_t o = al128((uint32_t)sizeof(G1Hdr));
   L.stage_bytes = spqr ? al128(kSpqrUnitBytes + kG1OutWords * 4) : al128(kW4UnitBytes);
@@ -130,6 +131,8 @@ G1Layout g1_layout(bool spqr, int xn, int stages) {
     o = al128(o + (uint32_t)xn * kW4Group * 2);
     L.xf = o;
     o = al128(o + (uint32_t)xn * kW4Group * 2);
+    L.xfull = o;  // act-order: the whole token, in input channel order
+    o = al128(o + (uint32_t)xfull_k * 2);
   }
   L.bytes = o;
   return L;
@@ -790,7 +793,9 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
 
 // ---------------------------------------------------------------------------------- W4
 
-template <int STAGES>
+// ACT: act-order (v.perm set): the consumers gather x[perm] from the staged row; a separate
+// instance, so that the static-group kernel carries none of that code
+template <int STAGES, bool ACT>
 __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     w4_gemv1_kernel(W4View v, const uint16_t* __restrict__ X, uint16_t* __restrict__ Y, Workspace ws, G1Layout L) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -839,7 +844,10 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     int pf = pro + kG1W4Prefetch < n ? pro + kG1W4Prefetch : n;  // end of the prefetched window
     if (pf > pro) prefetch_l2(unit_src(pro), (uint64_t)(pf - pro) * kW4UnitBytes);
     pdl_wait();  // x is written by the previous kernel on the stream
-    if (q == 0) {
+    if (ACT && q == 0) {  // act-order: the whole row; the consumers gather from it
+      mbar_arrive_expect_tx(&h.x_bar, (uint32_t)G * (kW4Group * 2));
+      bulk_g2s(sb + L.xfull, X, (uint32_t)G * (kW4Group * 2), &h.x_bar);
+    } else if (q == 0) {
       const int xn = h.xn;
       const int64_t ks = u0c % G;
       const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
@@ -867,8 +875,35 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
 
   // -------------------------------------------------------------------- consumers
   const int grp = warp >> 2, rt = warp & 3;
-  pdl_wait();
-  if (!g1_wait(&h.x_bar, 0, ws.status)) return;
+  if constexpr (ACT) {
+    // act-order: staged element j (K group (ks + j / 128) mod G, column j mod 128) is
+    // x[perm[k]], gathered in shared memory from the whole row.  The permutation is part of
+    // the weights, so this thread's entries are read (coalesced) before the wait for the
+    // previous kernel.
+    static_assert(kG1GatherMaxK <= 8192, "a consumer thread gathers at most 32 elements");
+    constexpr int kPer = 8192 / (32 * kG1Consumers);
+    const int nj = h.xn * kW4Group;
+    const int64_t ks = u0c % G;
+    int32_t pk[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = threadIdx.x + e * 32 * kG1Consumers;
+      pk[e] = j < nj ? __ldg(v.perm + ((ks + j / kW4Group) % G) * kW4Group + j % kW4Group) : 0;
+    }
+    pdl_wait();
+    const bool got = g1_wait(&h.x_bar, 0, ws.status);
+    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(sb + L.xfull);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = threadIdx.x + e * 32 * kG1Consumers;
+      if (j < nj) xs[j] = xrow[pk[e]];
+    }
+    named_bar_sync(1, 32 * kG1Consumers);  // every consumer thread, no early exit before it
+    if (!got) return;
+  } else {
+    pdl_wait();
+    if (!g1_wait(&h.x_bar, 0, ws.status)) return;
+  }
   {
     // x in B-fragment order: per 128-group, lane column t, MMA j: the pairs (16j + 2t, +1)
     // and (16j + 2t + 8, +9), so that a lane reads its sixteen B registers of a group with
@@ -983,15 +1018,17 @@ int g1_grid(int64_t U, int sms, bool spqr) {
 // Launches with the deepest ring (of `deep` stages, or one less) whose shared memory fits.
 template <typename KDeep, typename KShallow, typename View>
 int g1_launch(KDeep* kdeep, KShallow* kshallow, int deep, std::atomic<uint64_t>* attr_done, const View& v, int64_t U,
-              int64_t per_rg, bool spqr, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
+              int64_t per_rg, bool spqr, bool xfull, const uint16_t* X, uint16_t* Y, const Workspace& ws,
+              void* stream) {
   const int grid = g1_grid(U, ws.sms, spqr);
   if ((int64_t)grid * kG1Groups > ws.grid) return (int)cudaErrorInvalidValue;  // workspace slots
   const int xn = (int)std::min<int64_t>(per_rg, (U + grid - 1) / grid);
+  const int xfull_k = xfull ? (int)(per_rg * kW4Group) : 0;
   int stages = deep;
-  G1Layout L = g1_layout(spqr, xn, stages);
+  G1Layout L = g1_layout(spqr, xn, stages, xfull_k);
   if ((size_t)L.bytes + 128 > kG1MaxSmem) {
     stages = deep - 1;
-    L = g1_layout(spqr, xn, stages);
+    L = g1_layout(spqr, xn, stages, xfull_k);
   }
   const size_t smem = (size_t)L.bytes + 128;
   if (smem > kG1MaxSmem) return (int)cudaErrorInvalidValue;
@@ -1021,13 +1058,16 @@ int gemv1_slots(int64_t units, int sms, bool spqr) { return g1_grid(units, sms, 
 int launch_spqr_gemv1(const SpqrView& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
   static std::atomic<uint64_t> attr_done[2];
   return g1_launch(spqr_gemv1_kernel<kG1SpStages>, spqr_gemv1_kernel<kG1SpStages - 1>, kG1SpStages, attr_done, v,
-                   (int64_t)v.RG * v.S, v.S, true, X, Y, ws, stream);
+                   (int64_t)v.RG * v.S, v.S, true, false, X, Y, ws, stream);
 }
 
 int launch_w4_gemv1(const W4View& v, const uint16_t* X, uint16_t* Y, const Workspace& ws, void* stream) {
-  static std::atomic<uint64_t> attr_done[2];
-  return g1_launch(w4_gemv1_kernel<kG1W4Stages>, w4_gemv1_kernel<kG1W4Stages - 1>, kG1W4Stages, attr_done, v,
-                   (int64_t)v.RG * v.G, v.G, false, X, Y, ws, stream);
+  static std::atomic<uint64_t> attr_done[4];
+  if (v.perm)
+    return g1_launch(w4_gemv1_kernel<kG1W4Stages, true>, w4_gemv1_kernel<kG1W4Stages - 1, true>, kG1W4Stages,
+                     attr_done + 2, v, (int64_t)v.RG * v.G, v.G, false, true, X, Y, ws, stream);
+  return g1_launch(w4_gemv1_kernel<kG1W4Stages, false>, w4_gemv1_kernel<kG1W4Stages - 1, false>, kG1W4Stages,
+                   attr_done, v, (int64_t)v.RG * v.G, v.G, false, false, X, Y, ws, stream);
 }
 
 }  // namespace qlin

@@ -1409,14 +1409,21 @@ static qlin_status run_decode(qlin_handle h, const uint16_t* X, uint16_t* Y, int
                               cudaStream_t s) {
   int e = 0;
   switch (h->format) {
-    case QLIN_FMT_W4G128:
-      if (!h->perm.empty()) {  // act-order: gather X's channels into the permuted order first
-        uint16_t* xp = reinterpret_cast<uint16_t*>(h->wsv.qx);
-        e = launch_w4_gather(X, reinterpret_cast<const int32_t*>(h->dev + h->sec_perm), xp, M, h->K, s);
-        X = xp;
+    case QLIN_FMT_W4G128: {
+      W4View v = w4view(h);
+      if (!h->perm.empty()) {  // act-order: x's channels are read in the permuted order
+        const int32_t* perm = reinterpret_cast<const int32_t*>(h->dev + h->sec_perm);
+        if (M == 1 && h->K <= kG1GatherMaxK) {
+          v.perm = perm;  // the single-token kernel gathers x while staging it
+        } else {          // a gather launch first
+          uint16_t* xp = reinterpret_cast<uint16_t*>(h->wsv.qx);
+          e = launch_w4_gather(X, perm, xp, M, h->K, s);
+          X = xp;
+        }
       }
-      if (!e) e = launch_w4_decode(w4view(h), X, Y, M, h->wsv, h->grid, s);
+      if (!e) e = launch_w4_decode(v, X, Y, M, h->wsv, h->grid, s);
       break;
+    }
     case QLIN_FMT_SPQR:
       e = launch_spqr_decode(spqrview(h), X, Y, M, h->wsv, h->grid, s);
       break;

@@ -72,7 +72,14 @@ constexpr int kStatusTimeout = 5;
 struct W4View {
   const uint8_t* units;  // [RG][G] units
   int N, K, RG, G;
+  // act-order column permutation, when the single-token kernel gathers x itself (M == 1,
+  // K <= kG1GatherMaxK); otherwise null and x arrives already permuted
+  const int32_t* perm = nullptr;
 };
+#ifndef QLIN_G1_GATHER_MAX_K
+#define QLIN_G1_GATHER_MAX_K 8192
+#endif
+constexpr int kG1GatherMaxK = QLIN_G1_GATHER_MAX_K;
 
 struct SpqrView {
   const uint8_t* units;      // [RG][S] units

@@ -89,6 +89,27 @@ def test_w4_gptq_layer(qlin, M, act):
     _check(_y(layer, X, M), X, ref["w_hat"])
 
 
+# K = 8192: the largest K whose single-token forward gathers x inside the kernel; 8320: past
+# it (a gather launch first); 1152: nine K groups, so the CTAs' staged ranges wrap around K
+@pytest.mark.parametrize("N,K", [(2048, 8192), (1000, 8320), (4096, 1152)])
+def test_w4_act_order_single_token(qlin, N, K):
+    """One token through an act-order layer (codes in permuted column order, imported with a
+    permutation) equals, bit for bit, the same codes without the permutation fed x[perm] (the
+    staged activations are the same values), and the oracle within the tolerance."""
+    W = synth.normal(23, synth.KEY_W, 0.02, (N, K))
+    c = qlin.QLinear.from_w4g128(W).export()
+    perm = np.random.default_rng(23).permutation(K).astype(np.int32)
+    plain = qlin.QLinear(qlin.qlin_import(qlin.FMT_W4G128, N, K, c)).to("cuda")
+    act = qlin.QLinear(qlin.qlin_import(qlin.FMT_W4G128, N, K, dict(c, perm=perm))).to("cuda")
+    X = synth.activations_bf16(23, 1, K)
+    y_act = _y(act, X, 1)
+    assert np.array_equal(y_act.view(np.uint32), _y(plain, np.ascontiguousarray(X[:, perm]), 1).view(np.uint32))
+    w_hat = gptq_w4.dequantize(gptq_w4.unpack_codes(c["codes"]), c["scale"], c["zero"])
+    y_ref, bound = forward.reference(bits_to_f32(X)[:, perm], w_hat)
+    ok, worst = forward.within_tolerance(y_act, y_ref, bound)
+    assert ok, worst
+
+
 @pytest.mark.parametrize("kind", ["w4", "w4_act", "spqr", "w8a8"])
 def test_checkpoint_reload_computes_the_same(qlin, kind, tmp_path):
     """A layer saved and loaded back (qlin_import, no requantization) gives the same outputs
