@@ -24,7 +24,10 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesSp = 3;
+#ifndef QLIN_SP_DEC_STAGES
+#define QLIN_SP_DEC_STAGES 3
+#endif
+constexpr int kStagesSp = QLIN_SP_DEC_STAGES;
 constexpr int kXHalfSp = 136;      // each 128-wide half of the X slice as [XR][128 + 8 pad]
 constexpr int kOutCap = 640;       // outlier entries staged per unit (more -> read from global)
 constexpr int kOffsCap = 1024 + 16;  // offsets staged per CTA
@@ -90,8 +93,11 @@ __device__ __forceinline__ uint32_t qsqz_entry(const uint8_t* area, int r, int g
   return __funnelshift_r(lo, hi, bit & 31) & 63u;
 }
 
+#ifndef QLIN_SP_CPS16
+#define QLIN_SP_CPS16 3
+#endif
 template <int MT, int OWN>  // MT: 8-token column tiles (M <= 8 MT); OWN: see below
-__global__ void __launch_bounds__(160, MT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     spqr_decode_kernel(const __grid_constant__ CUtensorMap xmap, SpqrView v, const uint16_t* __restrict__ X,
                        uint16_t* __restrict__ Y, int M, Workspace ws) {
   constexpr int XR = 8 * MT;
@@ -412,7 +418,7 @@ int spqr_decode_grid(const SpqrView& v, int M, int sms) {
   // several CTAs per SM hide the unpack latency; every CTA stages its slice of the bucket
   // offsets, so ranges stay below kOffsCap entries
   const int64_t U = (int64_t)v.RG * v.S;
-  const int cps = std::min(M <= 8 ? 3 : 2, QLIN_DECODE_CPS_MAX);
+  const int cps = std::min(M <= 8 ? 3 : QLIN_SP_CPS16, QLIN_DECODE_CPS_MAX);
   int64_t grid = std::min<int64_t>(U, (int64_t)cps * sms);
   const int64_t need = (U * 4 + (kOffsCap - 24) - 1) / (kOffsCap - 24);
   if (grid < need) grid = std::min<int64_t>(U, need);

@@ -36,8 +36,11 @@ struct W4Smem {
   float own[kRowGroup * 4];  // up to 4 tokens: this CTA's partial sums of the row group it owns
 };
 
+#ifndef QLIN_W4_CPS16
+#define QLIN_W4_CPS16 3
+#endif
 template <int MT, int OWN>  // OWN: 4 (M <= 4, owner-reduces split completion), 0 counted
-__global__ void __launch_bounds__(160, 4)
+__global__ void __launch_bounds__(160, MT == 1 ? 4 : QLIN_W4_CPS16)
     w4_decode_kernel(const __grid_constant__ CUtensorMap xmap, W4View v, const uint16_t* __restrict__ X,
                      uint16_t* __restrict__ Y, int M, Workspace ws) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -317,7 +320,8 @@ int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
   if (M == 1) return launch_w4_gemv1(v, X, Y, ws, stream);
-  grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms);
+  const int cps = M <= 8 ? 4 : QLIN_W4_CPS16;  // CTAs per SM the launch bounds allow
+  grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(cps, QLIN_DECODE_CPS_MAX) * ws.sms);
   if (M <= 4) return launch_w4_mt<1, 4>(v, X, Y, M, ws, grid, stream);
   if (M <= 8) return launch_w4_mt<1, 0>(v, X, Y, M, ws, grid, stream);
   return launch_w4_mt<2, 0>(v, X, Y, M, ws, grid, stream);

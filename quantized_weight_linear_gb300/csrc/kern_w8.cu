@@ -24,7 +24,10 @@
 namespace qlin {
 namespace {
 
-constexpr int kStagesW8 = 4;
+#ifndef QLIN_W8_DEC_STAGES
+#define QLIN_W8_DEC_STAGES 4
+#endif
+constexpr int kStagesW8 = QLIN_W8_DEC_STAGES;
 constexpr int kXStrideW8 = 72;  // staged qx row: 64 fp16 + 8 pad
 
 // Where the fp16 code of (token m, channel k) goes.  blk == 0: row-major [M][K] (the prefill
