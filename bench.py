@@ -487,7 +487,8 @@ def _all_configs(q, torch, stream, l2, peaks):
     """Every configuration of the workload list other than the headline (SpQR 11008 x 4096,
     M = 1): W4 g128 4096^2 M = 1; W8A8 4096^2 at M = 16 and 2048; the 70B-class decode sweep
     (M = 1, 4, 16; W4 g128 and SpQR at 0.5 / 1 / 2 % outliers); prefill M = 4096 on both
-    shapes for the three formats.  Each entry carries its roofline fraction and its clocks."""
+    shapes for the three formats; W8A8 at M = 16 on 8192 x 28672.  Each entry carries its
+    roofline fraction and its clocks."""
     out = {}
 
     def guard(name, fn):
@@ -504,6 +505,8 @@ def _all_configs(q, torch, stream, l2, peaks):
         for frac in (0.005, 0.01, 0.02):
             guard(f"cfg3_spqr_{frac}_{K}_{N}",
                   lambda: _decode_entries(q, torch, stream, l2, peaks, "spqr", K, N, (1, 4, 16), frac))
+    # W8A8 multi-token decode on a 70B-class shape as well (same generator as the 4096^2 layer)
+    guard("w8a8_decode_8192_28672", lambda: _decode_entries(q, torch, stream, l2, peaks, "w8a8", 8192, 28672, (16,)))
     for K, N in PREFILL_SHAPES:
         for fmt in ("w4g128", "spqr", "w8a8"):
             guard(f"cfg4_{fmt}_{K}_{N}", lambda: _prefill_entry(q, torch, stream, peaks, fmt, K, N))
