@@ -1024,9 +1024,22 @@ int g1_launch(KDeep* kdeep, KShallow* kshallow, int deep, std::atomic<uint64_t>*
   if ((int64_t)grid * kG1Groups > ws.grid) return (int)cudaErrorInvalidValue;  // workspace slots
   const int xn = (int)std::min<int64_t>(per_rg, (U + grid - 1) / grid);
   const int xfull_k = xfull ? (int)(per_rg * kW4Group) : 0;
+  // the deeper ring only if kG1CtasPerSm CTAs still share an SM: the grid assumes that many,
+  // and one CTA fewer per SM runs the launch in two waves
+  static std::atomic<int> sm_smem{0};
+  if (sm_smem.load() == 0) {
+    int dev = 0, per_sm = 0, reserved = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess)
+      sm_smem.store(per_sm / kG1CtasPerSm - reserved);
+    else
+      cudaGetLastError();
+  }
+  const size_t share = sm_smem.load() > 0 ? (size_t)sm_smem.load() : kG1MaxSmem;
   int stages = deep;
   G1Layout L = g1_layout(spqr, xn, stages, xfull_k);
-  if ((size_t)L.bytes + 128 > kG1MaxSmem) {
+  if ((size_t)L.bytes + 128 > std::min(share, kG1MaxSmem)) {
     stages = deep - 1;
     L = g1_layout(spqr, xn, stages, xfull_k);
   }
