@@ -282,6 +282,10 @@ def _time_steps(rot, steps, warmup, dist_ctx):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()
     torch.cuda.synchronize()
+    # a ~50 us device spin ahead of the start event keeps the GPU busy while the host submits
+    # the graph, so the timed region holds the forwards and not the host's submission latency
+    with torch.cuda.stream(rot.stream):
+        torch.cuda._sleep(100_000)
     ev0.record(rot.stream)
     for _ in range(reps):
         rot.graph.replay()
