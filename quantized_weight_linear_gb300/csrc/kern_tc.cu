@@ -21,21 +21,22 @@
 //   shared-memory stage;
 // * converter warps (8 for W4 and W8A8, 16 in two groups for SpQR): turn packed codes into
 //   the bf16 / fp16 weight operand; for W4 / SpQR they then run the epilogue
-//   (tcgen05.ld -> bf16 -> Y).  W4 writes the operand straight into TMEM (tcgen05.st, one
-//   32-column stage of 128 lanes x 64 k per k-block, beside the 256-column accumulator) and the
-//   MMA reads A from TMEM: shared memory then carries only the X tiles and the packed units.
-//   Writing the bf16 tile to shared memory and reading it back in the MMA made shared-memory
-//   bandwidth the limit (measured: the same loop without conversion runs at the cuBLAS rate);
-//   SpQR and W8A8 still build a K-major 128B-swizzled tile in shared memory;
+//   (tcgen05.ld -> bf16 -> Y).  W4 and W8A8 write the operand straight into TMEM
+//   (tcgen05.st, one 32-column stage of 128 lanes x 64 k per k-block, beside the accumulator)
+//   and the MMA reads A from TMEM: shared memory then carries only the X tiles and the packed
+//   units.  Writing the tile to shared memory and reading it back in the MMA made
+//   shared-memory bandwidth the limit (measured: the same loop without conversion runs at the
+//   cuBLAS rate).  SpQR builds a K-major 128B-swizzled tile in shared memory;
 // * W8A8 only, 8 more warps: exactness drain -- int8 x int8 products are exact in the fp16
-//   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds of
-//   sum |qx| that the act-quant kernel gathers), so the fp32 accumulators (TMEM columns
-//   0..255) hold exact integers; after each chunk but the last these warps split every
-//   accumulator v into v = 2^16 hi + lo (0 <= lo < 2^16), add hi into a 16-bit high part kept
-//   in TMEM (columns 256..383, two tokens per column), write lo back as the accumulator the
-//   next chunk continues from, and release it; after the last chunk the int32 result is
-//   2^16 high + accumulator, written as y = bf16((acc * sx) * sw) (or acc).  The 16-bit high
-//   part covers every int32 result; columns 384..511 hold the weight operand stages.
+//   MMA, and a K chunk is cut wherever its sum could reach 2^24 (from per-block bounds: the
+//   act-quant kernel's maxima of sum qx^2 and the weight tile's of sum qw^2), so the fp32
+//   accumulators (TMEM columns 0..255) hold exact integers; after each chunk but the last
+//   these warps split every accumulator v into v = 2^16 hi + lo (0 <= lo < 2^16), add hi into
+//   a 16-bit high part kept in TMEM (columns 256..383, two tokens per column), write lo back
+//   as the accumulator the next chunk continues from, and release it; after the last chunk
+//   the int32 result is 2^16 high + accumulator, written as y = bf16((acc * sx) * sw) (or
+//   acc).  The 16-bit high part covers every int32 result; columns 384..511 hold the weight
+//   operand stages.
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace status word.
 #include "kern_common.cuh"
 
@@ -45,11 +46,29 @@ namespace {
 constexpr int kBN = 128, kBK = 64;
 constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
 // W8A8 exact chunks: a chunk of k-blocks is accumulated in fp32 as long as the sum of its
-// blocks' bounds (max over the tile's tokens of sum |qx| per block) stays <= kExactL1.  A
-// chunk starts from a carried low part in [0, 2^16) (see the drain), so every partial sum is
-// an integer of magnitude < 2^16 + 127 * kExactL1 <= 2^24 and fp32 holds it exactly.  A
-// block's bound is at most 64 * 127, so a chunk holds at least 16 blocks (1024 K).
-constexpr int kExactL1 = 131588;  // floor((2^24 - 2^16) / 127)
+// blocks' bounds stays <= kExactSum.  A block's bound is ceil(sqrt(X2 W2)), X2 the largest sum
+// of squared activation codes over the block among the tile's tokens and W2 the same over its
+// weight rows: by Cauchy-Schwarz no token-row product sum of the block exceeds it.  A chunk
+// starts from a carried low part in [0, 2^16) (see the drain), so every partial sum is an
+// integer of magnitude < 2^16 + kExactSum <= 2^24 and fp32 holds it exactly.  A block's bound
+// is at most 64 * 127^2, so a chunk holds at least 16 blocks (1024 K).
+constexpr int kExactSum = (1 << 24) - (1 << 16);
+
+// an upper bound of ceil(sqrt(x2 w2)): both < 2^24 are exact in fp32, the product and the
+// square root each round by at most 2^-24 relative, the 2^-20 margin covers both
+__device__ __forceinline__ int block_bound(int32_t x2, uint32_t w2) {
+  return (int)(sqrtf((float)x2 * (float)w2) * 1.00000095f) + 1;
+}
+
+// Whether a whole tile's blocks fit one exact chunk: the sum of all block bounds, the lanes of
+// a warp taking every 32nd block (every lane of the warp calls this)
+__device__ __forceinline__ bool one_exact_chunk(const int32_t* kb, const uint32_t* kw, int nkb, int lane) {
+  long long tot = 0;
+  for (int j = lane; j < nkb; j += 32) tot += block_bound(kb[j], kw[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  return tot <= kExactSum;
+}
 constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
 constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
 #ifndef QLIN_TC_RASTER_G
@@ -144,7 +163,8 @@ struct TcArgs {
   const uint32_t* ents;   // SpQR outlier entries
   const float* sw;        // W8: per-row scales
   const float* sx;        // W8: per-token scales
-  const int32_t* kbound;  // W8: [M tiles of 256][K / 64] per-block bounds of sum |qx|
+  const int32_t* kbound;  // W8: [M tiles of 256][K / 64] per-block max of sum qx^2
+  const uint32_t* w2;     // W8: [N tiles of 128][K / 64] per-block max of sum qw^2
   uint16_t* Y;
   int32_t* acc_out;
   int32_t* status;
@@ -524,7 +544,9 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   const int nkb = a.K / kBK;
   const int bpu = C::kBlocksPerUnit;
   const int nunits = nkb / bpu;
-  const int32_t* kb = F == kW8 ? a.kbound + (int64_t)m_tile * nkb : nullptr;  // this tile's block bounds
+  // W8A8: this tile's per-block maxima of sum qx^2 (token tile) and sum qw^2 (weight tile)
+  const int32_t* kb = F == kW8 ? a.kbound + (int64_t)m_tile * nkb : nullptr;
+  const uint32_t* kw = F == kW8 ? a.w2 + (int64_t)n_tile * nkb : nullptr;
   // W4, W8A8: one MMA per k-step, A = the converted weight tile (M = 128 rows), B = the X tile
   // (N = 256 tokens); D in TMEM has the weight rows in its lanes and the tokens in its columns.
   // SpQR: two MMAs per k-step, A = one 128-token half of X, B = the weight tile (N = 128); D
@@ -647,8 +669,14 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     pdl_wait();
+    // W8A8: a tile whose bounds fit one exact chunk issues its k-blocks without any bound
+    // arithmetic (the common case: chunk sizes are computed per block only otherwise)
+    bool one_chunk = true;
+    if constexpr (F == kW8) one_chunk = one_exact_chunk(kb, kw, nkb, lane);
     if (lane == 0) {
       int bound = 0, chunk = 0;  // W8A8: running bound of the current exact chunk, its index
+      int bnext = 0;             // W8A8: the next block's bound, read one k-block ahead
+      if constexpr (F == kW8) bnext = one_chunk ? 0 : block_bound(kb[0], kw[0]);
       for (int i = 0; i < nkb && ok; ++i) {
         const int s = i % NST;
         const uint32_t ph = (uint32_t)(i / NST) & 1u;
@@ -656,21 +684,25 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         bool first = (i == 0);
         bool chunk_end = false;
         if constexpr (F == kW8) {
-          // one fp32 accumulator: chunk c starts once the drain has split chunk c - 1's
-          // accumulators and written back their low parts, and continues from them
-          const int bi = kb[i];
-          if (i > 0 && bound + bi > kExactL1) {
-            ++chunk;
-            if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(chunk - 1) & 1u, a.status)) {
-              ok = false;
-              break;
+          chunk_end = i == nkb - 1;
+          if (!one_chunk) {
+            // one fp32 accumulator: chunk c starts once the drain has split chunk c - 1's
+            // accumulators and written back their low parts, and continues from them
+            const int bi = bnext;
+            bnext = i + 1 < nkb ? block_bound(kb[i + 1], kw[i + 1]) : 0;
+            if (i > 0 && bound + bi > kExactSum) {
+              ++chunk;
+              if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(chunk - 1) & 1u, a.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              bound = bi;
+            } else {
+              bound += bi;
             }
-            tc_fence_after();
-            bound = bi;
-          } else {
-            bound += bi;
+            chunk_end = i == nkb - 1 || bound + bnext > kExactSum;
           }
-          chunk_end = i == nkb - 1 || bound + kb[i + 1] > kExactL1;
         }
         if (!mbar_wait(&sm.ab_full[s], ph, a.status)) {
           ok = false;
@@ -825,9 +857,10 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     const int n = n_tile * kBN + 32 * q + lane;  // this lane's weight row
     const float swn = n < a.N ? a.sw[n] : 0.f;
     int nchunks = 1;  // the MMA issuer's chunking, replayed
-    for (int i = 0, bound = 0; i < nkb; ++i) {
-      const int bi = kb[i];
-      if (i > 0 && bound + bi > kExactL1) {
+    const bool one_chunk = one_exact_chunk(kb, kw, nkb, lane);
+    for (int i = 0, bound = 0; i < nkb && !one_chunk; ++i) {
+      const int bi = block_bound(kb[i], kw[i]);
+      if (i > 0 && bound + bi > kExactSum) {
         ++nchunks;
         bound = bi;
       } else {
@@ -953,19 +986,19 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
 }  // namespace
 
 int launch_w4_prefill(const W4View& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
-  TcArgs a{v.units, nullptr, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.G};
+  TcArgs a{v.units, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.G};
   return launch_tc<kW4>(X, a, stream);
 }
 
 int launch_spqr_prefill(const SpqrView& v, const uint16_t* X, uint16_t* Y, int M, int32_t* status, void* stream) {
-  TcArgs a{v.units, v.offs, v.ents, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.S};
+  TcArgs a{v.units, v.offs, v.ents, nullptr, nullptr, nullptr, nullptr, Y, nullptr, status, M, v.N, v.K, v.RG, v.S};
   return launch_tc<kSpqr>(X, a, stream);
 }
 
 int launch_w8_prefill(const W8View& v, const uint16_t* q16, const float* sx, const int32_t* kbound, uint16_t* Y,
                       int32_t* acc, int M,
                       int32_t* status, void* stream) {
-  TcArgs a{v.units, nullptr, nullptr, v.sw, sx, kbound, Y, acc, status, M, v.N, v.K, v.RG, v.KB};
+  TcArgs a{v.units, nullptr, nullptr, v.sw, sx, kbound, v.w2, Y, acc, status, M, v.N, v.K, v.RG, v.KB};
   return launch_tc<kW8>(q16, a, stream);
 }
 

@@ -83,17 +83,17 @@ __global__ void __launch_bounds__(256)
       qv[e] = q < -127 ? -127 : (q > 127 ? 127 : q);
     }
     if (kbound) {
-      // sum |q| of this token's 64-wide k-block (8 threads of 8 codes), max into its tile's bound
-      int l1 = 0;
+      // sum q^2 of this token's 64-wide k-block (8 threads of 8 codes), max into its tile's bound
+      int l2 = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) l1 += qv[e] < 0 ? -qv[e] : qv[e];
+      for (int e = 0; e < 8; ++e) l2 += qv[e] * qv[e];
       // K is a multiple of 64, so the 8 lanes of a k-block are in the loop together (a warp's
       // tail may not be)
       const unsigned am = __activemask();
-      l1 += __shfl_xor_sync(am, l1, 1);
-      l1 += __shfl_xor_sync(am, l1, 2);
-      l1 += __shfl_xor_sync(am, l1, 4);
-      if ((threadIdx.x & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + k / 64, l1);
+      l2 += __shfl_xor_sync(am, l2, 1);
+      l2 += __shfl_xor_sync(am, l2, 2);
+      l2 += __shfl_xor_sync(am, l2, 4);
+      if ((threadIdx.x & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + k / 64, l2);
     }
     if constexpr (F16OUT) {
       uint32_t o[4];
@@ -174,15 +174,15 @@ __global__ void __launch_bounds__(kAqThreads)
       qv[e] = q < -127 ? -127 : (q > 127 ? 127 : q);
     }
     if (kbound) {
-      // sum |q| over a 64-wide k-block: 8 consecutive chunks are 8 consecutive lanes, all valid
+      // sum q^2 over a 64-wide k-block: 8 consecutive chunks are 8 consecutive lanes, all valid
       // or all past the row (K is a multiple of 64)
-      int l1 = 0;
+      int l2 = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) l1 += qv[e] < 0 ? -qv[e] : qv[e];
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
-      if (valid && (lane & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + c / 8, l1);
+      for (int e = 0; e < 8; ++e) l2 += qv[e] * qv[e];
+      l2 += __shfl_xor_sync(0xffffffffu, l2, 1);
+      l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
+      l2 += __shfl_xor_sync(0xffffffffu, l2, 4);
+      if (valid && (lane & 7) == 0) atomicMax(kbound + (int64_t)(m >> 8) * (K / 64) + c / 8, l2);
     }
     if (!valid) continue;
     if constexpr (F16OUT) {

@@ -213,7 +213,7 @@ struct qlin_layer {
   std::vector<float> sw, s, s_inv;
   // device image and its sections
   std::vector<uint8_t> image;
-  size_t sec_units = 0, sec_offs = 0, sec_ents = 0, sec_sw = 0, sec_sinv = 0, sec_perm = 0;
+  size_t sec_units = 0, sec_offs = 0, sec_ents = 0, sec_sw = 0, sec_sinv = 0, sec_perm = 0, sec_w2 = 0;
   int RG = 0, KU = 0;  // row groups, K units per row group
   // bound state
   uint8_t* dev = nullptr;
@@ -965,10 +965,13 @@ static void build_w8_image(qlin_layer* L) {
   const size_t units_bytes = align256((size_t)RG * KB * kW8UnitBytes);
   const size_t sw_bytes = align256((size_t)RG * kRowGroup * 4);
   const size_t sinv_bytes = align256((size_t)K * 4);
+  const int RT = (N + 127) / 128;  // the prefill's 128-row weight tiles
+  const size_t w2_bytes = align256((size_t)RT * KB * 4);
   L->sec_units = 0;
   L->sec_sw = units_bytes;
   L->sec_sinv = units_bytes + sw_bytes;
-  L->image.assign(units_bytes + sw_bytes + sinv_bytes, 0);
+  L->sec_w2 = units_bytes + sw_bytes + sinv_bytes;
+  L->image.assign(units_bytes + sw_bytes + sinv_bytes + w2_bytes, 0);
   uint8_t* img = L->image.data();
   parallel_for(RG, [&](int64_t b, int64_t e) {
     for (int64_t rg = b; rg < e; ++rg) {
@@ -1003,6 +1006,21 @@ static void build_w8_image(qlin_layer* L) {
   float* swd = reinterpret_cast<float*>(img + L->sec_sw);
   for (int n = 0; n < RG * kRowGroup; ++n) swd[n] = n < N ? L->sw[n] : 0.f;
   std::memcpy(img + L->sec_sinv, L->s_inv.data(), (size_t)K * 4);
+  // per (128-row tile, 64-wide k-block): the largest sum of squared codes over the tile's rows
+  uint32_t* w2 = reinterpret_cast<uint32_t*>(img + L->sec_w2);
+  parallel_for(RT, [&](int64_t b, int64_t e) {
+    for (int64_t rt = b; rt < e; ++rt)
+      for (int kb = 0; kb < KB; ++kb) {
+        uint32_t mx = 0;
+        for (int64_t n = rt * 128; n < std::min<int64_t>((rt + 1) * 128, N); ++n) {
+          const int8_t* q = L->qw.data() + n * K + (int64_t)kb * kW8Block;
+          uint32_t s2 = 0;
+          for (int k = 0; k < kW8Block; ++k) s2 += (uint32_t)((int)q[k] * (int)q[k]);
+          mx = std::max(mx, s2);
+        }
+        w2[rt * KB + kb] = mx;
+      }
+  });
 }
 
 // ------------------------------------------------------------------------------------
@@ -1017,7 +1035,8 @@ static SpqrView spqrview(const qlin_layer* L) {
 }
 static W8View w8view(const qlin_layer* L) {
   return W8View{L->dev + L->sec_units, reinterpret_cast<const float*>(L->dev + L->sec_sw),
-                reinterpret_cast<const float*>(L->dev + L->sec_sinv), L->N, L->K, L->RG, L->KU};
+                reinterpret_cast<const float*>(L->dev + L->sec_sinv), L->N, L->K, L->RG, L->KU,
+                reinterpret_cast<const uint32_t*>(L->dev + L->sec_w2)};
 }
 
 int qlin_spqr_view_of(qlin_layer* h, SpqrView* out) {

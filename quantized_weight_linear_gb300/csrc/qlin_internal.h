@@ -93,6 +93,9 @@ struct W8View {
   const float* sw;       // [Npad]
   const float* s_inv;    // [K]
   int N, K, RG, KB;
+  // [ceil(N / 128)][K / 64]: max over a 128-row tile of sum qw^2 over a 64-wide k-block (the
+  // prefill's exact-chunk bounds)
+  const uint32_t* w2;
 };
 
 // Workspace carve-up (all offsets 256-byte aligned).
@@ -105,7 +108,7 @@ struct Workspace {
   void* qx;            // W8A8: fp16 activation codes [maxM][K]
   float* sx;           // W8A8: [maxM]
   int32_t* kbound;     // W8A8 prefill: [ceil(maxM / 256)][K / 64] max over a 256-token tile of
-                       // sum |qx| over a 64-wide k-block (sizes the exact fp32 chunks)
+                       // sum qx^2 over a 64-wide k-block (sizes the exact fp32 chunks)
   int grid;            // largest decode grid the partial slots were sized for
   int sms;             // SM count of the device
 };
