@@ -418,7 +418,7 @@ __device__ __forceinline__ uint32_t sp_pair(const uint32_t (&w)[6], const SpOr& 
 // = 2h, 2h + 1 of its MMAs 2m and 2m + 1.  The B operand of column g then holds four
 // consecutive activations of group g (one aligned register pair) on the four lanes of the
 // set's diagonal and zeros elsewhere, and accumulator column n still sums group n.
-template <int M, int H>
+template <int M, int H, bool Z = false>
 __device__ __forceinline__ void sp_mma(const uint32_t (&w)[6], const SpOr& k, const uint32_t (&b)[8],
                                        float (&c)[4]) {
   uint32_t a[4];
@@ -426,7 +426,12 @@ __device__ __forceinline__ void sp_mma(const uint32_t (&w)[6], const SpOr& k, co
   a[1] = sp_pair<2 * M, 2 * H + 1>(w, k);
   a[2] = sp_pair<2 * M + 1, 2 * H>(w, k);
   a[3] = sp_pair<2 * M + 1, 2 * H + 1>(w, k);
-  mma_bf16(c, a, b[2 * M], b[2 * M + 1]);
+  if constexpr (Z) {  // the first MMA of a chain: zero C operand
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16_c(c, a, b[2 * M], b[2 * M + 1], zero4);
+  } else {
+    mma_bf16(c, a, b[2 * M], b[2 * M + 1]);
+  }
 }
 
 template <int STAGES>
@@ -664,7 +669,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
       // sums of x of the accumulator columns 2t, 2t + 1 of both blocks
       const float4 qA = gq[ls * 8 + t], qB = gq[ls * 8 + 4 + t];
       const float2 gA = gs[ls * 8 + t], gB = gs[ls * 8 + 4 + t];
-      float c0[4], c1[4];
+      float c0[4], c1[4], e0[4], e1[4];
       {
         uint32_t bx0[8], by0[8], bx1[8], by1[8];
         {
@@ -701,20 +706,21 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
           a[3] = sp_pair<1, 1>(w1, kor);
           mma_bf16_c4(c1, a, bx1[0], bx1[1], qB);
         }
+        // the second set of each block in chains of its own (four chains of four MMAs)
+        sp_mma<0, 1, true>(w0, kor, by0, e0);
+        sp_mma<0, 1, true>(w1, kor, by1, e1);
         sp_mma<1, 0>(w0, kor, bx0, c0);
         sp_mma<1, 0>(w1, kor, bx1, c1);
+        sp_mma<1, 1>(w0, kor, by0, e0);
+        sp_mma<1, 1>(w1, kor, by1, e1);
         sp_mma<2, 0>(w0, kor, bx0, c0);
         sp_mma<2, 0>(w1, kor, bx1, c1);
+        sp_mma<2, 1>(w0, kor, by0, e0);
+        sp_mma<2, 1>(w1, kor, by1, e1);
         sp_mma<3, 0>(w0, kor, bx0, c0);
         sp_mma<3, 0>(w1, kor, bx1, c1);
-        sp_mma<0, 1>(w0, kor, by0, c0);
-        sp_mma<0, 1>(w1, kor, by1, c1);
-        sp_mma<1, 1>(w0, kor, by0, c0);
-        sp_mma<1, 1>(w1, kor, by1, c1);
-        sp_mma<2, 1>(w0, kor, by0, c0);
-        sp_mma<2, 1>(w1, kor, by1, c1);
-        sp_mma<3, 1>(w0, kor, by0, c0);
-        sp_mma<3, 1>(w1, kor, by1, c1);
+        sp_mma<3, 1>(w0, kor, by0, e0);
+        sp_mma<3, 1>(w1, kor, by1, e1);
       }
       // first-level statistics of the accumulator's (row, group) pairs, decoded exactly:
       // a 3-bit field at bit p OR-ed under the exponent of 2^23 is the float 2^23 + q 2^p;
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
             if (i == 3) { qb = and_or<7u << 18>(q24, kmagic); zb2 = and_or<7u << 18>(z24, kmagic); }
             const float sh = __fmul_rn(__fsub_rn(__uint_as_float(qb), kcs[i]), kms[i]);
             const float zh = __fmul_rn(__fsub_rn(__uint_as_float(zb2), kcz[i]), kmz[i]);
-            const float C = blk ? c1[i] : c0[i];
+            const float C = blk ? c1[i] + e1[i] : c0[i] + e0[i];
             acc[i] = fmaf(sh, fmaf(-zh, (i & 1) ? S1 : S0, C), acc[i]);
           }
         }
@@ -959,14 +965,20 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
       const uint4 q0 = *reinterpret_cast<const uint4*>(unit + code_off);
       const uint4 q1 = *reinterpret_cast<const uint4*>(unit + code_off + 512);
       mbar_arrive(&h.empty[grp][s]);  // the stage's bytes are in registers
+      if (++s == STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
       const float Sg = gtab[ls];
       const uint4* xb = reinterpret_cast<const uint4*>(xfl + ls * 64);
       const uint4 xa = xb[0], xbb = xb[1], xc = xb[2], xd = xb[3];
       const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
       const uint32_t bx[16] = {xa.x, xa.y, xa.z, xa.w, xbb.x, xbb.y, xbb.z, xbb.w,
                                xc.x, xc.y, xc.z, xc.w, xd.x, xd.y, xd.z, xd.w};
-      // two accumulator chains (even / odd k16 step); each starts from a zero C operand
-      float c[4], d[4];
+      // four independent accumulator chains over the eight k16 steps (two dependent MMAs each,
+      // measured 2% faster than two chains of four); each starts from a zero C operand
+      constexpr int NC = 4;
+      float c[NC][4];
       const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -976,23 +988,21 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
         a[1] = and_or<0x000F000Fu>(w >> 4, kor);
         a[2] = and_or<0x000F000Fu>(w >> 8, kor);
         a[3] = and_or<0x000F000Fu>(w >> 12, kor);
-        if (j == 0)
-          mma_bf16_c(c, a, bx[0], bx[1], zero4);
-        else if (j == 1)
-          mma_bf16_c(d, a, bx[2], bx[3], zero4);
-        else if (j & 1)
-          mma_bf16(d, a, bx[2 * j], bx[2 * j + 1]);
+        if (j < NC)
+          mma_bf16_c(c[j % NC], a, bx[2 * j], bx[2 * j + 1], zero4);
         else
-          mma_bf16(c, a, bx[2 * j], bx[2 * j + 1]);
+          mma_bf16(c[j % NC], a, bx[2 * j], bx[2 * j + 1]);
+      }
+      float r0 = c[0][0], r2 = c[0][2];
+#pragma unroll
+      for (int q = 1; q < NC; ++q) {
+        r0 += c[q][0];
+        r2 += c[q][2];
       }
       // sum (128 + q) x - (128 + z) sum x = sum (q - z) x, then the group's scale
       const float2 p0 = h2f2(sz0), p1 = h2f2(sz1);  // (scale, zero) of rows g and g + 8
-      acc0 = fmaf(p0.x, fmaf(-(128.f + p0.y), Sg, c[0] + d[0]), acc0);
-      acc1 = fmaf(p1.x, fmaf(-(128.f + p1.y), Sg, c[2] + d[2]), acc1);
-      if (++s == STAGES) {
-        s = 0;
-        ph ^= 1u;
-      }
+      acc0 = fmaf(p0.x, fmaf(-(128.f + p0.y), Sg, r0), acc0);
+      acc1 = fmaf(p1.x, fmaf(-(128.f + p1.y), Sg, r2), acc1);
       if (++ls == (int)G) ls = 0;
     }
     if (t == 0) {
