@@ -138,8 +138,10 @@ qlin_status qlin_pack_w4g128(const float* W, int N, int K, qlin_handle* out);
  * irregular in the original order): the columns are taken by decreasing diag(H) (an
  * always-zero input counted as 1, ties to the smaller index) and W[:, perm] is quantized as
  * above under H[perm][perm]; the handle keeps perm (exported and imported with the codes),
- * and every forward first gathers X[:, perm] into the workspace (one more kernel launch, the
- * run-time price the page mentions; M <= the workspace's max_M).
+ * and the forward reads X in the permuted order: one token with K <= 8192 is gathered by the
+ * single-token kernel while it stages x, any other forward first gathers X[:, perm] into the
+ * workspace (one more kernel launch; M <= the workspace's max_M) -- the run-time price the
+ * page mentions.
  * W: host fp32 [N][K]; Xcal: host fp32 [S][K] calibration inputs (row-major); both read only,
  * not retained.  K % 128 == 0, K <= 8192 (H and its factors are K x K fp64 on the host),
  * S >= 1, damp > 0 (0.01 is the usual value), W and Xcal finite.  Returns INVALID_ARG on bad
