@@ -104,6 +104,15 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #ifndef QLIN_SP_NPK
 #define QLIN_SP_NPK 2
 #endif
+#ifndef QLIN_SP_GROUPS
+#define QLIN_SP_GROUPS 2
+#endif
+#ifndef QLIN_SP_PAIR_ST
+#define QLIN_SP_PAIR_ST 4
+#endif
+#ifndef QLIN_TC_SPQR_PAIRS
+#define QLIN_TC_SPQR_PAIRS 1
+#endif
 #ifndef QLIN_W4_CONV
 #define QLIN_W4_CONV 8
 #endif
@@ -125,7 +134,7 @@ struct TcCfg<kW4> {
 template <>
 struct TcCfg<kSpqr> {
   static constexpr int kUnitBytes = kSpqrUnitBytes, kBlocksPerUnit = 4, kMH = 2, kConv = 16, kStages = 3;
-  static constexpr int kConvGroups = 2;  // two groups of 8 converter warps take alternate k-blocks
+  static constexpr int kConvGroups = QLIN_SP_GROUPS;  // two groups of 8 converter warps take alternate k-blocks
   static constexpr int kNPK = QLIN_SP_NPK;
   static constexpr uint32_t kAType = 1;
   static constexpr bool kRowsInLanes = false;  // D = tokens (lanes) x weight rows (columns)
@@ -141,15 +150,20 @@ struct TcCfg<kW8> {
   static constexpr bool kATmem = QLIN_W8_ATMEM;
 };
 
-template <int F>
+// CL: a CTA of a pair stages the packed units, outliers and offsets of its one row group, and
+// spends the room on one more operand stage
+template <int F, bool CL = false>
 struct TcSmem {
   using C = TcCfg<F>;
-  __align__(1024) uint8_t a[C::kStages][C::kMH * kTileBytes];
-  __align__(1024) uint8_t b[C::kStages][C::kATmem ? 16 : kTileBytes];
-  __align__(16) uint8_t pk[C::kNPK][2 * C::kUnitBytes];
-  __align__(16) uint32_t out[F == kSpqr ? C::kNPK : 1][2][F == kSpqr ? kOutCapTc + 8 : 4];
-  __align__(16) uint32_t offs[2][F == kSpqr ? kOffsCapTc : 4];
-  uint64_t ab_full[C::kStages], ab_empty[C::kStages];
+  static constexpr int kStages = CL && F == kSpqr ? QLIN_SP_PAIR_ST : C::kStages;
+  static constexpr int kRG = CL ? 1 : 2;  // row groups staged
+  __align__(1024) uint8_t a[kStages][C::kMH * kTileBytes];
+  __align__(1024) uint8_t b[kStages][C::kATmem ? 16 : kTileBytes];
+  __align__(16) uint8_t pk[C::kNPK][kRG * C::kUnitBytes];
+  __align__(16) uint32_t out[F == kSpqr ? C::kNPK : 1][kRG][F == kSpqr ? kOutCapTc + 8 : 4];
+  __align__(16) uint32_t offs[kRG][F == kSpqr ? kOffsCapTc : 4];
+  // stage releases: one barrier per k-block modulo max(stages, converter groups), see the kernel
+  uint64_t ab_full[kStages], ab_empty[kStages > 4 ? kStages : 4];
   uint64_t pk_full[C::kNPK], pk_empty[C::kNPK];
   uint64_t offs_bar;
   uint64_t acc_full;
@@ -209,6 +223,67 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// ---- a CTA pair (cluster of two) sharing one weight tile -------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the address of a shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// copy `bytes` (a multiple of 16) of this CTA's shared memory to `dst` in a CTA of the
+// cluster; the copy completes as transaction bytes on the barrier at `bar` in that CTA (both
+// shared::cluster addresses)
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// a bounded wait that acquires at cluster scope: for barriers the partner CTA arrives on
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_scope(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if constexpr (!CLUSTER) {
+    return mbar_wait(bar, parity, status);
+  } else {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if (global_ns() - t0 > kWaitLimitNs) break;
+    }
+    if (status) atomicExch(status, kStatusTimeout);
+    return false;
+  }
+}
+
+// commit to the same barrier in both CTAs of the pair
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -521,16 +596,34 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <int F>
+// CL (SpQR, an even number of token tiles): the two CTAs of a cluster take consecutive token
+// tiles of one weight tile; each loads and converts one of its two 64-row groups and bulk-copies
+// the converted rows into the partner's operand tile, so a weight tile is converted once per pair.
+template <int F, bool CL = false>
 __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  TcSmem<F>& sm = *reinterpret_cast<TcSmem<F>*>(base);
+  using SM = TcSmem<F, CL>;
+  SM& sm = *reinterpret_cast<SM*>(base);
   using C = TcCfg<F>;
-  constexpr int MH = C::kMH, NCONV = C::kConv, NST = C::kStages;
-  constexpr int NGRP = C::kConvGroups, GCONV = NCONV / NGRP;  // converter warps per k-block
+  constexpr int MH = C::kMH, NCONV = C::kConv, NST = SM::kStages;
+  static_assert(!CL || F == kSpqr, "CTA pairs are built for SpQR");
+  // converter warps per k-block: a pair's CTA converts 64 rows, with four groups of four warps
+  // taking every fourth k-block
+  constexpr int NGRP = CL ? 4 : C::kConvGroups, GCONV = NCONV / NGRP;
+  // Stage releases.  The MMA commit of k-block j arrives on ab_empty[j % NEB]; whoever fills
+  // k-block i's stage first waits for the commit of k-block i - NST there.  A parity wait only
+  // tells a phase from the next one, so the phase before (k-block i - NST - NEB) must already be
+  // known complete: the X producer and each converter group waited for exactly that commit on
+  // the same barrier before their previous k-block (i - 1, resp. i - NGRP) whenever NEB is a
+  // multiple of NGRP, which NEB = max(NST, NGRP) makes true for NGRP > NST.  With one barrier
+  // per stage and four groups over three stages, a group two stages ahead passed the wait
+  // and overwrote a stage the tensor cores had not read yet.
+  constexpr int NEB = NGRP > NST ? NGRP : NST;
+  static_assert(NEB <= (NST > 4 ? NST : 4), "ab_empty holds max(stages, 4) barriers");
   constexpr int BM = 128 * MH;
   constexpr int kLoaderWarp = tc_loader_warp<F>();
+  const uint32_t crank = CL ? cluster_rank() : 0u, partner = crank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // grouped raster: consecutive CTAs walk kRasterG token tiles of one weight tile before the
   // next weight tile, so a wave reads each weight tile from HBM once and shares it through L2
@@ -568,15 +661,13 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       const int64_t b = ((rg0 + r) * a.KU * 4) & ~int64_t(3);
       const int64_t e = ((rg0 + r) * a.KU * 4 + 4 * a.KU + 1 + 3) & ~int64_t(3);
       off_base[r] = b;
-      off_len[r] = (rg0 + r < a.RG) ? (uint32_t)(e - b) : 0u;
+      off_len[r] = (rg0 + r < a.RG && (!CL || r == (int)crank)) ? (uint32_t)(e - b) : 0u;
     }
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&sm.ab_full[s], 1 + GCONV);
-      mbar_init(&sm.ab_empty[s], 1);
-    }
+    for (int s = 0; s < NST; ++s) mbar_init(&sm.ab_full[s], 1 + GCONV);  // CL: + the partner's rows as tx bytes
+    for (int e = 0; e < NEB; ++e) mbar_init(&sm.ab_empty[e], CL ? 2 : 1);                    // CL: both CTAs' MMAs
     for (int s = 0; s < C::kNPK; ++s) {
       mbar_init(&sm.pk_full[s], 1);
       mbar_init(&sm.pk_empty[s], NCONV);
@@ -599,9 +690,18 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (CL) cluster_sync_all();  // the partner's barriers are initialized
   const uint32_t tmem = sm.tmem;
   bool ok = true;
-  auto soffs = [&](int r, int64_t gi) -> uint32_t { return sm.offs[r][gi - off_base[r]]; };
+  // staging slot of row group r (0 or 1 of the weight tile); a pair's CTA stages only its own
+  auto slot = [&](int r) -> int { return CL ? 0 : r; };
+  auto soffs = [&](int r, int64_t gi) -> uint32_t { return sm.offs[slot(r)][gi - off_base[r]]; };
+  // k-block i's stage is free: the tensor cores have read k-block i - NST (both CTAs' in a pair)
+  auto stage_free = [&](int i) -> bool {
+    if (i < NST) return true;
+    const int j = i - NST;
+    return mbar_wait_scope<CL>(&sm.ab_empty[j % NEB], (uint32_t)(j / NEB) & 1u, a.status);
+  };
 
   if (warp == kLoaderWarp) {
     // ------------------------------------------------------------------ packed-unit loader
@@ -615,7 +715,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         for (int r = 0; r < 2; ++r) bytes += off_len[r] * 4;
         mbar_arrive_expect_tx(&sm.offs_bar, bytes);
         for (int r = 0; r < 2; ++r)
-          if (off_len[r]) bulk_g2s(sm.offs[r], a.offs + off_base[r], off_len[r] * 4, &sm.offs_bar);
+          if (off_len[r]) bulk_g2s(sm.offs[slot(r)], a.offs + off_base[r], off_len[r] * 4, &sm.offs_bar);
         ok = mbar_wait(&sm.offs_bar, 0, a.status);
       }
       for (int ui = 0; ui < nunits && ok; ++ui) {
@@ -628,7 +728,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         uint32_t bytes = 0;
         uint32_t e_lo[2] = {0, 0}, e_hi[2] = {0, 0};
         for (int r = 0; r < 2; ++r) {
-          if (rg0 + r >= a.RG) continue;
+          if (rg0 + r >= a.RG || (CL && r != (int)crank)) continue;
           bytes += C::kUnitBytes;
           if constexpr (F == kSpqr) {
             const int64_t u = (rg0 + r) * a.KU + ui;
@@ -642,11 +742,11 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         }
         mbar_arrive_expect_tx(&sm.pk_full[p], bytes);
         for (int r = 0; r < 2; ++r) {
-          if (rg0 + r >= a.RG) continue;
-          bulk_g2s(sm.pk[p] + r * C::kUnitBytes, a.units + ((rg0 + r) * a.KU + ui) * (int64_t)C::kUnitBytes,
+          if (rg0 + r >= a.RG || (CL && r != (int)crank)) continue;
+          bulk_g2s(sm.pk[p] + slot(r) * C::kUnitBytes, a.units + ((rg0 + r) * a.KU + ui) * (int64_t)C::kUnitBytes,
                    C::kUnitBytes, &sm.pk_full[p]);
           if constexpr (F == kSpqr) {
-            if (e_hi[r] > e_lo[r]) bulk_g2s(sm.out[p][r], a.ents + e_lo[r], (e_hi[r] - e_lo[r]) * 4, &sm.pk_full[p]);
+            if (e_hi[r] > e_lo[r]) bulk_g2s(sm.out[p][slot(r)], a.ents + e_lo[r], (e_hi[r] - e_lo[r]) * 4, &sm.pk_full[p]);
           }
         }
       }
@@ -657,12 +757,12 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     if (lane == 0) {
       for (int i = 0; i < nkb && ok; ++i) {
         const int s = i % NST;
-        const uint32_t ph = (uint32_t)(i / NST) & 1u;
-        if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
+        if (!stage_free(i)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.ab_full[s], MH * kTileBytes);
+        // CL: the partner's 64 converted rows arrive on this barrier too
+        mbar_arrive_expect_tx(&sm.ab_full[s], MH * kTileBytes + (CL ? 64u * 128u : 0u));
         tma_load_2d(sm.a[s], &xmap, i * kBK, m_tile * BM, &sm.ab_full[s]);
       }
     }
@@ -704,7 +804,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
             chunk_end = i == nkb - 1 || bound + bnext > kExactSum;
           }
         }
-        if (!mbar_wait(&sm.ab_full[s], ph, a.status)) {
+        if (!mbar_wait_scope<CL>(&sm.ab_full[s], ph, a.status)) {
           ok = false;
           break;
         }
@@ -731,12 +831,23 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
                        (first && kk == 0) ? 0u : 1u);
           }
         }
-        umma_commit(&sm.ab_empty[s]);
+        if constexpr (CL)
+          umma_commit_pair(&sm.ab_empty[i % NEB]);  // the partner's converters write this stage too
+        else
+          umma_commit(&sm.ab_empty[i % NEB]);
         if constexpr (F == kW8) {
           if (chunk_end) umma_commit(&sm.ch_full[0]);
         }
       }
       umma_commit(&sm.acc_full);
+      if constexpr (CL) {
+        // commits reach both CTAs' barriers asynchronously; a converter waited for each one up to
+        // k-block nkb - NST - 1 before filling the stage again.  Wait for the last NST here (the
+        // partner does the same), so that no arrival is still on its way to a CTA when the pair
+        // passes its final cluster barrier and leaves
+        for (int i = nkb - NST > 0 ? nkb - NST : 0; i < nkb && ok; ++i)
+          if (!mbar_wait_scope<CL>(&sm.ab_empty[i % NEB], (uint32_t)(i / NEB) & 1u, a.status)) ok = false;
+      }
     }
     __syncwarp();
   } else if (warp < 2 + NCONV) {
@@ -744,11 +855,12 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     pdl_wait();
     const int grp = (warp - 2) / GCONV;  // this warp converts the k-blocks i with i % NGRP == grp
     const int cw = (warp - 2) % GCONV;
-    constexpr int RPW = 128 / GCONV;  // rows per converter warp: 16 or 32
+    constexpr int RPW = (CL ? 64 : 128) / GCONV;  // rows per converter warp: 16 or 32
     const LaneSwz swz = lane_swz(lane);
     // TMEM operand: a warp may only reach the lane quadrant warp % 4, so converter warp cw
-    // takes rows 32 ((2 + cw) % 4) + 16 (cw / 4) (the group's first warp index is 2 mod 4)
-    const int row_t = C::kATmem ? 32 * ((2 + cw) % 4) + 16 * (cw / 4) : cw * RPW;
+    // takes rows 32 ((2 + cw) % 4) + 16 (cw / 4) (the group's first warp index is 2 mod 4);
+    // CL: the rows of this CTA's row group
+    const int row_t = C::kATmem ? 32 * ((2 + cw) % 4) + 16 * (cw / 4) : (CL ? 64 * (int)crank : 0) + cw * RPW;
     const int rg_local = row_t / 64;
     const bool rg_valid = rg0 + rg_local < a.RG;
     if constexpr (F == kSpqr) {
@@ -760,13 +872,12 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         ok = false;
         break;
       }
-      const uint8_t* unit = sm.pk[p] + rg_local * C::kUnitBytes;
+      const uint8_t* unit = sm.pk[p] + slot(rg_local) * C::kUnitBytes;
       for (int b = 0; b < bpu; ++b) {
         const int i = ui * bpu + b;
         if (NGRP > 1 && i % NGRP != grp) continue;
         const int s = i % NST;
-        const uint32_t ph = (uint32_t)(i / NST) & 1u;
-        if (!mbar_wait(&sm.ab_empty[s], ph ^ 1u, a.status)) {
+        if (!stage_free(i)) {
           ok = false;
           break;
         }
@@ -778,7 +889,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
         } else {
 #pragma unroll
           for (int h = 0; h < RPW / 16; ++h) {
-            const int row0 = cw * RPW + 16 * h;
+            const int row0 = row_t + 16 * h;
             const int rt = (row0 % 64) / 16;
             convert_tile<F>(sm.b[s], unit, b, rt, row0, lane, rg_valid, swz);
             if constexpr (F == kSpqr) {
@@ -787,7 +898,7 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
                 const int64_t u = (rg0 + rg_local) * a.KU + ui;
                 const uint32_t e0 = soffs(rg_local, 4 * u), e1 = soffs(rg_local, 4 * u + 4);
                 const bool staged = e1 > e0 && e1 - e0 <= (uint32_t)kOutCapTc;
-                spqr_outliers_tile(sm.b[s], staged ? sm.out[p][rg_local] : nullptr, e0 & ~3u, a.ents,
+                spqr_outliers_tile(sm.b[s], staged ? sm.out[p][slot(rg_local)] : nullptr, e0 & ~3u, a.ents,
                                    soffs(rg_local, 4 * u + rt), soffs(rg_local, 4 * u + rt + 1), b, row0, lane);
               }
             }
@@ -795,7 +906,16 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ab_full[s]);
+        if (lane == 0) {
+          mbar_arrive(&sm.ab_full[s]);
+          if constexpr (CL) {
+            // the same rows into the partner's tile (RPW rows of 128 bytes, whole swizzle atoms);
+            // its stage is free: both CTAs' tensor cores have read k-block i - NST
+            const uint32_t o = (uint32_t)row_t * 128u;
+            bulk_s2s_cluster(mapa_shared(smem_u32(sm.b[s] + o), partner), sm.b[s] + o, RPW * 128u,
+                             mapa_shared(smem_u32(&sm.ab_full[s]), partner));
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.pk_empty[p]);
@@ -805,8 +925,9 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
       // 32q.., the two warps of a quadrant take one 128-token half each; a warp's store of one
       // token writes 32 consecutive outputs of Y's row
       const int q = warp & 3;
-      const int mh = cw / 4;
-      if (grp == 0 && ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
+      const int mh = (warp - 2) / 4;
+      const bool epi = warp - 2 < 8;  // the first eight converter warps, two per TMEM lane quadrant
+      if (epi && ok && mbar_wait(&sm.acc_full, 0u, a.status)) {
         tc_fence_after();
         if constexpr (kRowsInLanes) {
           const int n = n_tile * kBN + 32 * q + lane;
@@ -941,6 +1062,9 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     }
   }
 
+  __syncwarp();
+  // CL: neither CTA leaves while the partner may still write into its tile or barriers
+  if constexpr (CL) cluster_sync_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -967,20 +1091,31 @@ int launch_tc(const void* Xop, const TcArgs& args, void* stream) {
   CUresult r = enc(&map, dt, 2, const_cast<void*>(Xop), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
-  const size_t smem = sizeof(TcSmem<F>) + 1024;
-  static std::atomic<uint64_t> attr_done{0};
-  if (const int e = smem_attr_once(tc_gemm_kernel<F>, smem, attr_done)) return e;
+  const int mt_count = (args.M + BM - 1) / BM;
+  // SpQR with an even number of token tiles: CTA pairs (every pair of consecutive tiles of the
+  // grouped raster shares its weight tile then)
+  const bool pair = F == kSpqr && QLIN_TC_SPQR_PAIRS && mt_count % 2 == 0;
+  static_assert(sizeof(TcSmem<F, true>) + 1024 <= 227 * 1024 && sizeof(TcSmem<F>) + 1024 <= 227 * 1024,
+                "shared memory per CTA");
+  const size_t smem = (pair ? sizeof(TcSmem<F, true>) : sizeof(TcSmem<F>)) + 1024;
+  auto* kern = pair ? tc_gemm_kernel<F, F == kSpqr> : tc_gemm_kernel<F, false>;
+  static std::atomic<uint64_t> attr_done[2];
+  if (const int e = smem_attr_once(kern, smem, attr_done[pair ? 1 : 0])) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(((args.N + kBN - 1) / kBN) * ((args.M + BM - 1) / BM)));
+  cfg.gridDim = dim3((unsigned)(((args.N + kBN - 1) / kBN) * mt_count));
   cfg.blockDim = dim3(tc_threads<F>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = QLIN_USE_PDL;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, tc_gemm_kernel<F>, map, args);
+  cfg.numAttrs = pair ? 2 : 1;
+  return (int)cudaLaunchKernelEx(&cfg, kern, map, args);
 }
 
 }  // namespace

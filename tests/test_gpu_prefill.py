@@ -34,7 +34,10 @@ def test_w4_prefill_tolerance(qlin, N, K, M):
     assert ok, worst
 
 
-@pytest.mark.parametrize("N,K,M,frac", [(128, 512, 17, 0.01), (256, 1024, 160, 0.02), (192, 768, 64, 0.01)])
+# M = 300, 1024: an even number of 256-token tiles, so CTA pairs share the weight tiles (N = 320:
+# a last weight tile of one 64-row group)
+@pytest.mark.parametrize("N,K,M,frac", [(128, 512, 17, 0.01), (256, 1024, 160, 0.02), (192, 768, 64, 0.01),
+                                        (256, 1024, 300, 0.01), (320, 512, 1024, 0.02)])
 def test_spqr_prefill_tolerance(qlin, N, K, M, frac):
     W, X = synth.spqr_layer(N, K, M, seed=M)
     layer = qlin.QLinear.from_spqr(W, frac).to("cuda")
