@@ -211,11 +211,12 @@ def test_spqr_forward_tolerance(qlin, N, K, frac, M):
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
 
 
-@pytest.mark.parametrize("M", [1, 5, 16, 40])
+@pytest.mark.parametrize("M", [1, 5, 16, 40, 512])
 def test_spqr_outliers_crowded_into_few_rows(qlin, M):
     """Four rows carry weights 100x larger, so most outliers sit in them: row runs of
     hundreds of entries inside one bucket, and units whose outliers overflow the staged copy
-    (read from global memory instead).  M = 40 runs the same layer through the prefill path."""
+    (read from global memory instead).  M = 40 runs the same layer through the prefill path,
+    M = 512 through its CTA pairs (two token tiles share each weight tile)."""
     N, K, frac = 128, 1024, 0.04
     W = synth.student_t3(23, 0.02, (N, K))
     W[[5, 6, 7, 70]] *= 100.0
@@ -224,10 +225,11 @@ def test_spqr_outliers_crowded_into_few_rows(qlin, M):
     _check(_y(layer, X, M), X, spqr.pack(W, frac)["w_hat"])
 
 
-@pytest.mark.parametrize("M", [1, 5, 40])
+@pytest.mark.parametrize("M", [1, 5, 40, 512])
 def test_spqr_widest_rows(qlin, M):
     """K = 32768, the widest row the int16 outlier columns allow (128 supergroups per row
-    group, a long staged range of bucket offsets per CTA), decode and prefill."""
+    group, a long staged range of bucket offsets per CTA), decode and prefill (M = 512: CTA
+    pairs over 512 k-blocks)."""
     N, K = 96, 32768
     W, X = synth.spqr_layer(N, K, M, seed=31)
     layer = qlin.QLinear.from_spqr(W, 0.01).to("cuda")
@@ -273,16 +275,17 @@ def test_spqr_one_hot_rows(qlin):
 def test_spqr_zero_dequantized_scale_groups(qlin):
     """Groups whose 3-bit scale code is 0 (dequantized scale exactly 0, codes 0, the group's
     outlier kept as fp16(w)): device dequantization bit-exact, decode (M = 1, 5) and prefill
-    (M = 40) within tolerance, and the one-hot columns of the outliers bit-exact at M = 1."""
+    (M = 40; 512 in CTA pairs) within tolerance, and the one-hot columns of the outliers
+    bit-exact at M = 1."""
     N, K = 128, 512
     W = synth.spqr_quiet_group_layer(N, K, seed=4)
     frac = (N + 0.5) / (N * K)
     p = spqr.pack(W, frac)
-    layer = qlin.QLinear.from_spqr(W, frac).to("cuda", max_M=40)
+    layer = qlin.QLinear.from_spqr(W, frac).to("cuda", max_M=512)
     assert layer.handle.info.nnz == N
     wd = layer.dequant_device().cpu().numpy()
     assert np.array_equal(wd.view(np.uint32), p["w_hat"].view(np.uint32))
-    for M in (1, 5, 40):
+    for M in (1, 5, 40, 512):
         X = synth.activations_bf16(4, M, K)
         _check(_y(layer, X, M), X, p["w_hat"])
     for k in sorted({int(np.flatnonzero(p["mask"][r])[0]) for r in range(0, N, 9)}):
