@@ -137,7 +137,7 @@ struct TcCfg<kSpqr> {
   static constexpr int kConvGroups = QLIN_SP_GROUPS;  // two groups of 8 converter warps take alternate k-blocks
   static constexpr int kNPK = QLIN_SP_NPK;
   static constexpr uint32_t kAType = 1;
-  static constexpr bool kRowsInLanes = false;  // D = tokens (lanes) x weight rows (columns)
+  static constexpr bool kRowsInLanes = false;  // D = tokens (lanes) x weight rows (columns); pairs: see the kernel
   static constexpr bool kATmem = false;
 };
 template <>
@@ -644,7 +644,11 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
   // (N = 256 tokens); D in TMEM has the weight rows in its lanes and the tokens in its columns.
   // SpQR: two MMAs per k-step, A = one 128-token half of X, B = the weight tile (N = 128); D
   // has the tokens in its lanes (measured faster for SpQR only).
-  constexpr bool kRowsInLanes = C::kRowsInLanes;
+  // CL: weight rows in the lanes too.  With the conversion shared by the pair, shared-memory
+  // reads limit the loop, and one M = 128 x N = 256 MMA per k-step reads the weight tile once
+  // where two 128-token MMAs read it twice (1.65 -> 1.48 ms at K = 8192, N = 28672; single
+  // CTAs, bound by their converters, are 2% faster with the tokens in the lanes)
+  constexpr bool kRowsInLanes = C::kRowsInLanes || CL;
   static_assert(F != kW8 || kRowsInLanes, "the W8A8 drain reads weight rows from TMEM lanes");
   constexpr uint32_t idesc = kRowsInLanes ? idesc_f16(C::kAType, BM, kBN) : idesc_f16(C::kAType, kBN, 128);
   // W8A8: fp32 chunk sums + int32 partials; W4: the accumulator, then one 32-column A operand
