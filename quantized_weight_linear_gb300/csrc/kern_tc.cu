@@ -51,8 +51,10 @@ constexpr int kTileBytes = 128 * kBK * 2;  // 16 KB, one 128-row operand tile
 // weight rows: by Cauchy-Schwarz no token-row product sum of the block exceeds it.  A chunk
 // starts from a carried low part in [0, 2^16) (see the drain), so every partial sum is an
 // integer of magnitude < 2^16 + kExactSum <= 2^24 and fp32 holds it exactly.  A block's bound
-// is at most 64 * 127^2, so a chunk holds at least 16 blocks (1024 K).
+// is at most 64 * 127^2, so a chunk holds at least kChunkMin = 16 blocks (1024 K).
 constexpr int kExactSum = (1 << 24) - (1 << 16);
+constexpr int kChunkMin = 16;
+static_assert(kChunkMin * 64 * 127 * 127 <= kExactSum, "kChunkMin blocks always fit one chunk");
 
 // an upper bound of ceil(sqrt(x2 w2)): both < 2^24 are exact in fp32, the product and the
 // square root each round by at most 2^-24 relative, the 2^-20 margin covers both
@@ -60,15 +62,6 @@ __device__ __forceinline__ int block_bound(int32_t x2, uint32_t w2) {
   return (int)(sqrtf((float)x2 * (float)w2) * 1.00000095f) + 1;
 }
 
-// Whether a whole tile's blocks fit one exact chunk: the sum of all block bounds, the lanes of
-// a warp taking every 32nd block (every lane of the warp calls this)
-__device__ __forceinline__ bool one_exact_chunk(const int32_t* kb, const uint32_t* kw, int nkb, int lane) {
-  long long tot = 0;
-  for (int j = lane; j < nkb; j += 32) tot += block_bound(kb[j], kw[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  return tot <= kExactSum;
-}
 constexpr int kOutCapTc = 1024;            // SpQR outlier entries staged per (unit, row group)
 constexpr int kOffsCapTc = 1040;           // SpQR bucket offsets staged per row group
 #ifndef QLIN_TC_RASTER_G
@@ -106,6 +99,9 @@ enum Fmt { kW4 = 0, kSpqr = 1, kW8 = 2 };
 #endif
 #ifndef QLIN_SP_GROUPS
 #define QLIN_SP_GROUPS 2
+#endif
+#ifndef QLIN_W8_PLAN_PAR
+#define QLIN_W8_PLAN_PAR 1
 #endif
 #ifndef QLIN_SP_PAIR_ST
 #define QLIN_SP_PAIR_ST 4
@@ -168,6 +164,9 @@ struct TcSmem {
   uint64_t offs_bar;
   uint64_t acc_full;
   uint64_t ch_full[2], ch_empty[2];
+  uint64_t plan_full;  // W8A8: the drain warps have decided whether the tile is one exact chunk
+  unsigned long long plan_sum;  // W8A8: the sum of the tile's block bounds
+  int plan_one;
   uint32_t tmem;
 };
 
@@ -678,6 +677,8 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     }
     mbar_init(&sm.offs_bar, 1);
     mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.plan_full, 1);
+    sm.plan_sum = 0ull;
     for (int r = 0; r < 2; ++r) {
       mbar_init(&sm.ch_full[r], 1);
       mbar_init(&sm.ch_empty[r], 8);
@@ -774,27 +775,75 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     // ------------------------------------------------------------------ MMA issuer
     pdl_wait();
     // W8A8: a tile whose bounds fit one exact chunk issues its k-blocks without any bound
-    // arithmetic (the common case: chunk sizes are computed per block only otherwise)
-    bool one_chunk = true;
-    if constexpr (F == kW8) one_chunk = one_exact_chunk(kb, kw, nkb, lane);
+    // arithmetic (the common case: chunk sizes are computed per block only otherwise).  No
+    // chunk can end before k-block kChunkMin - 1, so the first blocks go out at once, and the
+    // decision, which the drain warps take from the tile's block bounds meanwhile, is read
+    // there.  The one-chunk path is a loop of its own with no bound bookkeeping in it: summing
+    // the bounds up front delayed every tile's first MMA, and the bookkeeping inside the one
+    // issue loop slowed every k-block (each cost about 8% of the kernel).
     if (lane == 0) {
-      int bound = 0, chunk = 0;  // W8A8: running bound of the current exact chunk, its index
-      int bnext = 0;             // W8A8: the next block's bound, read one k-block ahead
-      if constexpr (F == kW8) bnext = one_chunk ? 0 : block_bound(kb[0], kw[0]);
-      for (int i = 0; i < nkb && ok; ++i) {
+      // one k-block: wait for its operands, issue its MMAs, release the stage; chunk_end
+      // (W8A8) also hands the accumulators to the drain
+      auto issue = [&](int i, bool chunk_end) -> bool {
         const int s = i % NST;
-        const uint32_t ph = (uint32_t)(i / NST) & 1u;
-        uint32_t dcol = 0;
-        bool first = (i == 0);
-        bool chunk_end = false;
+        if (!mbar_wait_scope<CL>(&sm.ab_full[s], (uint32_t)(i / NST) & 1u, a.status)) return false;
+        tc_fence_after();
+        const bool first = i == 0;
+        const uint64_t dw = umma_desc_sw128(sm.b[s]);  // weights, 128 rows
+        if constexpr (C::kATmem) {
+          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
+          const uint32_t ta = tmem + kACol + 32u * (uint32_t)s;  // weights, 128 lanes x 32 columns
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16_ta(tmem, ta + 8u * kk, dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        } else if constexpr (kRowsInLanes) {
+          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16(tmem, dw + (uint64_t)(2 * kk), dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
+        } else {
+#pragma unroll
+          for (int mh = 0; mh < MH; ++mh) {
+            const uint64_t dx = umma_desc_sw128(sm.a[s] + mh * kTileBytes);  // X, 128 tokens
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_f16(tmem + 128u * mh, dx + (uint64_t)(2 * kk), dw + (uint64_t)(2 * kk), idesc,
+                       (first && kk == 0) ? 0u : 1u);
+          }
+        }
+        if constexpr (CL)
+          umma_commit_pair(&sm.ab_empty[i % NEB]);  // the partner's converters write this stage too
+        else
+          umma_commit(&sm.ab_empty[i % NEB]);
         if constexpr (F == kW8) {
-          chunk_end = i == nkb - 1;
-          if (!one_chunk) {
-            // one fp32 accumulator: chunk c starts once the drain has split chunk c - 1's
-            // accumulators and written back their low parts, and continues from them
+          if (chunk_end) umma_commit(&sm.ch_full[0]);
+        }
+        return true;
+      };
+      int i = 0;
+      if constexpr (F != kW8) {
+        for (; i < nkb && ok; ++i) ok = issue(i, false);
+      } else {
+        const int n0 = nkb < kChunkMin - 1 ? nkb : kChunkMin - 1;
+        for (; i < n0 && ok; ++i) ok = issue(i, i == nkb - 1);
+        bool one_chunk = true;
+        if (ok && i < nkb) {
+          ok = mbar_wait(&sm.plan_full, 0u, a.status);
+          one_chunk = sm.plan_one != 0;
+        }
+        if (one_chunk) {
+          for (; i < nkb && ok; ++i) ok = issue(i, i == nkb - 1);
+        } else {
+          // one fp32 accumulator: chunk c starts once the drain has split chunk c - 1's
+          // accumulators and written back their low parts, and continues from them.  Catch up
+          // on the bounds of the blocks issued so far (i > 0 from here on).
+          int bound = 0, chunk = 0;  // running bound of the current exact chunk, its index
+          for (int b = 0; b < i; ++b) bound += block_bound(kb[b], kw[b]);
+          int bnext = block_bound(kb[i], kw[i]);  // the next block's bound, read one k-block ahead
+          for (; i < nkb && ok; ++i) {
             const int bi = bnext;
             bnext = i + 1 < nkb ? block_bound(kb[i + 1], kw[i + 1]) : 0;
-            if (i > 0 && bound + bi > kExactSum) {
+            if (bound + bi > kExactSum) {
               ++chunk;
               if (!mbar_wait(&sm.ch_empty[0], (uint32_t)(chunk - 1) & 1u, a.status)) {
                 ok = false;
@@ -805,42 +854,8 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
             } else {
               bound += bi;
             }
-            chunk_end = i == nkb - 1 || bound + bnext > kExactSum;
+            ok = issue(i, i == nkb - 1 || bound + bnext > kExactSum);
           }
-        }
-        if (!mbar_wait_scope<CL>(&sm.ab_full[s], ph, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t dw = umma_desc_sw128(sm.b[s]);  // weights, 128 rows
-        if constexpr (C::kATmem) {
-          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
-          const uint32_t ta = tmem + kACol + 32u * (uint32_t)s;  // weights, 128 lanes x 32 columns
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16_ta(tmem + dcol, ta + 8u * kk, dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
-        } else if constexpr (kRowsInLanes) {
-          const uint64_t dx = umma_desc_sw128(sm.a[s]);  // X, 256 tokens
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16(tmem + dcol, dw + (uint64_t)(2 * kk), dx + (uint64_t)(2 * kk), idesc, (first && kk == 0) ? 0u : 1u);
-        } else {
-#pragma unroll
-          for (int mh = 0; mh < MH; ++mh) {
-            const uint64_t dx = umma_desc_sw128(sm.a[s] + mh * kTileBytes);  // X, 128 tokens
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_f16(tmem + dcol + 128u * mh, dx + (uint64_t)(2 * kk), dw + (uint64_t)(2 * kk), idesc,
-                       (first && kk == 0) ? 0u : 1u);
-          }
-        }
-        if constexpr (CL)
-          umma_commit_pair(&sm.ab_empty[i % NEB]);  // the partner's converters write this stage too
-        else
-          umma_commit(&sm.ab_empty[i % NEB]);
-        if constexpr (F == kW8) {
-          if (chunk_end) umma_commit(&sm.ch_full[0]);
         }
       }
       umma_commit(&sm.acc_full);
@@ -982,7 +997,27 @@ __global__ void __launch_bounds__(tc_threads<F>(), 1) tc_gemm_kernel(const __gri
     const int n = n_tile * kBN + 32 * q + lane;  // this lane's weight row
     const float swn = n < a.N ? a.sw[n] : 0.f;
     int nchunks = 1;  // the MMA issuer's chunking, replayed
-    const bool one_chunk = one_exact_chunk(kb, kw, nkb, lane);
+    // whether the tile's blocks fit one exact chunk: the sum of all block bounds, the 256 drain
+    // threads taking every 256th block, so the MMA issuer finds the answer ready at k-block
+    // kChunkMin - 1 (one lane walking every 32nd block took longer than those 15 blocks)
+    {
+      long long part = 0;
+#if QLIN_W8_PLAN_PAR
+      for (int j = (warp - 2 - NCONV) * 32 + lane; j < nkb; j += 256) part += block_bound(kb[j], kw[j]);
+#else
+      if (warp == 2 + NCONV)
+        for (int j = lane; j < nkb; j += 32) part += block_bound(kb[j], kw[j]);
+#endif
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0 && part) atomicAdd(&sm.plan_sum, (unsigned long long)part);
+      named_bar_sync(1, 256);  // the eight drain warps
+    }
+    const bool one_chunk = sm.plan_sum <= (unsigned long long)kExactSum;
+    if (warp == 2 + NCONV && lane == 0) {  // the MMA issuer reads it at k-block kChunkMin - 1
+      sm.plan_one = one_chunk ? 1 : 0;
+      mbar_arrive(&sm.plan_full);
+    }
     for (int i = 0, bound = 0; i < nkb && !one_chunk; ++i) {
       const int bi = block_bound(kb[i], kw[i]);
       if (i > 0 && bound + bi > kExactSum) {
