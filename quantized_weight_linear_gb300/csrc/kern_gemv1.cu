@@ -18,8 +18,11 @@
 //   a CTA of this one leaves its SM.  (Measured alternatives: one CTA of four groups, and one
 //   co-resident CTA of two groups per forward, were as fast or slower.);
 // * the token's activations are copied into shared memory once per CTA (the K units its
-//   range touches, after griddepcontrol.wait) and the sums of x that the formulation needs
-//   are prepared once per CTA, so a unit costs only its weight bytes;
+//   range touches, by a thread of their own right after griddepcontrol.wait, so the copy
+//   never waits behind the weight stream's set-up) and the sums of x that the formulation
+//   needs are prepared once per CTA, so a unit costs only its weight bytes.  The CTAs that
+//   become resident only as the previous forward leaves set the forward's end: for them this
+//   prologue is on the critical path;
 // * integer-exact MMA formulation: the A operand is bf16(base + q) made from the code bits
 //   with one AND/OR per register pair, (base + q) x accumulates in fp32, and the base and
 //   zero-point terms come off once per (row, group) through the prepared sums of x.  A
@@ -464,6 +467,31 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     mbar_init(&h.offs_bar, 1);
     fence_mbar_init();
     pdl_launch_dependents();
+    // Weights never depend on the previous kernel: the CTA's bucket offsets and each group's
+    // first ring units go out now, before the plan is shared (the same unit ranges as the
+    // plan's).  A CTA that becomes resident only when the previous forward's CTAs leave its SM
+    // has its first units' outliers on the critical path, behind the offsets' round trip:
+    // issuing that here took the 11008 x 4096 forward from 10.3 to 9.6 us.  (W4, with no such
+    // round trip, is faster with its producers issuing after the plan.)
+    int64_t ub[kG1Groups + 1];
+    const int64_t W = (int64_t)gridDim.x * kG1Groups, c0 = (int64_t)blockIdx.x * kG1Groups;
+#pragma unroll
+    for (int q = 0; q <= kG1Groups; ++q) ub[q] = g1_div((c0 + q) * U, W);
+    if (ub[kG1Groups] > ub[0]) {
+      const int64_t ob = 4 * ub[0], oe = 4 * ub[kG1Groups] + 4;
+      mbar_arrive_expect_tx(&h.offs_bar, (uint32_t)(oe - ob) * 4u);
+      bulk_g2s(offs_s, v.offs + ob, (uint32_t)(oe - ob) * 4u, &h.offs_bar);
+      const uint64_t pol = policy_evict_first();
+#pragma unroll
+      for (int q = 0; q < kG1Groups; ++q) {
+        const int n = (int)(ub[q + 1] - ub[q]);
+        for (int i = 0; i < (n < STAGES ? n : STAGES); ++i) {  // completed by the outliers' arrival
+          mbar_expect_tx(&h.full[q][i], kSpqrUnitBytes);
+          bulk_g2s_ef(sb + L.ring + (uint32_t)(q * STAGES + i) * L.stage_bytes,
+                      v.units + (ub[q] + i) * (int64_t)kSpqrUnitBytes, kSpqrUnitBytes, &h.full[q][i], pol);
+        }
+      }
+    }
   }
   if (threadIdx.x >= 64 && threadIdx.x < 80) h.zeros[threadIdx.x - 64] = 0u;
   if (warp < kG1Consumers) {
@@ -482,15 +510,22 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   if (warp >= kG1Consumers) {
     // ------------------------------------------- producers: one thread per group, own ring
     const int q = warp - kG1Consumers;
+    if (q == 0 && lane == 1) {
+      // x, as soon as the previous kernel is done (apart from the weight stream, which may
+      // still wait for its bucket offsets)
+      pdl_wait();  // x is written by the previous kernel on the stream
+      const int xn = h.xn;
+      const int64_t ks = u0c % S;
+      const int na = (int)((int64_t)xn < S - ks ? (int64_t)xn : S - ks);
+      mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kSpqrSuper * 2));
+      bulk_g2s(xs, X + ks * kSpqrSuper, (uint32_t)na * (kSpqrSuper * 2), &h.x_bar);
+      if (xn > na) bulk_g2s(xs + (size_t)na * kSpqrSuper, X, (uint32_t)(xn - na) * (kSpqrSuper * 2), &h.x_bar);
+      return;
+    }
     if (lane != 0) return;
     const int64_t a = h.u0[q];
     const int n = (int)(h.u0[q + 1] - a);
     const uint64_t pol = policy_evict_first();
-    if (q == 0) {  // the CTA's bucket offsets [4 u0c, 4 u1c], rounded up to 16 bytes
-      const int64_t ob = 4 * u0c, oe = 4 * u1c + 4;
-      mbar_arrive_expect_tx(&h.offs_bar, (uint32_t)(oe - ob) * 4u);
-      bulk_g2s(offs_s, v.offs + ob, (uint32_t)(oe - ob) * 4u, &h.offs_bar);
-    }
     auto stage_at = [&](int s) { return sb + L.ring + (uint32_t)(q * STAGES + s) * L.stage_bytes; };
     auto unit_src = [&](int i) { return v.units + (a + i) * (int64_t)kSpqrUnitBytes; };
     // outlier entries of unit a + i staged with it (16-byte aligned range), or none
@@ -507,12 +542,9 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
       const uint32_t e0 = offs_s[4 * (int)(a + i0 - u0c)] & ~3u, e1 = (offs_s[4 * (int)(a + i1 - u0c)] + 3u) & ~3u;
       if (e1 > e0) prefetch_l2(v.ents + e0, (uint64_t)(e1 - e0) * 4u);
     };
-    // the ring's first units go out at once; their outliers follow once the offsets are in
+    // the ring's first units went out with the barrier set-up; their outliers follow once the
+    // offsets are in
     const int pro = n < STAGES ? n : STAGES;
-    for (int i = 0; i < pro; ++i) {
-      mbar_expect_tx(&h.full[q][i], kSpqrUnitBytes);
-      bulk_g2s_ef(stage_at(i), unit_src(i), kSpqrUnitBytes, &h.full[q][i], pol);
-    }
     if (!mbar_wait(&h.offs_bar, 0, ws.status)) return;
     for (int i = 0; i < pro; ++i) {
       uint32_t a0, a1;
@@ -522,15 +554,6 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     }
     int pf = pro + kG1SpPrefetch < n ? pro + kG1SpPrefetch : n;  // end of the prefetched window
     prefetch(pro, pf);
-    pdl_wait();  // x is written by the previous kernel on the stream
-    if (q == 0) {
-      const int xn = h.xn;
-      const int64_t ks = u0c % S;
-      const int na = (int)((int64_t)xn < S - ks ? (int64_t)xn : S - ks);
-      mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kSpqrSuper * 2));
-      bulk_g2s(xs, X + ks * kSpqrSuper, (uint32_t)na * (kSpqrSuper * 2), &h.x_bar);
-      if (xn > na) bulk_g2s(xs + (size_t)na * kSpqrSuper, X, (uint32_t)(xn - na) * (kSpqrSuper * 2), &h.x_bar);
-    }
     int s = 0;
     uint32_t ph = 1u;  // the ring's first pass is done: waiting for the consumers' first release
     for (int i = pro; i < n; ++i) {
@@ -836,6 +859,21 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   if (warp >= kG1Consumers) {
     // ------------------------------------------- producers: one thread per group, own ring
     const int q = warp - kG1Consumers;
+    if (q == 0 && lane == 1) {  // x, as soon as the previous kernel is done
+      pdl_wait();  // x is written by the previous kernel on the stream
+      if (ACT) {  // act-order: the whole row; the consumers gather from it
+        mbar_arrive_expect_tx(&h.x_bar, (uint32_t)G * (kW4Group * 2));
+        bulk_g2s(sb + L.xfull, X, (uint32_t)G * (kW4Group * 2), &h.x_bar);
+      } else {
+        const int xn = h.xn;
+        const int64_t ks = u0c % G;
+        const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
+        mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kW4Group * 2));
+        bulk_g2s(xs, X + ks * kW4Group, (uint32_t)na * (kW4Group * 2), &h.x_bar);
+        if (xn > na) bulk_g2s(xs + (size_t)na * kW4Group, X, (uint32_t)(xn - na) * (kW4Group * 2), &h.x_bar);
+      }
+      return;
+    }
     if (lane != 0) return;
     const int64_t a = h.u0[q];
     const int n = (int)(h.u0[q + 1] - a);
@@ -843,24 +881,12 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     auto stage_at = [&](int s) { return sb + L.ring + (uint32_t)(q * STAGES + s) * L.stage_bytes; };
     auto unit_src = [&](int i) { return v.units + (a + i) * (int64_t)kW4UnitBytes; };
     const int pro = n < STAGES ? n : STAGES;
+    int pf = pro + kG1W4Prefetch < n ? pro + kG1W4Prefetch : n;  // end of the prefetched window
     for (int i = 0; i < pro; ++i) {
       mbar_arrive_expect_tx(&h.full[q][i], kW4UnitBytes);
       bulk_g2s_ef(stage_at(i), unit_src(i), kW4UnitBytes, &h.full[q][i], pol);
     }
-    int pf = pro + kG1W4Prefetch < n ? pro + kG1W4Prefetch : n;  // end of the prefetched window
     if (pf > pro) prefetch_l2(unit_src(pro), (uint64_t)(pf - pro) * kW4UnitBytes);
-    pdl_wait();  // x is written by the previous kernel on the stream
-    if (ACT && q == 0) {  // act-order: the whole row; the consumers gather from it
-      mbar_arrive_expect_tx(&h.x_bar, (uint32_t)G * (kW4Group * 2));
-      bulk_g2s(sb + L.xfull, X, (uint32_t)G * (kW4Group * 2), &h.x_bar);
-    } else if (q == 0) {
-      const int xn = h.xn;
-      const int64_t ks = u0c % G;
-      const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
-      mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kW4Group * 2));
-      bulk_g2s(xs, X + ks * kW4Group, (uint32_t)na * (kW4Group * 2), &h.x_bar);
-      if (xn > na) bulk_g2s(xs + (size_t)na * kW4Group, X, (uint32_t)(xn - na) * (kW4Group * 2), &h.x_bar);
-    }
     int s = 0;
     uint32_t ph = 1u;  // the ring's first pass is done: waiting for the consumers' first release
     for (int i = pro; i < n; ++i) {
