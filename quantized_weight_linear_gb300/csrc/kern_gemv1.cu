@@ -1045,8 +1045,17 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   fin.finish(cs, threadIdx.x - grp * 128, done);
 }
 
+// Layers below this many packed bytes get one CTA per SM instead of kG1CtasPerSm: the ring
+// depth still leaves room for a second CTA, so the next forward's CTAs are all resident (and
+// past their prologue) when this one ends, and for a small layer that start-up is a large
+// part of the forward.  Measured, us per forward (one CTA per SM / two): W4 2048 x 4096
+// 3.65 / 3.98, W4 4096^2 4.86 / 4.98 and act-order 5.41 / 6.72, SpQR 4096^2 5.58 / 6.00;
+// above it W4 4096 x 5120 (11.1 MB) 5.54 / 5.09, SpQR 4096 x 6144 6.88 / 7.09 the other way.
+constexpr int64_t kG1SmallBytes = 10ll << 20;
 int g1_grid(int64_t U, int sms, bool spqr) {
-  int64_t grid = std::min<int64_t>((int64_t)kG1CtasPerSm * sms, (U + kG1Groups - 1) / kG1Groups);
+  const int64_t bytes = U * (spqr ? kSpqrUnitBytes : kW4UnitBytes);
+  const int64_t cps = bytes < kG1SmallBytes ? 1 : kG1CtasPerSm;
+  int64_t grid = std::min<int64_t>(cps * sms, (U + kG1Groups - 1) / kG1Groups);
   if (spqr) grid = std::max<int64_t>(grid, (U + kG1MaxUnitsPerCta - 1) / kG1MaxUnitsPerCta);
   return (int)std::max<int64_t>(1, std::min<int64_t>(grid, 1 << 30));
 }
