@@ -80,6 +80,7 @@ struct G1Hdr {
   uint64_t all_bar;             // every consumer thread
   uint64_t x_bar;               // the staged activations (transaction count)
   uint64_t offs_bar;            // the staged bucket offsets (SpQR)
+  uint64_t perm_bar;            // the staged permutation entries (W4 act-order)
   int64_t u0[kG1Groups + 1];    // unit ranges: group g owns [u0[g], u0[g + 1])
   int64_t rg0[kG1Groups];       // row group of each group's first unit
   int k0[kG1Groups];            // K unit (within the row) of each group's first unit
@@ -106,6 +107,7 @@ struct G1Layout {
   uint32_t xf;           // W4: staged x in B-fragment order
   uint32_t bytes;        // total
   uint32_t xfull;        // W4 act-order: the whole x row (input channel order)
+  uint32_t perm;         // W4 act-order: the permutation entries of the staged K units
 };
 
 namespace {
@@ -136,6 +138,8 @@ G1Layout g1_layout(bool spqr, int xn, int stages, int xfull_k = 0) {
     o = al128(o + (uint32_t)xn * kW4Group * 2);
     L.xfull = o;  // act-order: the whole token, in input channel order
     o = al128(o + (uint32_t)xfull_k * 2);
+    L.perm = o;
+    o = al128(o + (xfull_k ? (uint32_t)xn * kW4Group * 4 : 0u));
   }
   L.bytes = o;
   return L;
@@ -849,8 +853,26 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     }
     mbar_init(&h.all_bar, 32 * kG1Consumers);
     mbar_init(&h.x_bar, 1);
+    mbar_init(&h.perm_bar, 1);
     fence_mbar_init();
     pdl_launch_dependents();
+    if constexpr (ACT) {
+      // act-order: the permutation entries of the K units this CTA stages (part of the
+      // weights, so they go out now, with the plan's unit range computed here): read from
+      // global memory by the gather itself they sat on the critical path of the CTAs that
+      // start last (and took 32 registers)
+      const int64_t W = (int64_t)gridDim.x * kG1Groups, c0 = (int64_t)blockIdx.x * kG1Groups;
+      const int64_t a = g1_div(c0 * U, W), n = g1_div((c0 + kG1Groups) * U, W) - a;
+      if (n > 0) {
+        const int xn = (int)(n < G ? n : G);
+        const int64_t ks = a % G;
+        const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
+        int32_t* ps = reinterpret_cast<int32_t*>(sb + L.perm);
+        mbar_arrive_expect_tx(&h.perm_bar, (uint32_t)xn * (kW4Group * 4));
+        bulk_g2s(ps, v.perm + ks * kW4Group, (uint32_t)na * (kW4Group * 4), &h.perm_bar);
+        if (xn > na) bulk_g2s(ps + (size_t)na * kW4Group, v.perm, (uint32_t)(xn - na) * (kW4Group * 4), &h.perm_bar);
+      }
+    }
   }
   __syncthreads();
   const int64_t u0c = h.u0[0], u1c = h.u0[kG1Groups];
@@ -909,27 +931,15 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   const int grp = warp >> 2, rt = warp & 3;
   if constexpr (ACT) {
     // act-order: staged element j (K group (ks + j / 128) mod G, column j mod 128) is
-    // x[perm[k]], gathered in shared memory from the whole row.  The permutation is part of
-    // the weights, so this thread's entries are read (coalesced) before the wait for the
-    // previous kernel.
-    static_assert(kG1GatherMaxK <= 8192, "a consumer thread gathers at most 32 elements");
-    constexpr int kPer = 8192 / (32 * kG1Consumers);
+    // x[perm[k]], gathered in shared memory from the whole row with the permutation entries
+    // staged beside it
     const int nj = h.xn * kW4Group;
-    const int64_t ks = u0c % G;
-    int32_t pk[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int j = threadIdx.x + e * 32 * kG1Consumers;
-      pk[e] = j < nj ? __ldg(v.perm + ((ks + j / kW4Group) % G) * kW4Group + j % kW4Group) : 0;
-    }
     pdl_wait();
-    const bool got = g1_wait(&h.x_bar, 0, ws.status);
+    const bool got = g1_wait(&h.x_bar, 0, ws.status) && g1_wait(&h.perm_bar, 0, ws.status);
     const uint16_t* xrow = reinterpret_cast<const uint16_t*>(sb + L.xfull);
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int j = threadIdx.x + e * 32 * kG1Consumers;
-      if (j < nj) xs[j] = xrow[pk[e]];
-    }
+    const int32_t* ps = reinterpret_cast<const int32_t*>(sb + L.perm);
+    if (got)
+      for (int j = threadIdx.x; j < nj; j += 32 * kG1Consumers) xs[j] = xrow[ps[j]];
     named_bar_sync(1, 32 * kG1Consumers);  // every consumer thread, no early exit before it
     if (!got) return;
   } else {
