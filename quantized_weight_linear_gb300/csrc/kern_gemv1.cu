@@ -97,6 +97,12 @@ struct G1Hdr {
 }  // namespace
 
 // Section offsets of the dynamic shared memory (from the 128-byte aligned base)
+// floor(n / d) by a multiply with a precomputed inverse of d, for every 32-bit n (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994, Figure 4.1)
+struct G1Div {
+  uint32_t m, s1, s2;
+};
+
 struct G1Layout {
   uint32_t ring;         // [groups][stages] stages of stage_bytes
   uint32_t stage_bytes;
@@ -108,6 +114,7 @@ struct G1Layout {
   uint32_t bytes;        // total
   uint32_t xfull;        // W4 act-order: the whole x row (input channel order)
   uint32_t perm;         // W4 act-order: the permutation entries of the staged K units
+  G1Div dW, dU, dR;      // inverses of the worker count, the unit count and the units per row group
 };
 
 namespace {
@@ -145,26 +152,36 @@ G1Layout g1_layout(bool spqr, int xn, int stages, int xfull_k = 0) {
   return L;
 }
 
-// Division of non-negative values; 32-bit when both fit (every realistic layer), which is
-// far cheaper than the 64-bit routine
-__device__ __forceinline__ int64_t g1_div(int64_t a, int64_t b) {
-  if (((uint64_t)a | (uint64_t)b) >> 32) return a / b;
-  return (int64_t)((uint32_t)a / (uint32_t)b);
+G1Div g1_div_make(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (uint64_t(1) << l) < d) ++l;  // ceil(log2 d)
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return {(uint32_t)m, l < 1 ? l : 1u, l > 1 ? l - 1 : 0u};
+}
+
+// floor(a / b) of non-negative a and b, v the inverse of b: a high multiply and two shifts
+// when a fits 32 bits (every realistic layer).  The plan's chains of divisions are on the
+// critical path of every CTA that starts late; done by the division routine they took about
+// a microsecond.
+__device__ __forceinline__ int64_t g1_div(int64_t a, int64_t b, const G1Div& v) {
+  if ((uint64_t)a >> 32) return a / b;
+  const uint32_t n = (uint32_t)a, t1 = __umulhi(n, v.m);
+  return (int64_t)((t1 + ((n - t1) >> v.s1)) >> v.s2);
 }
 
 // Work plan of a CTA, computed by warp 0: its workers' unit ranges, where their ranges
 // share row groups with other workers, and the K units of x the CTA needs.  Worker w owns
 // units [w U / W, (w + 1) U / W); the owner of unit u is ((u + 1) W - 1) / U.
-__device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane) {
+__device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane, const G1Layout& L) {
   const int64_t W = (int64_t)gridDim.x * kG1Groups, c0 = (int64_t)blockIdx.x * kG1Groups;
-  if (lane <= kG1Groups) h.u0[lane] = g1_div((c0 + lane) * U, W);
+  if (lane <= kG1Groups) h.u0[lane] = g1_div((c0 + lane) * U, W, L.dW);
   __syncwarp();
   const int64_t u0c = h.u0[0];
   if (lane < kG1Groups) {
-    const int64_t u0 = h.u0[lane], rg0 = g1_div(u0, per_rg), d = u0 - u0c;
+    const int64_t u0 = h.u0[lane], rg0 = g1_div(u0, per_rg, L.dR), d = u0 - u0c;
     h.rg0[lane] = rg0;
     h.k0[lane] = (int)(u0 - rg0 * per_rg);
-    h.ls0[lane] = (int)(d - g1_div(d, per_rg) * per_rg);
+    h.ls0[lane] = (int)(d - g1_div(d, per_rg, L.dR) * per_rg);
     h.owned[lane] = -1;
     h.others[lane] = 0;
   }
@@ -178,10 +195,10 @@ __device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane) {
     const int64_t w = c0 + g, u0 = h.u0[g], u1 = h.u0[g + 1];
     int out = -1;
     if (u1 > u0) {
-      const int64_t r = g1_div(s == 0 ? u0 : u1 - 1, per_rg);
+      const int64_t r = g1_div(s == 0 ? u0 : u1 - 1, per_rg, L.dR);
       if (!(s == 1 && r == h.rg0[g])) {
-        const int64_t first = g1_div((r * per_rg + 1) * W - 1, U);
-        const int64_t last = g1_div((r * per_rg + per_rg) * W - 1, U);
+        const int64_t first = g1_div((r * per_rg + 1) * W - 1, U, L.dU);
+        const int64_t last = g1_div((r * per_rg + per_rg) * W - 1, U, L.dU);
         if (first != last) {
           out = (int)r;
           if (first == w) {  // at most one side: a range starting at its row group's first unit
@@ -193,9 +210,9 @@ __device__ void g1_plan_warp(G1Hdr& h, int64_t U, int64_t per_rg, int lane) {
     } else if (s == 0 && u0 < U) {
       // an empty range (more workers than units) that sits inside a shared row group still
       // counts among its contributors: it contributes zeros
-      const int64_t r = g1_div(u0, per_rg);
-      const int64_t first = g1_div((r * per_rg + 1) * W - 1, U);
-      const int64_t last = g1_div((r * per_rg + per_rg) * W - 1, U);
+      const int64_t r = g1_div(u0, per_rg, L.dR);
+      const int64_t first = g1_div((r * per_rg + 1) * W - 1, U, L.dU);
+      const int64_t last = g1_div((r * per_rg + per_rg) * W - 1, U, L.dU);
       if (first < w && w <= last) out = (int)r;
     }
     h.rg[g][s] = out;
@@ -456,7 +473,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   uint16_t* xs = reinterpret_cast<uint16_t*>(sb + L.xs);
   const int g = lane >> 2, t = lane & 3;
 
-  if (warp == 0) g1_plan_warp(h, U, S, lane);
+  if (warp == 0) g1_plan_warp(h, U, S, lane, L);
   if (threadIdx.x == 32) {
 #pragma unroll
     for (int q = 0; q < kG1Groups; ++q) {
@@ -480,7 +497,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
     int64_t ub[kG1Groups + 1];
     const int64_t W = (int64_t)gridDim.x * kG1Groups, c0 = (int64_t)blockIdx.x * kG1Groups;
 #pragma unroll
-    for (int q = 0; q <= kG1Groups; ++q) ub[q] = g1_div((c0 + q) * U, W);
+    for (int q = 0; q <= kG1Groups; ++q) ub[q] = g1_div((c0 + q) * U, W, L.dW);
     if (ub[kG1Groups] > ub[0]) {
       const int64_t ob = 4 * ub[0], oe = 4 * ub[kG1Groups] + 4;
       mbar_arrive_expect_tx(&h.offs_bar, (uint32_t)(oe - ob) * 4u);
@@ -519,7 +536,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
       // still wait for its bucket offsets)
       pdl_wait();  // x is written by the previous kernel on the stream
       const int xn = h.xn;
-      const int64_t ks = u0c % S;
+      const int64_t ks = u0c - g1_div(u0c, S, L.dR) * S;
       const int na = (int)((int64_t)xn < S - ks ? (int64_t)xn : S - ks);
       mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kSpqrSuper * 2));
       bulk_g2s(xs, X + ks * kSpqrSuper, (uint32_t)na * (kSpqrSuper * 2), &h.x_bar);
@@ -841,7 +858,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
   uint32_t* xf = reinterpret_cast<uint32_t*>(sb + L.xf);
   const int g = lane >> 2, t = lane & 3;
 
-  if (warp == 0) g1_plan_warp(h, U, G, lane);
+  if (warp == 0) g1_plan_warp(h, U, G, lane, L);
   if (threadIdx.x == 32) {
 #pragma unroll
     for (int q = 0; q < kG1Groups; ++q) {
@@ -862,10 +879,10 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
       // global memory by the gather itself they sat on the critical path of the CTAs that
       // start last (and took 32 registers)
       const int64_t W = (int64_t)gridDim.x * kG1Groups, c0 = (int64_t)blockIdx.x * kG1Groups;
-      const int64_t a = g1_div(c0 * U, W), n = g1_div((c0 + kG1Groups) * U, W) - a;
+      const int64_t a = g1_div(c0 * U, W, L.dW), n = g1_div((c0 + kG1Groups) * U, W, L.dW) - a;
       if (n > 0) {
         const int xn = (int)(n < G ? n : G);
-        const int64_t ks = a % G;
+        const int64_t ks = a - g1_div(a, G, L.dR) * G;
         const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
         int32_t* ps = reinterpret_cast<int32_t*>(sb + L.perm);
         mbar_arrive_expect_tx(&h.perm_bar, (uint32_t)xn * (kW4Group * 4));
@@ -888,7 +905,7 @@ __global__ void __launch_bounds__(kG1Threads, kG1CtasPerSm)
         bulk_g2s(sb + L.xfull, X, (uint32_t)G * (kW4Group * 2), &h.x_bar);
       } else {
         const int xn = h.xn;
-        const int64_t ks = u0c % G;
+        const int64_t ks = u0c - g1_div(u0c, G, L.dR) * G;
         const int na = (int)((int64_t)xn < G - ks ? (int64_t)xn : G - ks);
         mbar_arrive_expect_tx(&h.x_bar, (uint32_t)xn * (kW4Group * 2));
         bulk_g2s(xs, X + ks * kW4Group, (uint32_t)na * (kW4Group * 2), &h.x_bar);
@@ -1098,6 +1115,10 @@ int g1_launch(KDeep* kdeep, KShallow* kshallow, int deep, std::atomic<uint64_t>*
     stages = deep - 1;
     L = g1_layout(spqr, xn, stages, xfull_k);
   }
+  if (U >= (int64_t(1) << 32) || per_rg >= (int64_t(1) << 32)) return (int)cudaErrorInvalidValue;
+  L.dW = g1_div_make((uint32_t)grid * kG1Groups);
+  L.dU = g1_div_make((uint32_t)U);
+  L.dR = g1_div_make((uint32_t)per_rg);
   const size_t smem = (size_t)L.bytes + 128;
   if (smem > kG1MaxSmem) return (int)cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
