@@ -320,7 +320,13 @@ int launch_w4_gather(const uint16_t* X, const int32_t* perm, uint16_t* Xp, int M
 int launch_w4_decode(const W4View& v, const uint16_t* X, uint16_t* Y, int M, const Workspace& ws, int grid,
                      void* stream) {
   if (M == 1) return launch_w4_gemv1(v, X, Y, ws, stream);
-  const int cps = M <= 8 ? 4 : QLIN_W4_CPS16;  // CTAs per SM the launch bounds allow
+  // CTAs per SM: up to eight tokens the launch bounds allow four, but a layer under 64 MB of
+  // packed weights runs faster with two (fewer CTAs share each split row group, and a CTA's
+  // fixed start and finish weigh less).  Same box, us per forward (4 / 2 CTAs per SM): 4096^2
+  // M = 2 7.27 / 5.64, M = 4 7.05 / 5.46, M = 8 7.48 / 7.25; 4096 x 11008 M = 4 9.68 / 9.43;
+  // 8192^2 M = 4 13.06 / 12.76; 8192 x 28672 (125 MB) M = 4 36.0 / 38.4 the other way.
+  const bool small = (int64_t)v.RG * v.G * kW4UnitBytes < (int64_t(64) << 20);
+  const int cps = M <= 8 ? (small ? 2 : 4) : QLIN_W4_CPS16;
   grid = (int)std::min<int64_t>((int64_t)v.RG * v.G, (int64_t)std::min(cps, QLIN_DECODE_CPS_MAX) * ws.sms);
   if (M <= 4) return launch_w4_mt<1, 4>(v, X, Y, M, ws, grid, stream);
   if (M <= 8) return launch_w4_mt<1, 0>(v, X, Y, M, ws, grid, stream);
