@@ -453,7 +453,11 @@ int launch_w8_act_quant_f16(const W8View& v, const uint16_t* X, uint16_t* q16, f
 int launch_w8_decode(const W8View& v, const uint16_t* q16, const float* sx, uint16_t* Y, int32_t* acc_out, int M,
                      const Workspace& ws, int grid, void* stream) {
   const int64_t U = (int64_t)v.RG * v.KB;
-  if (M <= 8) return launch_w8_mt<1>(v, q16, sx, Y, acc_out, M, ws, (int)std::min<int64_t>(U, (int64_t)std::min(4, QLIN_DECODE_CPS_MAX) * ws.sms), stream);
+  // up to eight tokens: four CTAs per SM, three for a layer under 24 MB of packed weights (same
+  // box, us per forward, four / three: 4096^2 M = 2 10.21 / 9.88, M = 4 10.70 / 10.26, M = 8
+  // 11.99 / 11.16; 8192^2 and the 70B-class layer measured the other way)
+  const int cps8 = U * kW8UnitBytes < (int64_t(24) << 20) ? 3 : 4;
+  if (M <= 8) return launch_w8_mt<1>(v, q16, sx, Y, acc_out, M, ws, (int)std::min<int64_t>(U, (int64_t)std::min(cps8, QLIN_DECODE_CPS_MAX) * ws.sms), stream);
   return launch_w8_mt<2>(v, q16, sx, Y, acc_out, M, ws, (int)std::min<int64_t>(U, (int64_t)std::min(3, QLIN_DECODE_CPS_MAX) * ws.sms), stream);
 }
 
