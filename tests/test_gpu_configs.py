@@ -107,6 +107,22 @@ def test_decode_sweep_w4(qlin, K, N):
         assert ok, (M, worst)
 
 
+def test_decode_w8a8_8192x8192_sampled(qlin):
+    """A 67 MB W8A8 layer at 1, 4 and 16 tokens (up to eight tokens layers of 24 MB and more run
+    four CTAs per SM, smaller ones three): sampled rows, outputs bit-exact."""
+    N = K = 8192
+    W, X, absmax, _ = synth.smoothquant_layer(N, K, 16, seed=2)
+    layer = qlin.QLinear.from_w8(W, absmax, 0.85).to("cuda")
+    ns = _sample(N, 160, 4)
+    s, s_inv = smoothquant.smoothing_factors(absmax, W, 0.85)
+    qw, sw = smoothquant.quantize_rows_int8(smoothquant.fold_weights(W[ns], s))
+    for M in (1, 4, 16):
+        Y = _run(layer, X[:M])
+        qx, sx = smoothquant.quantize_activations(bits_to_f32(X[:M]), s_inv)
+        y_ref = smoothquant.epilogue(smoothquant.accumulate(qx, qw), sx, sw)
+        assert np.array_equal(_rows(Y, np.arange(M), ns).view(np.uint32), y_ref.view(np.uint32)), M
+
+
 @pytest.mark.parametrize("K,N", SHAPES)
 @pytest.mark.parametrize("frac", [0.005, 0.01, 0.02])
 def test_decode_sweep_spqr(qlin, K, N, frac):
