@@ -8,8 +8,13 @@
 // * CTA tile: 128 output rows x 256 tokens (each dequantized weight tile serves 256 tokens,
 //   halving the dequantization per FLOP); K in blocks of 64.  W4 / W8A8: one MMA per k-step
 //   with the weight tile as A (M = 128) and the X tile as B (N = 256), so D has the weight
-//   rows in its TMEM lanes; SpQR: two MMAs per k-step (X halves as A, M = 128; the weight
-//   tile as B, N = 128), tokens in the lanes (each orientation measured faster for its formats);
+//   rows in its TMEM lanes; SpQR in single CTAs: two MMAs per k-step (X halves as A, M = 128;
+//   the weight tile as B, N = 128), tokens in the lanes (each orientation measured faster for
+//   its formats);
+// * SpQR with an even number of token tiles: clusters of two CTAs on consecutive token tiles of
+//   one weight tile; each converts its own 64-row group and bulk-copies the converted rows
+//   into the partner's stage over DSMEM (the tile is converted once per pair), with the weight
+//   rows in the TMEM lanes as for W4;
 // * grouped raster: consecutive CTAs take 4 token tiles of one weight tile before the next,
 //   so the CTAs of a wave share weight tiles through L2;
 // * warp 0: X producer -- X tiles through a 2-D tensor map (128B swizzle) into the operand
@@ -19,7 +24,8 @@
 // * warp 1: allocates TMEM and issues tcgen05.mma (kind::f16, bf16 or fp16 operands, fp32
 //   accumulators in TMEM) from one elected thread, committing each k-block back to its
 //   shared-memory stage;
-// * converter warps (8 for W4 and W8A8, 16 in two groups for SpQR): turn packed codes into
+// * converter warps (8 for W4 and W8A8; 16 for SpQR, in two groups on alternate k-blocks in a
+//   single CTA, in four groups on every fourth k-block in a pair): turn packed codes into
 //   the bf16 / fp16 weight operand; for W4 / SpQR they then run the epilogue
 //   (tcgen05.ld -> bf16 -> Y).  W4 and W8A8 write the operand straight into TMEM
 //   (tcgen05.st, one 32-column stage of 128 lanes x 64 k per k-block, beside the accumulator)
