@@ -13,7 +13,7 @@
 //   producer fills with cp.async.bulk while it prefetches the units after the ring into L2
 //   (the streamed copies are marked evict-first, so they do not push prefetched lines out);
 // * two CTAs per SM (sixteen consumer warps keep the issue slots busy; the work is issue
-//   bound).  Under programmatic dependent launch a CTA of the next forward issues its first
+//   bound); one for layers under 10 MB, whose start-up weighs more than their units.  Under programmatic dependent launch a CTA of the next forward issues its first
 //   weight copies and L2 prefetches (weights never depend on the previous kernel) as soon as
 //   a CTA of this one leaves its SM.  (Measured alternatives: one CTA of four groups, and one
 //   co-resident CTA of two groups per forward, were as fast or slower.);
