@@ -278,6 +278,10 @@ def _time_steps(rot, steps, warmup, dist_ctx):
         raise ValueError("capture the remainder graph with rot.capture(steps % R) first")
     for _ in range(max(1, math.ceil(warmup / R))):
         rot.graph.replay()
+    if rem:
+        # the remainder graph is warmed up too: a graph's first launch also uploads it, and
+        # with steps < R the timed region is that graph's one replay
+        rot.graph_rem.replay()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_ctx.barrier()

@@ -244,6 +244,13 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 r = __hadd2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
   __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
   __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);

@@ -25,7 +25,7 @@ namespace qlin {
 namespace {
 
 #ifndef QLIN_SP_DEC_STAGES
-#define QLIN_SP_DEC_STAGES 3
+#define QLIN_SP_DEC_STAGES 2  // two: room for the outlier-correction table at three CTAs per SM
 #endif
 constexpr int kStagesSp = QLIN_SP_DEC_STAGES;
 constexpr int kXHalfSp = 136;      // each 128-wide half of the X slice as [XR][128 + 8 pad]
@@ -41,6 +41,10 @@ struct SpSmem {
   __align__(16) uint32_t offs[kOffsCap];
   float rowacc[4][16][XR];
   float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
+  // up to eight tokens: per consumer warp, MMA step of the unit (16: two 128-wide blocks of
+  // eight) and lane, the bf16 outlier corrections of the lane's A registers (zero where there
+  // is none); a step's row of 32 lanes is contiguous, so its loads are free of bank conflicts
+  __align__(16) uint32_t otab[XR == 8 ? 4 : 1][XR == 8 ? 16 : 1][32][4];
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
   {
     uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0]);
     for (int i = threadIdx.x; i < kStagesSp * SpSmem<XR>::kXE / 2; i += blockDim.x) xz[i] = 0u;
+    uint32_t* oz = &sm.otab[0][0][0][0];
+    for (int i = threadIdx.x; i < (int)(sizeof(sm.otab) / 4); i += blockDim.x) oz[i] = 0u;
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -280,7 +286,39 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     const uint16_t* rb = sgst + (rt * 16 + g + 8) * 4;
     const float ssA = h2f_dev(ra[0]), zsA = h2f_dev(ra[1]), szA = h2f_dev(ra[2]), zzA = h2f_dev(ra[3]);
     const float ssB = h2f_dev(rb[0]), zsB = h2f_dev(rb[1]), szB = h2f_dev(rb[2]), zzB = h2f_dev(rb[3]);
+    // the unit's four bucket starts in one 16-byte load (the staged offsets start at 4 u0)
+    const uint4 o4 = *reinterpret_cast<const uint4*>(&sm.offs[4 * it]);
+    const uint32_t e0 = o4.x, e1 = offs(4 * u + 4);
+    const uint32_t b0 = rt == 0 ? o4.x : rt == 1 ? o4.y : rt == 2 ? o4.z : o4.w;
+    const uint32_t b1 = rt == 0 ? o4.y : rt == 1 ? o4.z : rt == 2 ? o4.w : e1;
+    const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
+    const uint32_t* bs = sm.out[s] + (b0 - (e0 & ~3u));  // staged bucket
+    const uint32_t* bg = v.ents + b0;               // the same bucket in global memory
+    const int n = (int)(b1 - b0);
 
+    if constexpr (MT == 1) {
+      // Up to eight tokens the outliers are folded into the dequantized A registers before
+      // the MMAs: entry i of the (unit, row tile) bucket writes its value, as bf16, into the
+      // table slot of the lane and register that hold its weight (element 2j + (k & 1) of
+      // group G = (k & 127) / 16: lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2),
+      // step 8 (k / 128) + j); every position is unique, so the 16-bit stores never collide.
+      // Each MMA step then adds its table row without a branch.  (A walk per row and token
+      // took a third of the kernel; a branch in the unrolled steps broke their scheduling;
+      // a table per 128-wide block, refilled between the blocks, gained nothing.)
+      for (int i = lane; i < n; i += 32) {
+        uint32_t e;
+        if (staged)
+          e = bs[i];
+        else
+          e = __ldg(bg + i);
+        const int kin = (int)((e >> 4) & 255u);
+        const int row = (int)(e & 15u), kb = kin & 127;
+        uint16_t* p = reinterpret_cast<uint16_t*>(
+            &sm.otab[rt][(kin >> 7) * 8 + ((kb & 15) >> 1)][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
+        p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
+      }
+      __syncwarp();
+    }
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
@@ -322,6 +360,13 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
         const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
 #pragma unroll
         for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
+        if constexpr (MT == 1) {
+          const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][8 * blk + j][lane]);
+          a[0] = bf16x2_add(a[0], d.x);
+          a[1] = bf16x2_add(a[1], d.y);
+          a[2] = bf16x2_add(a[2], d.z);
+          a[3] = bf16x2_add(a[3], d.w);
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const uint16_t* xr = &sm.x[s][(blk * XR + g + 8 * mt) * kXHalfSp];
@@ -331,22 +376,19 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
         }
       }
     }
-  
+    if constexpr (MT == 1) {  // clear this lane's table entries for the next unit
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+    }
 
     // outliers of this row tile in this unit; the bucket is sorted by row (then k), so each
     // row's outliers form one run.  M == 1: 32 entries at a time, a segmented sum over the
     // runs, the run's last lane adds it to the row (no atomics, no divergence).  M >= 2: lane
     // q <= 16 finds where row q starts by bisection and each lane walks its row's run.
-    {
-      // the unit's four bucket starts in one 16-byte load (the staged offsets start at 4 u0)
-      const uint4 o4 = *reinterpret_cast<const uint4*>(&sm.offs[4 * it]);
-      const uint32_t e0 = o4.x, e1 = offs(4 * u + 4);
-      const uint32_t b0 = rt == 0 ? o4.x : rt == 1 ? o4.y : rt == 2 ? o4.z : o4.w;
-      const uint32_t b1 = rt == 0 ? o4.y : rt == 1 ? o4.z : rt == 2 ? o4.w : e1;
-      const bool staged = (e1 - e0 <= (uint32_t)kOutCap) && e1 > e0;
-      const uint32_t* bs = sm.out[s] + (b0 - (e0 & ~3u));  // staged bucket
-      const uint32_t* bg = v.ents + b0;                     // the same bucket in global memory
-      const int n = (int)(b1 - b0);
+    // (Up to eight tokens they were folded into the A registers above.)
+    if constexpr (MT != 1) {
       // Every walk below is instantiated once per source (staged copy, global memory) behind
       // a warp-uniform branch: a select between the two would issue the global load as well.
       auto from_smem = [bs](int i) -> uint32_t { return bs[i]; };
