@@ -39,12 +39,12 @@ struct SpSmem {
   __align__(128) uint16_t x[kStagesSp][kXE];
   __align__(16) uint32_t out[kStagesSp][kOutCap + 8];
   __align__(16) uint32_t offs[kOffsCap];
-  float rowacc[4][16][XR];
   float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
-  // up to eight tokens: per consumer warp, MMA step of the unit (16: two 128-wide blocks of
-  // eight) and lane, the bf16 outlier corrections of the lane's A registers (zero where there
-  // is none); a step's row of 32 lanes is contiguous, so its loads are free of bank conflicts
-  __align__(16) uint32_t otab[XR == 8 ? 4 : 1][XR == 8 ? 16 : 1][32][4];
+  // per consumer warp, MMA step and lane, the bf16 outlier corrections of the lane's A
+  // registers (zero where there is none): all 16 steps of a unit up to eight tokens, the 8 of
+  // one 128-wide block at sixteen (its larger X stages leave room for no more); a step's row
+  // of 32 lanes is contiguous, so its loads are free of bank conflicts
+  __align__(16) uint32_t otab[4][XR == 8 ? 16 : 8][32][4];
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -198,17 +198,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
   float acc[NACC];
 #pragma unroll
   for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
-  // outlier sums.  M == 1: per row of the tile in shared memory (orow).  M >= 2: lane L owns
-  // row L % 16 of the tile in registers; with up to eight tokens the two lanes of a row take
-  // alternate outliers of the row and every token, with up to sixteen each takes every
-  // outlier of the row and eight of the tokens.
-  constexpr int OT = 8;
-  constexpr bool kSplitEntries = MT == 1;
-  const int orow = lane & 15, ohalf = lane >> 4;
-  const int otok0 = kSplitEntries ? 0 : 8 * ohalf;
-  float oacc[OT];
-#pragma unroll
-  for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
   int64_t cur_rg = u0 / S;
   UnitCursor cur{cur_rg, (int)(u0 - cur_rg * S), (int)S};
 
@@ -238,30 +227,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     else
       return RowGroupFinisher<float, NV>(S, U, grid, cta, ws.partials, ws.counters);
   }();
-  auto flush = [&](int64_t rg) {
-    __syncwarp();
-    float vals[NV];
-    if constexpr (kSplitEntries) {
-#pragma unroll
-      for (int j = 0; j < OT; ++j) oacc[j] += __shfl_xor_sync(0xffffffffu, oacc[j], 16);
-    }
-    if (!kSplitEntries || ohalf == 0) {
-#pragma unroll
-      for (int j = 0; j < OT; ++j)
-        if (otok0 + j < M) sm.rowacc[rt][orow][otok0 + j] = oacc[j];
-    }
-    __syncwarp();
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = g + ((i & 2) ? 8 : 0);
-        const int m = 2 * t + (i & 1) + 8 * mt;
-        vals[mt * 4 + i] = acc[mt * 4 + i] + (m < M ? sm.rowacc[rt][r][m] : 0.f);
-      }
-  
-    fin.stage(rg, vals, idx, done);
-  };
+  auto flush = [&](int64_t rg) { fin.stage(rg, acc, idx, done); };
 
   // the previous kernel on the stream may still read this launch's outputs or workspace
   pdl_wait();
@@ -275,8 +241,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
       flush(cur_rg);
 #pragma unroll
       for (int i = 0; i < NACC; ++i) acc[i] = 0.f;
-#pragma unroll
-      for (int j = 0; j < OT; ++j) oacc[j] = 0.f;
       cur_rg = rg;
     }
     if (!mbar_wait(&sm.full[s], ph, ws.status)) return;
@@ -296,31 +260,34 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     const uint32_t* bg = v.ents + b0;               // the same bucket in global memory
     const int n = (int)(b1 - b0);
 
-    if constexpr (MT == 1) {
-      // Up to eight tokens the outliers are folded into the dequantized A registers before
-      // the MMAs: entry i of the (unit, row tile) bucket writes its value, as bf16, into the
-      // table slot of the lane and register that hold its weight (element 2j + (k & 1) of
-      // group G = (k & 127) / 16: lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2),
-      // step 8 (k / 128) + j); every position is unique, so the 16-bit stores never collide.
-      // Each MMA step then adds its table row without a branch.  (A walk per row and token
-      // took a third of the kernel; a branch in the unrolled steps broke their scheduling;
-      // a table per 128-wide block, refilled between the blocks, gained nothing.)
-      for (int i = lane; i < n; i += 32) {
-        uint32_t e;
-        if (staged)
-          e = bs[i];
-        else
-          e = __ldg(bg + i);
-        const int kin = (int)((e >> 4) & 255u);
-        const int row = (int)(e & 15u), kb = kin & 127;
-        uint16_t* p = reinterpret_cast<uint16_t*>(
-            &sm.otab[rt][(kin >> 7) * 8 + ((kb & 15) >> 1)][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
-        p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
-      }
-      __syncwarp();
-    }
+    constexpr int TS = XR == 8 ? 16 : 8;  // MMA steps per fill of the correction table
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
+      if (blk * 8 % TS == 0) {
+        // The outliers are folded into the dequantized A registers before
+        // the MMAs: entry i of the (unit, row tile) bucket writes its value, as bf16, into the
+        // table slot of the lane and register that hold its weight (element 2j + (k & 1) of
+        // group G = (k & 127) / 16: lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2),
+        // step 8 (k / 128) + j); every position is unique, so the 16-bit stores never collide.
+        // Each MMA step then adds its table row without a branch.  (A walk per row and token
+        // took a third of the kernel; a branch in the unrolled steps broke their scheduling.)
+        // At sixteen tokens the table holds one 128-wide block and is filled before each,
+        // every fill passing over the other block's entries.
+        for (int i = lane; i < n; i += 32) {
+          uint32_t e;
+          if (staged)
+            e = bs[i];
+          else
+            e = __ldg(bg + i);
+          const int kin = (int)((e >> 4) & 255u);
+          if (TS == 8 && (kin >> 7) != blk) continue;  // the table holds one block
+          const int row = (int)(e & 15u), kb = kin & 127;
+          uint16_t* p = reinterpret_cast<uint16_t*>(
+              &sm.otab[rt][((kin >> 7) * 8 + ((kb & 15) >> 1)) % TS][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
+          p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
+        }
+        __syncwarp();
+      }
       const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
       uint32_t w[6];
       {
@@ -360,8 +327,8 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
         const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
 #pragma unroll
         for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
-        if constexpr (MT == 1) {
-          const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][8 * blk + j][lane]);
+        {
+          const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][(8 * blk + j) % TS][lane]);
           a[0] = bf16x2_add(a[0], d.x);
           a[1] = bf16x2_add(a[1], d.y);
           a[2] = bf16x2_add(a[2], d.z);
@@ -375,47 +342,14 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
           mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
         }
       }
-    }
-    if constexpr (MT == 1) {  // clear this lane's table entries for the next unit
-      __syncwarp();
+      if ((blk * 8 + 8) % TS == 0) {  // clear this lane's table entries for the next fill
+        __syncwarp();
 #pragma unroll
-      for (int q = 0; q < 16; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
+        for (int q = 0; q < TS; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
     }
 
-    // outliers of this row tile in this unit; the bucket is sorted by row (then k), so each
-    // row's outliers form one run.  M == 1: 32 entries at a time, a segmented sum over the
-    // runs, the run's last lane adds it to the row (no atomics, no divergence).  M >= 2: lane
-    // q <= 16 finds where row q starts by bisection and each lane walks its row's run.
-    // (Up to eight tokens they were folded into the A registers above.)
-    if constexpr (MT != 1) {
-      // Every walk below is instantiated once per source (staged copy, global memory) behind
-      // a warp-uniform branch: a select between the two would issue the global load as well.
-      auto from_smem = [bs](int i) -> uint32_t { return bs[i]; };
-      auto from_gmem = [bg](int i) -> uint32_t { return __ldg(bg + i); };
-      // lane q <= 16 finds the first entry whose row position (2 (row & 7) + row / 8, the
-      // bucket's order) is >= q; row r's run starts at its position's answer
-      auto pos = [](uint32_t e) { return (int)(((e & 7u) << 1) | ((e >> 3) & 1u)); };
-      const int rpos = ((orow & 7) << 1) | (orow >> 3);
-      auto rows = [&](auto ld) {
-        int lo = 0, hi = n;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (pos(ld(mid)) < lane) lo = mid + 1; else hi = mid;
-        }
-        const int beg = __shfl_sync(0xffffffffu, lo, rpos), end = __shfl_sync(0xffffffffu, lo, rpos + 1);
-        for (int p = beg + (kSplitEntries ? ohalf : 0); p < end; p += kSplitEntries ? 2 : 1) {
-          const uint32_t e = ld(p);
-          const int k = (int)((e >> 4) & 255u);
-          const float val = h2f_dev((uint16_t)(e >> 16));
-#pragma unroll
-          for (int j = 0; j < OT; ++j)
-            if (otok0 + j < M) oacc[j] += val * bf2f(sm.x[s][((k >> 7) * XR + otok0 + j) * kXHalfSp + (k & 127)]);
-        }
-      };
-      if (staged) rows(from_smem); else rows(from_gmem);
-    
-    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
