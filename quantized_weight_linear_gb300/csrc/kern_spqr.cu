@@ -7,18 +7,19 @@
 //
 // * a persistent weight stream: up to three CTAs per SM, equal contiguous ranges of
 //   (64 rows x 256-wide supergroup) units (7424 bytes of codes, 3-bit group statistics and
-//   fp16 supergroup statistics), a producer warp with cp.async.bulk into a 3-deep ring per
+//   fp16 supergroup statistics), a producer warp with cp.async.bulk into a 2-deep ring per
 //   CTA, the unit's outlier bucket and X slice staged alongside (the slice is two 2D tensor
 //   copies of all M rows, not one copy per token);
 // * code words hold five 3-bit fields per 16-bit half; one AND/OR turns a field pair into
 //   bf16 (base + q) with base 128 or 16 depending on the field;
 // * the A pairs are dequantized to bf16 s^ (q - z^) in registers and the MMA columns carry
 //   the tokens;
-// * outliers: each warp walks its row tile's bucket in the staged unit (k < 256, row < 16,
-//   fp16 value; sorted by quad (row & 7), then row, then k).  Lane L owns row L % 16, finds
-//   its run by bisection and accumulates value * x[k] in registers, so no two lanes ever add
-//   into the same sum (no atomics; the page's warning about the sparse part is about exactly
-//   this scattered accumulation).
+// * outliers: each warp scatters its row tile's bucket (k < 256, row < 16, fp16 value) into a
+//   shared-memory table with one bf16 slot per (MMA step, lane, A register, half), and every
+//   MMA step adds its row of the table to the dequantized A registers.  An outlier then costs
+//   the same at any token count, no two lanes ever write one slot (no atomics), and the steps
+//   carry no branch (the page's warning about the sparse part is about exactly this
+//   scattered accumulation and its divergence).
 #include "kern_decode_common.cuh"
 
 namespace qlin {
@@ -41,10 +42,9 @@ struct SpSmem {
   __align__(16) uint32_t offs[kOffsCap];
   float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
   // per consumer warp, MMA step and lane, the bf16 outlier corrections of the lane's A
-  // registers (zero where there is none): all 16 steps of a unit up to eight tokens, the 8 of
-  // one 128-wide block at sixteen (its larger X stages leave room for no more); a step's row
-  // of 32 lanes is contiguous, so its loads are free of bank conflicts
-  __align__(16) uint32_t otab[4][XR == 8 ? 16 : 8][32][4];
+  // registers (zero where there is none), all 16 steps of a unit; a step's row of 32 lanes is
+  // contiguous, so its loads are free of bank conflicts
+  __align__(16) uint32_t otab[4][16][32][4];
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
   uint64_t offs_bar;
@@ -260,34 +260,29 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     const uint32_t* bg = v.ents + b0;               // the same bucket in global memory
     const int n = (int)(b1 - b0);
 
-    constexpr int TS = XR == 8 ? 16 : 8;  // MMA steps per fill of the correction table
+    // The outliers are folded into the dequantized A registers before the MMAs: entry i of
+    // the (unit, row tile) bucket writes its value, as bf16, into the table slot of the lane
+    // and register that hold its weight (element 2j + (k & 1) of group G = (k & 127) / 16:
+    // lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2), step 8 (k / 128) + j);
+    // every position is unique, so the 16-bit stores never collide.  Each MMA step then adds
+    // its table row without a branch.  (A walk per row and token took a third of the kernel;
+    // a branch in the unrolled steps broke their scheduling; at sixteen tokens a table of one
+    // 128-wide block, filled before each block, was 6% slower on 70B-class layers.)
+    for (int i = lane; i < n; i += 32) {
+      uint32_t e;
+      if (staged)
+        e = bs[i];
+      else
+        e = __ldg(bg + i);
+      const int kin = (int)((e >> 4) & 255u);
+      const int row = (int)(e & 15u), kb = kin & 127;
+      uint16_t* p = reinterpret_cast<uint16_t*>(
+          &sm.otab[rt][(kin >> 7) * 8 + ((kb & 15) >> 1)][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
+      p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
+    }
+    __syncwarp();
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-      if (blk * 8 % TS == 0) {
-        // The outliers are folded into the dequantized A registers before
-        // the MMAs: entry i of the (unit, row tile) bucket writes its value, as bf16, into the
-        // table slot of the lane and register that hold its weight (element 2j + (k & 1) of
-        // group G = (k & 127) / 16: lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2),
-        // step 8 (k / 128) + j); every position is unique, so the 16-bit stores never collide.
-        // Each MMA step then adds its table row without a branch.  (A walk per row and token
-        // took a third of the kernel; a branch in the unrolled steps broke their scheduling.)
-        // At sixteen tokens the table holds one 128-wide block and is filled before each,
-        // every fill passing over the other block's entries.
-        for (int i = lane; i < n; i += 32) {
-          uint32_t e;
-          if (staged)
-            e = bs[i];
-          else
-            e = __ldg(bg + i);
-          const int kin = (int)((e >> 4) & 255u);
-          if (TS == 8 && (kin >> 7) != blk) continue;  // the table holds one block
-          const int row = (int)(e & 15u), kb = kin & 127;
-          uint16_t* p = reinterpret_cast<uint16_t*>(
-              &sm.otab[rt][((kin >> 7) * 8 + ((kb & 15) >> 1)) % TS][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
-          p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
-        }
-        __syncwarp();
-      }
       const uint32_t* cw = reinterpret_cast<const uint32_t*>(unit) + ((rt * 2 + blk) * 32 + lane) * 6;
       uint32_t w[6];
       {
@@ -328,7 +323,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
 #pragma unroll
         for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
         {
-          const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][(8 * blk + j) % TS][lane]);
+          const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][8 * blk + j][lane]);
           a[0] = bf16x2_add(a[0], d.x);
           a[1] = bf16x2_add(a[1], d.y);
           a[2] = bf16x2_add(a[2], d.z);
@@ -342,14 +337,11 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
           mma_bf16_4(acc[mt * 4 + 0], acc[mt * 4 + 1], acc[mt * 4 + 2], acc[mt * 4 + 3], a, b0, b1);
         }
       }
-      if ((blk * 8 + 8) % TS == 0) {  // clear this lane's table entries for the next fill
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < TS; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-      }
     }
-
+    // clear this lane's table entries for the next unit
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
