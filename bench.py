@@ -19,7 +19,9 @@ qlin_forward_host: pinned X -> device, forward, Y -> pinned host, per step), the
 of the kernel, the oracle timed on the host cores (cpu_baseline), SM clocks sampled
 during the timed region, and a few more configurations ("extra").
 
---impl reference times the oracle (numpy, host cores) on the same workload.
+--impl reference times the oracle (numpy, one host thread) on the same workload: W untimed and
+exactly K timed steps, each the oracle's forward over a slice of the layer's rows (the whole
+layer when K + W forwards fit in two minutes).
 Multi-GPU (torchrun): every rank runs an independent replica of the workload (the layer
 is row-parallel; replicas need no collective), value = all ranks' bytes / max time.
 """
@@ -145,10 +147,57 @@ def _oracle_spqr_forward_time(reps_min: int = 2, budget_s: float = 12.0):
             "host": _host_cpu()}
 
 
-def cpu_baseline_subprocess():
+def _oracle_spqr_steps(steps: int, warmup: int, budget_s: float = 120.0, N: int = N_, K: int = K_):
+    """The reference arm: the oracle's forward on the host, one thread, `warmup` untimed and
+    exactly `steps` timed steps.  The forward is separable by rows, so each step runs the
+    oracle on a slice of the layer's rows (canonical arrays of those rows -> dequant -> fp64
+    GEMV), consecutive steps on consecutive slices; the slice is the whole layer when
+    steps + warmup forwards fit in budget_s, else as many 64-row groups as do."""
+    import qlin_synth as synth
+    from oracle import forward, spqr
+    from oracle.fp import bits_to_f32
+
+    W, X = synth.spqr_layer(N, K, M_, seed=0)
+    p = spqr.pack(W, FRAC)
+    x = bits_to_f32(X)
+    rp = np.asarray(p["rowptr"])
+
+    def run(r0: int, r1: int) -> int:
+        a, b = int(rp[r0]), int(rp[r1])
+        w_hat = spqr.dequantize_canonical(r1 - r0, K, p["codes"][r0:r1], p["qs_bits"][r0:r1], p["qz_bits"][r0:r1],
+                                          p["stats"][r0:r1], rp[r0:r1 + 1] - a, p["col"][a:b], p["val"][a:b])
+        forward.reference(x, w_hat)
+        return spqr.packed_bytes(r1 - r0, K, b - a)
+
+    # size the slice from one untimed forward over an eighth of the rows
+    t0 = time.perf_counter()
+    run(0, max(64, N // 8 // 64 * 64))
+    t_full = N / max(64, N // 8 // 64 * 64) * (time.perf_counter() - t0)
+    rows = N
+    if (steps + warmup) * t_full > budget_s:
+        rows = max(64, min(N, int(N * budget_s / ((steps + warmup) * t_full)) // 64 * 64))
+
+    def step(i: int) -> int:
+        r0 = min((i * rows) % N, N - rows)
+        return run(r0, r0 + rows)
+
+    for i in range(warmup):
+        step(i)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        nbytes += step(warmup + i)
+    t = time.perf_counter() - t0
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "ms_per_step": t / steps * 1e3,
+            "sample": f"{steps} timed steps after {warmup} warm-up, each the oracle forward (canonical arrays -> "
+                      f"dequant -> fp64 GEMV) over {rows} of the {N}x{K} M=1 layer's rows, one host thread",
+            "host": _host_cpu()}
+
+
+def cpu_baseline_subprocess(extra=()):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_only"], capture_output=True, text=True,
-                       env=env, timeout=600)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle_only", *extra], capture_output=True,
+                       text=True, env=env, timeout=1200)
     if r.returncode != 0:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     return json.loads(r.stdout.strip().splitlines()[-1])
@@ -628,9 +677,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
-    r = cpu_baseline_subprocess()
+    r = cpu_baseline_subprocess(["--steps", str(args.steps), "--warmup", str(args.warmup)])
     line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r.get("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
             "config": _config(world),
             "cpu_baseline": r,
@@ -641,8 +691,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=480000)
-    ap.add_argument("--warmup", type=int, default=2400)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 480000 forwards; 20 oracle steps for --impl reference)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps, at least 3 (default 2400; 3 for --impl reference)")
     ap.add_argument("--impl", default="qlin", choices=["qlin", "reference"])
     ap.add_argument("--e2e-steps", dest="e2e_steps", type=int, default=2000)
     ap.add_argument("--no-extra", dest="no_extra", action="store_true")
@@ -654,9 +706,17 @@ def main():
                     help="time only this decode configuration, fmt,K,N,M[,outlier_frac] with fmt in "
                          "w4g128|spqr|w8a8 (for profiling), and print its line")
     args = ap.parse_args()
-    if args.oracle_only:
-        print(json.dumps(_oracle_spqr_forward_time()))
+    if args.oracle_only:  # a child process of this script: one host thread, nothing else loaded
+        if args.steps is None:
+            print(json.dumps(_oracle_spqr_forward_time()))
+        else:
+            print(json.dumps(_oracle_spqr_steps(args.steps, args.warmup)))
         return
+    reference = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 20 if reference else 480000
+    if args.warmup is None:
+        args.warmup = 3 if reference else 2400
     if args.prefill_case:
         import torch
         import quantized_weight_linear_gb300 as q

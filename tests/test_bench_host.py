@@ -1,7 +1,11 @@
 """Host-side pieces of bench.py that run without a GPU: the host description the CPU
-baseline carries (Arm and x86 /proc/cpuinfo forms)."""
+baseline carries (Arm and x86 /proc/cpuinfo forms), and the reference arm (the oracle on the
+host cores): its stepped timing and the JSON line it prints."""
+import argparse
 import builtins
 import io
+import json
+import re
 
 import bench
 
@@ -39,3 +43,46 @@ def test_host_cpu_unreadable(monkeypatch):
     monkeypatch.setattr(builtins, "open", no_file)
     h = bench._host_cpu()
     assert isinstance(h["cpu"], str) and h["cpu"]
+
+
+def test_reference_arm_times_exactly_k_steps_on_row_slices():
+    """W untimed and exactly K timed steps; when K + W whole forwards do not fit the budget,
+    each step runs the oracle on a slice of whole 64-row groups."""
+    r = bench._oracle_spqr_steps(5, 3, budget_s=0.05, N=1024, K=512)
+    m = re.match(r"5 timed steps after 3 warm-up, .* over (\d+) of the 1024x512 M=1 layer's rows", r["sample"])
+    assert m, r["sample"]
+    rows = int(m.group(1))
+    assert 64 <= rows < 1024 and rows % 64 == 0
+    assert r["value"] > 0 and r["ms_per_step"] > 0 and r["kind"] == "oracle" and r["cores"] == 1
+    r = bench._oracle_spqr_steps(2, 3, budget_s=1e6, N=1024, K=512)
+    assert "over 1024 of the 1024x512" in r["sample"]  # the whole layer when it fits
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    calls = []
+    fake = {"value": 0.04, "unit": "GB/s", "cores": 1, "kind": "oracle", "ms_per_step": 550.0, "sample": "s"}
+
+    def fake_subprocess(extra=()):
+        calls.append(list(extra))
+        return fake
+
+    monkeypatch.setattr(bench, "cpu_baseline_subprocess", fake_subprocess)
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(argparse.Namespace(steps=7, warmup=4))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert calls == [["--steps", "7", "--warmup", "4"]]
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["steps"] == 7 and line["warmup"] == 4 and line["ms_per_step"] == 550.0
+    assert line["value"] == 0.04 and line["higher_is_better"] is True and line["n_gpus"] == 1
+    assert line["cpu_baseline"] == fake
+    assert line["e2e"] == {"value": 0.04, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"] == bench._config(1)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setattr(bench, "cpu_baseline_subprocess", lambda extra=(): (_ for _ in ()).throw(AssertionError))
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    bench.run_reference(argparse.Namespace(steps=7, warmup=4))
+    assert capsys.readouterr().out == ""
