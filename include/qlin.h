@@ -48,7 +48,7 @@ typedef enum {
   QLIN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   QLIN_ERR_CUDA = 3,        /* a CUDA runtime call failed */
   QLIN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than qlin_workspace_bytes */
-  QLIN_ERR_TIMEOUT = 5,     /* a device-side wait gave up after its iteration limit */
+  QLIN_ERR_TIMEOUT = 5,     /* a device-side wait gave up after its time limit (2 s) */
   QLIN_ERR_NOT_BOUND = 6    /* forward on a handle whose weights were never bound */
 } qlin_status;
 
