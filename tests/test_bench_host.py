@@ -86,3 +86,26 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(argparse.Namespace(steps=7, warmup=4))
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_row_slice_equals_the_rows_of_the_whole_layer():
+    """The reference arm's steps rest on this: the oracle's dequantization of a row slice of
+    the canonical arrays is bit for bit the same rows of the whole layer's (rows with and
+    without outliers, a slice starting and ending mid-layer)."""
+    import numpy as np
+
+    import qlin_synth as synth
+    from oracle import spqr
+
+    N, K = 256, 1024
+    W, _ = synth.spqr_layer(N, K, 1, seed=5)
+    p = spqr.pack(W, 0.02)
+    full = spqr.dequantize_canonical(N, K, p["codes"], p["qs_bits"], p["qz_bits"], p["stats"], p["rowptr"], p["col"],
+                                     p["val"])
+    rp = np.asarray(p["rowptr"])
+    for r0, r1 in [(0, 64), (64, 192), (192, 256), (17, 18)]:
+        a, b = int(rp[r0]), int(rp[r1])
+        part = spqr.dequantize_canonical(r1 - r0, K, p["codes"][r0:r1], p["qs_bits"][r0:r1], p["qz_bits"][r0:r1],
+                                         p["stats"][r0:r1], rp[r0:r1 + 1] - a, p["col"][a:b], p["val"][a:b])
+        assert np.array_equal(part.view(np.uint32), full[r0:r1].view(np.uint32)), (r0, r1)
+    assert int(rp[-1]) > 0
