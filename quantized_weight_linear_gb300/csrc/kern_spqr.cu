@@ -14,9 +14,10 @@
 //   bf16 (base + q) with base 128 or 16 depending on the field;
 // * the A pairs are dequantized to bf16 s^ (q - z^) in registers and the MMA columns carry
 //   the tokens;
-// * outliers: each warp scatters its row tile's bucket (k < 256, row < 16, fp16 value) into a
-//   shared-memory table with one bf16 slot per (MMA step, lane, A register, half), and every
-//   MMA step adds its row of the table to the dequantized A registers.  An outlier then costs
+// * outliers: each warp keeps a shared-memory table with one bf16 slot per (MMA step, lane, A
+//   register, half), seeded with the register's -s^ z^; its row tile's bucket (k < 256,
+//   row < 16, fp16 value) is added into the slots, and every MMA step takes its row of the
+//   table as the addend of the FMA that dequantizes its A registers.  An outlier then costs
 //   the same at any token count, no two lanes ever write one slot (no atomics), and the steps
 //   carry no branch (the page's warning about the sparse part is about exactly this
 //   scattered accumulation and its divergence).
@@ -41,9 +42,10 @@ struct SpSmem {
   __align__(16) uint32_t out[kStagesSp][kOutCap + 8];
   __align__(16) uint32_t offs[kOffsCap];
   float own[kRowGroup * 4];  // M <= 4: this CTA's partial sums of the row group it owns
-  // per consumer warp, MMA step and lane, the bf16 outlier corrections of the lane's A
-  // registers (zero where there is none), all 16 steps of a unit; a step's row of 32 lanes is
-  // contiguous, so its loads are free of bank conflicts
+  // per consumer warp, MMA step and lane, the bf16 additive terms of the lane's A registers
+  // (-s^ z^ of the register's (row, group), plus the outlier where the weight has one), all 16
+  // steps of a unit; a step's row of 32 lanes is contiguous, so its loads are free of bank
+  // conflicts
   __align__(16) uint32_t otab[4][16][32][4];
   uint64_t full[kStagesSp];
   uint64_t empty[kStagesSp];
@@ -133,8 +135,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
   {
     uint32_t* xz = reinterpret_cast<uint32_t*>(&sm.x[0][0]);
     for (int i = threadIdx.x; i < kStagesSp * SpSmem<XR>::kXE / 2; i += blockDim.x) xz[i] = 0u;
-    uint32_t* oz = &sm.otab[0][0][0][0];
-    for (int i = threadIdx.x; i < (int)(sizeof(sm.otab) / 4); i += blockDim.x) oz[i] = 0u;
   }
   fence_proxy_async_smem();
   __syncthreads();
@@ -260,14 +260,40 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
     const uint32_t* bg = v.ents + b0;               // the same bucket in global memory
     const int n = (int)(b1 - b0);
 
-    // The outliers are folded into the dequantized A registers before the MMAs: entry i of
-    // the (unit, row tile) bucket writes its value, as bf16, into the table slot of the lane
-    // and register that hold its weight (element 2j + (k & 1) of group G = (k & 127) / 16:
-    // lane 4 (row & 7) + (G & 3), register (row >> 3) + 2 (G >> 2), step 8 (k / 128) + j);
-    // every position is unique, so the 16-bit stores never collide.  Each MMA step then adds
-    // its table row without a branch.  (A walk per row and token took a third of the kernel;
-    // a branch in the unrolled steps broke their scheduling; at sixteen tokens a table of one
-    // 128-wide block, filled before each block, was 6% slower on 70B-class layers.)
+    // A-side statistics of both blocks: (row g, group t), (row g+8, group t), (row g, group
+    // t+4), (row g+8, group t+4)
+    uint32_t sh2[2][4], ch2[2][4];
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = g + ((r & 1) ? 8 : 0), gb = t + ((r & 2) ? 4 : 0);
+        const uint32_t e = qsqz_entry(qarea, row, gb);
+        const float ss = (r & 1) ? ssB : ssA, zs = (r & 1) ? zsB : zsA;
+        const float sz = (r & 1) ? szB : szA, zz = (r & 1) ? zzB : zzA;
+        const float sh = __fmul_rn(__fsub_rn((float)(e & 7u), zs), ss);
+        const float zh = __fmul_rn(__fsub_rn((float)(e >> 3), zz), sz);
+        sh2[blk][r] = pack_bf16x2(sh, sh);
+        const float cz = -sh * zh;
+        ch2[blk][r] = pack_bf16x2(cz, cz);
+      }
+    }
+    // The table: every slot of this lane starts at its register's -s^ z^, and the outliers are
+    // added into it, so each MMA step dequantizes its A registers with one bf16x2 FMA whose
+    // addend is the table row: bf16((q - base) s^ + t), t = -s^ z^ or bf16(-s^ z^ + s).  Entry
+    // i of the (unit, row tile) bucket goes to the slot of the lane and register that hold
+    // its weight (element 2j + (k & 1) of group G = (k & 127) / 16: lane 4 (row & 7) + (G & 3),
+    // register (row >> 3) + 2 (G >> 2), step 8 (k / 128) + j); every position is unique, so
+    // the 16-bit read-modify-writes never collide.  (A walk per row and token took a third of
+    // the kernel; a branch in the unrolled steps broke their scheduling; at sixteen tokens a
+    // table of one 128-wide block, filled before each block, was 6% slower on 70B-class
+    // layers.)  The fill also overwrites whatever the previous unit left in the lane's slots.
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) =
+          make_uint4(ch2[q >> 3][0], ch2[q >> 3][1], ch2[q >> 3][2], ch2[q >> 3][3]);
+    __syncwarp();
     for (int i = lane; i < n; i += 32) {
       uint32_t e;
       if (staged)
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
       const int row = (int)(e & 15u), kb = kin & 127;
       uint16_t* p = reinterpret_cast<uint16_t*>(
           &sm.otab[rt][(kin >> 7) * 8 + ((kb & 15) >> 1)][4 * (row & 7) + ((kb >> 4) & 3)][(row >> 3) | ((kb >> 6) << 1)]);
-      p[kin & 1] = f2bf(h2f_dev((uint16_t)(e >> 16)));
+      p[kin & 1] = f2bf(bf2f(p[kin & 1]) + h2f_dev((uint16_t)(e >> 16)));
     }
     __syncwarp();
 #pragma unroll
@@ -290,21 +316,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
         const uint2 p1 = *reinterpret_cast<const uint2*>(cw + 2);
         const uint2 p2 = *reinterpret_cast<const uint2*>(cw + 4);
         w[0] = p0.x; w[1] = p0.y; w[2] = p1.x; w[3] = p1.y; w[4] = p2.x; w[5] = p2.y;
-      }
-      // A-side statistics: (row g, group t), (row g+8, group t), (row g, group t+4), (row g+8, group t+4)
-      const uint8_t* qarea = unit + kSpqrCodeBytes + (rt * 2 + blk) * 96;
-      uint32_t sh2[4], ch2[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int row = g + ((r & 1) ? 8 : 0), gb = t + ((r & 2) ? 4 : 0);
-        const uint32_t e = qsqz_entry(qarea, row, gb);
-        const float ss = (r & 1) ? ssB : ssA, zs = (r & 1) ? zsB : zsA;
-        const float sz = (r & 1) ? szB : szA, zz = (r & 1) ? zzB : zzA;
-        const float sh = __fmul_rn(__fsub_rn((float)(e & 7u), zs), ss);
-        const float zh = __fmul_rn(__fsub_rn((float)(e >> 3), zz), sz);
-        sh2[r] = pack_bf16x2(sh, sh);
-        const float cz = -sh * zh;
-        ch2[r] = pack_bf16x2(cz, cz);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -320,14 +331,12 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
           default: spqr_frag<7>(w, a); break;
         }
         const uint32_t base = j <= 4 ? 0x43004300u : 0x41804180u;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = bf16x2_fma(bf16x2_sub(a[r], base), sh2[r], ch2[r]);
         {
           const uint4 d = *reinterpret_cast<const uint4*>(sm.otab[rt][8 * blk + j][lane]);
-          a[0] = bf16x2_add(a[0], d.x);
-          a[1] = bf16x2_add(a[1], d.y);
-          a[2] = bf16x2_add(a[2], d.z);
-          a[3] = bf16x2_add(a[3], d.w);
+          a[0] = bf16x2_fma(bf16x2_sub(a[0], base), sh2[blk][0], d.x);
+          a[1] = bf16x2_fma(bf16x2_sub(a[1], base), sh2[blk][1], d.y);
+          a[2] = bf16x2_fma(bf16x2_sub(a[2], base), sh2[blk][2], d.z);
+          a[3] = bf16x2_fma(bf16x2_sub(a[3], base), sh2[blk][3], d.w);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -338,10 +347,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : QLIN_SP_CPS16)
         }
       }
     }
-    // clear this lane's table entries for the next unit
-    __syncwarp();
-#pragma unroll
-    for (int q = 0; q < 16; ++q) *reinterpret_cast<uint4*>(sm.otab[rt][q][lane]) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
